@@ -1,0 +1,311 @@
+/*
+ * Plain CPU oracle for the unified-precision FP8 linear layer (Jet-RL).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct
+ * statement of what the GPU path computes.  Only the test-suite, the smoke
+ * check and the CPU-baseline leg of the benchmark may load it; the product
+ * library never links, calls or falls back to it, and it shares no code,
+ * header, table or constant generator with the CUDA sources.
+ *
+ * What each part follows:
+ *   - Quantization granularities and scale type: "NVIDIA强化学习加速实操：10分钟
+ *     提升2倍训练效率" (nmedialink.com), section "为什么FP8适配线性层？", the
+ *     quantization table: weights E4M3 in [128,128] blocks, input activations
+ *     and output gradients E4M3 in [1,128] groups, FP32 block scales.
+ *   - Activations 1x128 / weights 128x128: "Jet-RL: Enabling On-Policy FP8
+ *     Reinforcement Learning with Unified Training and Rollout Precision Flow"
+ *     (gist.science), section "Quantisierungsschema".
+ *   - Backward: DGrad and WGrad GEMMs in FP8, WGrad fed by 1x128 and 128x1
+ *     groups: same page, same section, "Backward-Pass".
+ *   - Forward 1x128 activation groups re-quantized as 128x1 for the backward
+ *     pass: "英伟达破解AI训练效率难题" (163.com), section 五.
+ *   - Mismatch metric token-mult-prob-error = (1/n) sum_i exp|logp_train_i -
+ *     logp_infer_i|: nmedialink.com page, section "FP8面临的关键挑战：数值分歧".
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   E4M3 is the OCP "fn" format (bias 7, max 448, NaN 0x7F/0xFF, no inf);
+ *   encode = round to nearest, ties to the even code, saturating at +-448,
+ *   sign of zero kept; scale s = amax/448 as an IEEE binary32 division, and
+ *   s = 1 when amax = 0; codes q = E4(fl32(x / s)); the 128x1 groups are
+ *   re-quantized from the saved FP8 1x128 values v = fl32(D4(q) * s_row).
+ *
+ * Build with -O2 -fno-fast-math -ffp-contract=off so that every float
+ * operation below is one IEEE binary32/binary64 operation with
+ * round-to-nearest-even, in the order written.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* E4M3 codec                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Decode one E4M3 code from its bit fields: sign s (bit 7), exponent e
+ * (bits 6..3, bias 7), mantissa m (bits 2..0).  e == 0 is subnormal,
+ * m * 2^-9; e == 15 with m == 7 is NaN; everything else is normal,
+ * (1 + m/8) * 2^(e-7). */
+double jo_e4m3_decode(uint8_t c)
+{
+    int s = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 0x7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+static double g_dec[256];
+static int g_dec_ready = 0;
+void jo_init(void);
+
+static void dec_init(void)
+{
+    if (g_dec_ready)
+        return;
+    jo_init();
+}
+
+/* Fill the decode table; the loader calls this once before any threads. */
+void jo_init(void)
+{
+    if (g_dec_ready)
+        return;
+    for (int c = 0; c < 256; ++c)
+        g_dec[c] = jo_e4m3_decode((uint8_t)c);
+    g_dec_ready = 1;
+}
+
+/* Encode a finite binary32 value: the non-negative code 0x00..0x7E whose
+ * value is nearest to |v| (searched exhaustively, distances in binary64),
+ * ties to the code with an even bit pattern, |v| >= 448 saturating to 0x7E;
+ * then the sign bit of v is ORed in (so -0 and negative values that round to
+ * zero give 0x80). */
+uint8_t jo_e4m3_encode(float v)
+{
+    dec_init();
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0)
+        return (uint8_t)(0x7E | sign);
+    int best = 0;
+    double bestd = fabs(g_dec[0] - a);
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d = fabs(g_dec[c] - a);
+        if (d < bestd) {
+            bestd = d;
+            best = c;
+        } else if (d == bestd && (c & 1) == 0) {
+            best = c; /* exact tie between neighbours: keep the even code */
+        }
+    }
+    return (uint8_t)(best | sign);
+}
+
+/* Encode n values (same rule as jo_e4m3_encode). */
+void jo_e4m3_encode_n(const float *v, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = jo_e4m3_encode(v[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Group scale and one-group quantization                                   */
+/* ------------------------------------------------------------------------ */
+
+static float bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* s = amax / 448 (binary32 division), 1 when the group is all zero. */
+float jo_group_scale(float amax)
+{
+    if (amax == 0.0f)
+        return 1.0f;
+    return amax / 448.0f;
+}
+
+/* Quantize n values vals[0], vals[stride], ... : returns the scale and
+ * writes code i to codes[i * cstride]. */
+static float quant_group(const float *vals, int64_t stride, int64_t n,
+                         uint8_t *codes, int64_t cstride)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(vals[i * stride]);
+        if (a > amax)
+            amax = a;
+    }
+    float s = jo_group_scale(amax);
+    for (int64_t i = 0; i < n; ++i) {
+        float t = vals[i * stride] / s;
+        codes[i * cstride] = jo_e4m3_encode(t);
+    }
+    return s;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The three groupings                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* 1x128 groups along the last axis of x[M][K] (BF16 bits).
+ * q[M][K] codes; s[kb * M + m] is the scale of row m, columns
+ * 128*kb .. 128*kb+127.  Rows [m0, m1) only. */
+void jo_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, uint8_t *q,
+                        float *s, int64_t m0, int64_t m1)
+{
+    float g[128];
+    int64_t Kb = K / 128;
+    for (int64_t m = m0; m < m1; ++m)
+        for (int64_t kb = 0; kb < Kb; ++kb) {
+            for (int i = 0; i < 128; ++i)
+                g[i] = bf16_to_f32(x[m * K + kb * 128 + i]);
+            s[kb * M + m] = quant_group(g, 1, 128, q + m * K + kb * 128, 1);
+        }
+}
+
+/* 128x128 blocks of w[N][K] (BF16 bits).  q[N][K]; s[nb * Kb + kb].
+ * Block rows [nb0, nb1) only. */
+void jo_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K, uint8_t *q,
+                        float *s, int64_t nb0, int64_t nb1)
+{
+    (void)N;
+    int64_t Kb = K / 128;
+    float *g = (float *)malloc(sizeof(float) * 128 * 128);
+    uint8_t *c = (uint8_t *)malloc(128 * 128);
+    for (int64_t nb = nb0; nb < nb1; ++nb)
+        for (int64_t kb = 0; kb < Kb; ++kb) {
+            for (int r = 0; r < 128; ++r)
+                for (int i = 0; i < 128; ++i)
+                    g[r * 128 + i] =
+                        bf16_to_f32(w[(nb * 128 + r) * K + kb * 128 + i]);
+            s[nb * Kb + kb] = quant_group(g, 1, 128 * 128, c, 1);
+            for (int r = 0; r < 128; ++r)
+                memcpy(q + (nb * 128 + r) * K + kb * 128, c + r * 128, 128);
+        }
+    free(g);
+    free(c);
+}
+
+/* 128x1 re-quantization along the token axis, from the saved 1x128 form
+ * (q[M][K], s[kb * M + m]).  v[m][k] = fl32(D4(q[m][k]) * s[k/128][m]);
+ * each column k, token block mb (tokens 128*mb .. 128*mb+127) is one group.
+ * Output transposed: qT[k * M + m], sT[mb * K + k].  Columns [k0, k1). */
+void jo_requant_128x1(const uint8_t *q, const float *s, int64_t M, int64_t K,
+                      uint8_t *qT, float *sT, int64_t k0, int64_t k1)
+{
+    dec_init();
+    float g[128];
+    int64_t Mb = M / 128;
+    for (int64_t k = k0; k < k1; ++k)
+        for (int64_t mb = 0; mb < Mb; ++mb) {
+            for (int i = 0; i < 128; ++i) {
+                int64_t m = mb * 128 + i;
+                float d = (float)g_dec[q[m * K + k]];
+                g[i] = d * s[(k / 128) * M + m];
+            }
+            sT[mb * K + k] =
+                quant_group(g, 1, 128, qT + k * M + mb * 128, 1);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* GEMMs: binary64 product of the dequantized operands                       */
+/* ------------------------------------------------------------------------ */
+
+/* Row-sampled GEMM  out[r][j] = sum_c A(rows[r], c) * B(j, c), r in [r0, r1),
+ * every dequantized operand and every product and sum in binary64.
+ *   fwd   (kind 0): A = X  [M][K],  scale sx [c/128][i];
+ *                   B(j=n, c=k) = W[n][k],  scale sw [n/128][k/128].
+ *   dgrad (kind 1): A = dY [M][N],  scale sdy[c/128][i];
+ *                   B(j=k, c=n) = W[n][k],  scale sw [n/128][k/128].
+ *   wgrad (kind 2): A = dYT[N][M],  scale sdyT[c/128][i];
+ *                   B(j=k, c=m) = XT[k][m], scale sxT[m/128][k].
+ * nrows_a is the row count of A (the stride of its scale array),
+ * ncols_out the output width, depth the contraction length. */
+static double deq_a(const uint8_t *qa, const float *sa, int64_t nrows_a,
+                    int64_t depth, int64_t i, int64_t c)
+{
+    return g_dec[qa[i * depth + c]] * (double)sa[(c / 128) * nrows_a + i];
+}
+
+static double deq_b(int kind, const uint8_t *qb, const float *sb,
+                    int64_t ncols_out, int64_t depth, int64_t j, int64_t c)
+{
+    switch (kind) {
+    case 0:
+        return g_dec[qb[j * depth + c]] *
+               (double)sb[(j / 128) * (depth / 128) + c / 128];
+    case 1:
+        return g_dec[qb[c * ncols_out + j]] *
+               (double)sb[(c / 128) * (ncols_out / 128) + j / 128];
+    default:
+        return g_dec[qb[j * depth + c]] * (double)sb[(c / 128) * ncols_out + j];
+    }
+}
+
+static void gemm_rows(int kind, const uint8_t *qa, const float *sa,
+                      const uint8_t *qb, const float *sb, int64_t nrows_a,
+                      int64_t ncols_out, int64_t depth, const int64_t *rows,
+                      int64_t r0, int64_t r1, double *out)
+{
+    dec_init();
+    for (int64_t r = r0; r < r1; ++r) {
+        int64_t i = rows[r];
+        for (int64_t j = 0; j < ncols_out; ++j) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < depth; ++c)
+                acc += deq_a(qa, sa, nrows_a, depth, i, c) *
+                       deq_b(kind, qb, sb, ncols_out, depth, j, c);
+            out[r * ncols_out + j] = acc;
+        }
+    }
+}
+
+/* Y[r][n] = sum_k dq(X)[rows[r]][k] * dq(W)[n][k];  X [M][K], W [N][K]. */
+void jo_gemm_fwd(const uint8_t *qx, const float *sx, const uint8_t *qw,
+                 const float *sw, int64_t M, int64_t N, int64_t K,
+                 const int64_t *rows, int64_t r0, int64_t r1, double *y)
+{
+    gemm_rows(0, qx, sx, qw, sw, M, N, K, rows, r0, r1, y);
+}
+
+/* dX[r][k] = sum_n dq(dY)[rows[r]][n] * dq(W)[n][k];  dY [M][N]. */
+void jo_gemm_dgrad(const uint8_t *qdy, const float *sdy, const uint8_t *qw,
+                   const float *sw, int64_t M, int64_t N, int64_t K,
+                   const int64_t *rows, int64_t r0, int64_t r1, double *dx)
+{
+    gemm_rows(1, qdy, sdy, qw, sw, M, K, N, rows, r0, r1, dx);
+}
+
+/* dW[r][k] = sum_m dq(dYT)[rows[r]][m] * dq(XT)[k][m];
+ * dYT [N][M] with scales [M/128][N], XT [K][M] with scales [M/128][K]. */
+void jo_gemm_wgrad(const uint8_t *qdyT, const float *sdyT, const uint8_t *qxT,
+                   const float *sxT, int64_t M, int64_t N, int64_t K,
+                   const int64_t *rows, int64_t r0, int64_t r1, double *dw)
+{
+    gemm_rows(2, qdyT, sdyT, qxT, sxT, N, K, M, rows, r0, r1, dw);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Mismatch metric                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* (1/n) * sum_i exp(|a_i - b_i|), inputs widened to binary64. */
+double jo_token_mult_prob_error(const float *a, const float *b, int64_t n)
+{
+    double sum = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        sum += exp(fabs((double)a[i] - (double)b[i]));
+    return sum / (double)n;
+}
