@@ -1,0 +1,487 @@
+// Block-scaled FP8 GEMMs of the linear layer on the 5th-generation tensor
+// core (tcgen05), one kernel template for the three products:
+//
+//   forward  Y [M][N] = sum_kb sx[kb][m]  * sw[n/128][kb]  * (qx  . qw^T)_kb
+//   dgrad    dX[M][K] = sum_nb sdy[nb][m] * sw[nb][k/128]  * (qdy . qw)_nb
+//   wgrad    dW[N][K] = sum_mb sdyT[mb][n] * sxT[mb][k]    * (qdyT . qxT^T)_mb
+//
+// ("Jet-RL ..." gist.science summary, "Quantisierungsschema": FP8 forward,
+// DGrad and WGrad GEMMs; the scales are the FP32 per-group scales of the
+// nmedialink page's quantization table.)  Because each 128-long slice of the
+// contraction carries its own FP32 scales, the tensor core accumulates one
+// slice at a time in TMEM and the epilogue warps fold it into FP32 registers
+// with its row-scale x column-scale product.  MX block scaling (power-of-two
+// scales per 32 elements) cannot represent these scales, so it is not used.
+//
+// Kernel organisation (persistent, one CTA per SM, 384 threads = 3 warpgroups):
+//   warp 0     TMA producer: per 128-slice, one 128x128 A box and one 128xBN
+//              B box (two 128x128 boxes for dgrad) into a ring of shared
+//              memory stages with 128-byte swizzle.
+//   warp 1     allocates TMEM and issues tcgen05.mma (K = 32 per instruction,
+//              four per slice) into one of two TMEM accumulators of BN
+//              columns, then commits to the stage's "empty" and the
+//              accumulator's "full" barriers.
+//   warps 2-3  idle.  Warpgroup 0 (warps 0-3) gives registers back
+//              (setmaxnreg 56) so that the epilogue warpgroups can hold their
+//              accumulators (setmaxnreg 224): 128*56 + 256*224 = 384 * 168.
+//   warps 4-11 promotion/epilogue: two warpgroups split the tile's columns;
+//              each thread owns one output row (its TMEM lane) and BN/2 FP32
+//              accumulators, loads each slice from TMEM, applies the scales,
+//              releases the accumulator, and after the last slice writes
+//              BF16 (round to nearest even).
+// Operand majorness: A is always K-major (contraction contiguous).  B is
+// K-major for forward and wgrad; for dgrad the weight codes qw[N][K] are read
+// as they are, MN-major (the output column contiguous), so no transposed copy
+// of the weights is needed.
+// Every mbarrier wait is bounded (see jet_common.cuh); a role that gives up
+// records JET_ERR_TIMEOUT, the others stop at their next wait, in-flight
+// copies and MMAs are drained and TMEM is freed before the kernel returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "jet_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace {
+
+using namespace jet;
+using namespace jet::ptx;
+
+enum Mode { kFwd = 0, kDgrad = 1, kWgrad = 2 };
+
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsControl = 56;    // warpgroup 0 after setmaxnreg
+constexpr uint32_t kRegsEpilogue = 224;  // warpgroups 1-2 after setmaxnreg
+static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168,
+              "register split exceeds the launch allocation");
+constexpr int BM = 128;  // output rows per tile (TMEM lanes)
+constexpr int BK = 128;  // contraction slice = one scale block
+
+template <int BN>
+struct Cfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kABytes = BM * BK;
+    static constexpr int kBBytes = BN * BK;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + 1 KB alignment slack
+    static constexpr int kTmemCols = 2 * BN;                          // two accumulators
+    static constexpr int kHalf = BN / 2;                              // columns per epilogue thread
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// acc[base .. base+15] += p[j] * sc
+template <int N>
+__device__ __forceinline__ void promote16(float (&acc)[N], int base, const uint32_t (&p)[16],
+                                          float sc) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[base + j] = fmaf(__uint_as_float(p[j]), sc, acc[base + j]);
+}
+
+// acc[base .. base+15] += (p[j] * rs) * cs[j]   (per-column scales, wgrad)
+template <int N>
+__device__ __forceinline__ void promote16_cols(float (&acc)[N], int base, const uint32_t (&p)[16],
+                                               float rs, const float *__restrict__ cs) {
+    const float4 *c4 = reinterpret_cast<const float4 *>(cs);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 c = __ldg(c4 + q);
+        acc[base + 4 * q + 0] = fmaf(__uint_as_float(p[4 * q + 0]) * rs, c.x, acc[base + 4 * q + 0]);
+        acc[base + 4 * q + 1] = fmaf(__uint_as_float(p[4 * q + 1]) * rs, c.y, acc[base + 4 * q + 1]);
+        acc[base + 4 * q + 2] = fmaf(__uint_as_float(p[4 * q + 2]) * rs, c.z, acc[base + 4 * q + 2]);
+        acc[base + 4 * q + 3] = fmaf(__uint_as_float(p[4 * q + 3]) * rs, c.w, acc[base + 4 * q + 3]);
+    }
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const float *__restrict__ sa, const float *__restrict__ sb,
+                uint16_t *__restrict__ out, int R, int C, int D, unsigned *status) {
+    using CF = Cfg<BN>;
+    constexpr int S = CF::kStages;
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ uint64_t full_bar[S], empty_bar[S], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t smem_base = (smem_u32(dyn_smem) + 1023u) & ~1023u;
+    const int tiles_m = (R + BM - 1) / BM;
+    const int total = tiles_m * (C / BN);
+    const int nkb = D / BK;
+    volatile int *abort = &abort_sh;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull_bar[b], 1);
+            mbar_init(&tempty_bar[b], 8);
+        }
+        mbar_init(&drain_bar, 1);
+        abort_sh = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_sh, CF::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    // Each role is nested inside its own setmaxnreg branch so that the
+    // register limit of one branch never applies to the other.
+    if (warp < 4) {
+        reg_dealloc<kRegsControl>();
+        if (warp == 0) {
+            // ------------------------------------------------------ TMA producer
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % S;
+                    const uint32_t use = it / S;
+                    if (!mbar_wait(&empty_bar[s], (use & 1u) ^ 1u, abort, status,
+                                   SITE_GEMM_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const uint32_t a_s = smem_base + s * CF::kStageBytes;
+                        const uint32_t b_s = a_s + CF::kABytes;
+                        mbar_arrive_expect_tx(&full_bar[s], CF::kStageBytes);
+                        tma_load_2d(a_s, &tmA, &full_bar[s], kb * BK, m0);
+                        if (MODE == kDgrad) {
+    #pragma unroll
+                            for (int h = 0; h < BN / 128; ++h)
+                                tma_load_2d(b_s + h * 128 * BK, &tmB, &full_bar[s], n0 + 128 * h,
+                                            kb * BK);
+                        } else {
+                            tma_load_2d(b_s, &tmB, &full_bar[s], kb * BK, n0);
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            // Every issued load must have landed before the CTA can exit.
+            for (uint32_t j = it > (uint32_t)S ? it - S : 0u; j < it; ++j)
+                mbar_wait(&full_bar[j % S], (j / S) & 1u, nullptr, status, SITE_GEMM_DRAIN);
+        } else if (warp == 1) {
+            // ------------------------------------------------------- MMA issuer
+            constexpr uint32_t kIdesc = idesc_e4m3_f32(BM, MODE == kDgrad ? 128 : BN, MODE == kDgrad);
+            uint32_t it = 0, tc = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                for (int kb = 0; kb < nkb; ++kb, ++it, ++tc) {
+                    const int s = it % S;
+                    const uint32_t use = it / S;
+                    const int buf = tc & 1;
+                    const uint32_t tuse = tc >> 1;
+                    if (!mbar_wait(&tempty_bar[buf], (tuse & 1u) ^ 1u, abort, status,
+                                   SITE_GEMM_MMA_TMEM_EMPTY) ||
+                        !mbar_wait(&full_bar[s], use & 1u, abort, status, SITE_GEMM_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t a_s = smem_base + s * CF::kStageBytes;
+                        const uint32_t b_s = a_s + CF::kABytes;
+                        const uint32_t d = tmem + buf * BN;
+    #pragma unroll
+                        for (int ks = 0; ks < BK / 32; ++ks) {
+                            const uint64_t adesc = smem_desc(a_s + ks * 32, 16, 1024, kSwizzle128B);
+                            if (MODE == kDgrad) {
+                                // MN-major B: 8-row contraction groups 1024 B apart; each
+                                // MMA covers one 128-column swizzle atom.
+    #pragma unroll
+                                for (int h = 0; h < BN / 128; ++h) {
+                                    const uint64_t bdesc = smem_desc(
+                                        b_s + h * 128 * BK + ks * 32 * 128, 1024, 1024, kSwizzle128B);
+                                    mma_e4m3(d + h * 128, adesc, bdesc, kIdesc, ks > 0);
+                                }
+                            } else {
+                                const uint64_t bdesc = smem_desc(b_s + ks * 32, 16, 1024, kSwizzle128B);
+                                mma_e4m3(d, adesc, bdesc, kIdesc, ks > 0);
+                            }
+                        }
+                        mma_commit(&empty_bar[s]);
+                        mma_commit(&tfull_bar[buf]);
+                    }
+                    __syncwarp();
+                }
+            }
+            // All issued MMAs must complete before TMEM is released.
+            if (lane == 0) mma_commit(&drain_bar);
+            __syncwarp();
+            mbar_wait(&drain_bar, 0, nullptr, status, SITE_GEMM_DRAIN);
+        }
+    } else {
+        reg_alloc<kRegsEpilogue>();
+            // ------------------------------------------- promotion and epilogue
+            constexpr int H = CF::kHalf;
+            constexpr int NCH = H / 16;
+            const int ew = warp - 4;
+            const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+            const int ch = ew >> 2;     // column half
+            const int cb_stride = C / 128;
+            uint32_t tc = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+                const int row = m0 + quad * 32 + lane;
+                const bool row_ok = row < R;
+                const int col0 = n0 + ch * H;
+                float acc[H];
+    #pragma unroll
+                for (int i = 0; i < H; ++i) acc[i] = 0.0f;
+
+                for (int kb = 0; kb < nkb; ++kb, ++tc) {
+                    const int buf = tc & 1;
+                    const uint32_t tuse = tc >> 1;
+                    const float rs = row_ok ? __ldg(sa + (size_t)kb * R + row) : 0.0f;
+                    float cbs = 0.0f;
+                    if (MODE == kFwd) cbs = __ldg(sb + (size_t)(col0 / 128) * nkb + kb);
+                    if (MODE == kDgrad) cbs = __ldg(sb + (size_t)kb * cb_stride + col0 / 128);
+                    if (!mbar_wait(&tfull_bar[buf], tuse & 1u, abort, status,
+                                   SITE_GEMM_EPI_TMEM_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * BN + ch * H;
+                    uint32_t p0[16], p1[16];
+                    tmem_ld16(taddr, p0);
+                    if (MODE != kWgrad) {
+                        const float sc = rs * cbs;
+    #pragma unroll
+                        for (int c = 0; c < NCH; c += 2) {
+                            tmem_ld_wait(p0);
+                            tmem_ld16(taddr + (c + 1) * 16, p1);
+                            promote16(acc, c * 16, p0, sc);
+                            tmem_ld_wait(p1);
+                            if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
+                            promote16(acc, (c + 1) * 16, p1, sc);
+                        }
+                    } else {
+                        const float *cs = sb + (size_t)kb * C + col0;
+    #pragma unroll
+                        for (int c = 0; c < NCH; c += 2) {
+                            tmem_ld_wait(p0);
+                            tmem_ld16(taddr + (c + 1) * 16, p1);
+                            promote16_cols(acc, c * 16, p0, rs, cs + c * 16);
+                            tmem_ld_wait(p1);
+                            if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
+                            promote16_cols(acc, (c + 1) * 16, p1, rs, cs + (c + 1) * 16);
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                }
+                if (!ok) break;
+                if (row_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)row * C + col0);
+    #pragma unroll
+                    for (int i = 0; i < H / 8; ++i) {
+                        uint4 v;
+                        v.x = pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]);
+                        v.y = pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]);
+                        v.z = pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]);
+                        v.w = pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]);
+                        dst[i] = v;
+                    }
+                }
+            }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, CF::kTmemCols);
+    }
+}
+
+// Self-test of the bounded-wait path: waits on an mbarrier that nothing
+// arrives at, so the wait gives up after `limit_ns` and records a timeout.
+__global__ void selftest_wait_kernel(unsigned *status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    mbar_wait(&bar, 0, &abort_flag, status, SITE_TEST_NEVER_SET, limit_ns);
+}
+
+// ------------------------------------------------------------------- host --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// Row-major uint8 matrix [outer][inner] with a box of box_outer x box_inner
+// (box_inner = 128 bytes, 128-byte swizzle).
+bool make_map_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                 uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int MODE>
+jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, const uint8_t *b,
+                  const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D,
+                  cudaStream_t stream) {
+    using CF = Cfg<BN>;
+    static std::mutex mu;
+    static bool attr_set[64] = {};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev.ordinal]) {
+            if (cudaFuncSetAttribute(gemm_fp8_kernel<BN, MODE>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     CF::kSmemBytes) != cudaSuccess) {
+                cudaGetLastError();
+                return JET_ERR_CUDA;
+            }
+            attr_set[dev.ordinal] = true;
+        }
+    }
+    CUtensorMap ta, tb;
+    if (!make_map_u8(&ta, a, (uint64_t)D, (uint64_t)R, BK, BM)) return JET_ERR_CUDA;
+    bool okb = MODE == kDgrad ? make_map_u8(&tb, b, (uint64_t)C, (uint64_t)D, 128, BK)
+                              : make_map_u8(&tb, b, (uint64_t)D, (uint64_t)C, BK, BN);
+    if (!okb) return JET_ERR_CUDA;
+    const int64_t tiles = ((R + BM - 1) / BM) * (C / BN);
+    const int grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
+    gemm_fp8_kernel<BN, MODE><<<grid, kThreads, CF::kSmemBytes, stream>>>(
+        ta, tb, sa, sb, out, (int)R, (int)C, (int)D, dev.status_word);
+    return launch_status();
+}
+
+template <int MODE>
+jet_status run_gemm(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb,
+                    uint16_t *out, int64_t R, int64_t C, int64_t D, jet_stream_t s) {
+    DeviceInfo dev;
+    jet_status st = current_device(&dev);
+    if (st != JET_OK) return st;
+    cudaStream_t stream = as_stream(s);
+    if (R == 0 || C == 0) return JET_OK;
+    if (D == 0) {  // empty contraction: the product is zero
+        return cudaMemsetAsync(out, 0, (size_t)R * C * 2, stream) == cudaSuccess ? JET_OK
+                                                                               : JET_ERR_CUDA;
+    }
+    if (C % 256 == 0) return launch<256, MODE>(dev, a, sa, b, sb, out, R, C, D, stream);
+    return launch<128, MODE>(dev, a, sa, b, sb, out, R, C, D, stream);
+}
+
+constexpr int64_t kMaxDim = (int64_t)1 << 30;
+
+}  // namespace
+
+extern "C" {
+
+jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx, const uint8_t *qw,
+                            const float *sw, int64_t M, int64_t N, int64_t K, uint16_t *y,
+                            void *ws, size_t ws_bytes, jet_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    JET_REQUIRE(M >= 0 && N >= 0 && K >= 0, JET_ERR_SHAPE);
+    const bool out_empty = (M == 0 || N == 0), in_empty = out_empty || K == 0;
+    JET_REQUIRE(out_empty || y, JET_ERR_NULL);
+    JET_REQUIRE(in_empty || (qx && sx && qw && sw), JET_ERR_NULL);
+    JET_REQUIRE(N % 128 == 0 && K % 128 == 0 && M < kMaxDim && N < kMaxDim && K < kMaxDim,
+                JET_ERR_SHAPE);
+    JET_REQUIRE(aligned16(qx) && aligned16(sx) && aligned16(qw) && aligned16(sw) &&
+                    aligned16(y),
+                JET_ERR_ALIGN);
+    return run_gemm<kFwd>(qx, sx, qw, sw, y, M, N, K, stream);
+}
+
+jet_status jet_gemm_fp8_dgrad(const uint8_t *qdy, const float *sdy, const uint8_t *qw,
+                              const float *sw, int64_t M, int64_t N, int64_t K, uint16_t *dx,
+                              void *ws, size_t ws_bytes, jet_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    JET_REQUIRE(M >= 0 && N >= 0 && K >= 0, JET_ERR_SHAPE);
+    const bool out_empty = (M == 0 || K == 0), in_empty = out_empty || N == 0;
+    JET_REQUIRE(out_empty || dx, JET_ERR_NULL);
+    JET_REQUIRE(in_empty || (qdy && sdy && qw && sw), JET_ERR_NULL);
+    JET_REQUIRE(N % 128 == 0 && K % 128 == 0 && M < kMaxDim && N < kMaxDim && K < kMaxDim,
+                JET_ERR_SHAPE);
+    JET_REQUIRE(aligned16(qdy) && aligned16(sdy) && aligned16(qw) && aligned16(sw) &&
+                    aligned16(dx),
+                JET_ERR_ALIGN);
+    return run_gemm<kDgrad>(qdy, sdy, qw, sw, dx, M, K, N, stream);
+}
+
+jet_status jet_gemm_fp8_wgrad(const uint8_t *qdyT, const float *sdyT, const uint8_t *qxT,
+                              const float *sxT, int64_t M, int64_t N, int64_t K, uint16_t *dw,
+                              void *ws, size_t ws_bytes, jet_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    JET_REQUIRE(M >= 0 && N >= 0 && K >= 0, JET_ERR_SHAPE);
+    const bool out_empty = (N == 0 || K == 0), in_empty = out_empty || M == 0;
+    JET_REQUIRE(out_empty || dw, JET_ERR_NULL);
+    JET_REQUIRE(in_empty || (qdyT && sdyT && qxT && sxT), JET_ERR_NULL);
+    JET_REQUIRE(M % 128 == 0 && N % 128 == 0 && K % 128 == 0 && M < kMaxDim && N < kMaxDim &&
+                    K < kMaxDim,
+                JET_ERR_SHAPE);
+    JET_REQUIRE(aligned16(qdyT) && aligned16(sdyT) && aligned16(qxT) && aligned16(sxT) &&
+                    aligned16(dw),
+                JET_ERR_ALIGN);
+    return run_gemm<kWgrad>(qdyT, sdyT, qxT, sxT, dw, N, K, M, stream);
+}
+
+jet_status jet_selftest_bounded_wait(uint32_t limit_us, jet_stream_t stream) {
+    JET_REQUIRE(limit_us >= 1 && limit_us <= 1000000u, JET_ERR_SHAPE);
+    DeviceInfo dev;
+    jet_status st = current_device(&dev);
+    if (st != JET_OK) return st;
+    selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(dev.status_word,
+                                                          (uint64_t)limit_us * 1000ull);
+    return launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// Library-wide entry points: status strings, device checks, the device-side
+// status word and workspace sizing.
+#include <mutex>
+
+#include "jet_common.cuh"
+
+// Device-side status word: kernels record bounded-wait timeouts here.
+__device__ unsigned g_jet_status_word;
+
+namespace jet {
+
+namespace {
+constexpr int kMaxDevices = 64;
+struct Cached {
+    int state;  // 0 unknown, 1 ok, 2 wrong arch
+    int num_sms;
+    unsigned *status_word;
+};
+Cached g_cache[kMaxDevices];
+std::mutex g_mu;
+}  // namespace
+
+jet_status current_device(DeviceInfo *info) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return JET_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    Cached &c = g_cache[dev];
+    if (c.state == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return JET_ERR_DEVICE;
+        }
+        if (major != 10 || minor != 3) {
+            c.state = 2;
+        } else {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_jet_status_word) != cudaSuccess) {
+                cudaGetLastError();
+                return JET_ERR_CUDA;
+            }
+            c.num_sms = sms;
+            c.status_word = static_cast<unsigned *>(p);
+            c.state = 1;
+        }
+    }
+    if (c.state != 1) return JET_ERR_DEVICE;
+    info->ordinal = dev;
+    info->num_sms = c.num_sms;
+    info->status_word = c.status_word;
+    return JET_OK;
+}
+
+}  // namespace jet
+
+// Size of the per-block partial-sum array of the metric's first pass.
+int jet_metric_blocks(int64_t n);
+
+extern "C" {
+
+const char *jet_status_str(int status) {
+    switch (status) {
+    case JET_OK: return "JET_OK";
+    case JET_ERR_NULL: return "JET_ERR_NULL";
+    case JET_ERR_SHAPE: return "JET_ERR_SHAPE";
+    case JET_ERR_ALIGN: return "JET_ERR_ALIGN";
+    case JET_ERR_CUDA: return "JET_ERR_CUDA";
+    case JET_ERR_DEVICE: return "JET_ERR_DEVICE";
+    case JET_ERR_WORKSPACE: return "JET_ERR_WORKSPACE";
+    case JET_ERR_TIMEOUT: return "JET_ERR_TIMEOUT";
+    default: return "JET_ERR_UNKNOWN";
+    }
+}
+
+int jet_version(void) { return 10000; }
+
+size_t jet_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return 0;
+    switch (op) {
+    case JET_OP_TOKEN_MULT_PROB_ERROR:
+        return M > 0 ? (size_t)jet_metric_blocks(M) * sizeof(double) : 0;
+    default:
+        return 0;
+    }
+}
+
+jet_status jet_device_status(jet_stream_t stream, uint32_t *detail) {
+    if (detail) *detail = 0;
+    jet::DeviceInfo info;
+    jet_status st = jet::current_device(&info);
+    if (st != JET_OK) return st;
+    if (cudaStreamSynchronize(jet::as_stream(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return JET_ERR_CUDA;
+    }
+    unsigned word = 0, zero = 0;
+    if (cudaMemcpy(&word, info.status_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(info.status_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return JET_ERR_CUDA;
+    }
+    if (detail) *detail = word;
+    if (word == 0) return JET_OK;
+    return (jet_status)(word & 0xFFu);
+}
+
+}  // extern "C"

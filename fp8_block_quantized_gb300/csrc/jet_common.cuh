@@ -1,0 +1,74 @@
+// Shared host/device helpers of the jet_fp8 library (sm_103a only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/jet_fp8.h"
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+namespace jet {
+
+// Facts about the current device, cached per device ordinal.
+struct DeviceInfo {
+    int ordinal;
+    int num_sms;
+    unsigned *status_word;  // device address of the library's status word
+};
+
+// Checks that a current device exists and is sm_103; fills `info`.
+jet_status current_device(DeviceInfo *info);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline cudaStream_t as_stream(jet_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline jet_status launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? JET_OK : JET_ERR_CUDA;
+}
+
+}  // namespace jet
+
+// Early-return helpers for argument validation.
+#define JET_REQUIRE(cond, code) \
+    do {                        \
+        if (!(cond)) return (code); \
+    } while (0)
+
+// ---------------------------------------------------------------------------
+// Device side
+// ---------------------------------------------------------------------------
+
+namespace jet {
+
+// Status word layout: low byte = jet_status code, bits 8..31 = wait site.
+enum WaitSite : unsigned {
+    SITE_GEMM_PRODUCER_EMPTY = 1,
+    SITE_GEMM_MMA_FULL = 2,
+    SITE_GEMM_MMA_TMEM_EMPTY = 3,
+    SITE_GEMM_EPI_TMEM_FULL = 4,
+    SITE_GEMM_DRAIN = 5,
+    SITE_TEST_NEVER_SET = 99,
+};
+
+__device__ __forceinline__ void report_timeout(unsigned *status_word, unsigned site) {
+    // First error wins; later ones are dropped.
+    atomicCAS(status_word, 0u, (site << 8) | (unsigned)JET_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits longer than this are treated as a hang: the waiting role records a
+// timeout and abandons its work.  Healthy waits in these kernels last
+// microseconds; the limit is far above any of them.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+}  // namespace jet

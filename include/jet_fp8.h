@@ -1,0 +1,218 @@
+/*
+ * jet_fp8.h - C ABI of the GB300 (sm_103a) unified-precision FP8 linear layer.
+ *
+ * The layer is the one Jet-RL runs for both rollout and training ("Jet-RL:
+ * Enabling On-Policy FP8 Reinforcement Learning with Unified Training and
+ * Rollout Precision Flow", gist.science summary, sections "Kernarchitektur"
+ * and "Quantisierungsschema"): activations and output gradients quantized to
+ * E4M3 in 1x128 groups, weights in 128x128 blocks, each group with an FP32
+ * scale ("NVIDIA强化学习加速实操：10分钟提升2倍训练效率", nmedialink.com,
+ * section "为什么FP8适配线性层？", quantization table); forward, DGrad and WGrad
+ * GEMMs in FP8, WGrad fed by 1x128 and 128x1 groups.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates and frees nothing and keeps no pointer after a call returns.
+ *  - Tensors are dense and row-major (last index contiguous).  BF16 values are
+ *    passed as their uint16_t bit patterns; E4M3 codes as uint8_t (OCP E4M3FN:
+ *    bias 7, max 448, NaN 0x7F/0xFF).  Scales are IEEE binary32.
+ *  - Naming follows nn.Linear: X [M,K] (M tokens, K in-features), W [N,K]
+ *    (N out-features), Y = X W^T [M,N], dY [M,N], dX = dY W [M,K],
+ *    dW = dY^T X [N,K].  Kb = K/128, Nb = N/128, Mb = M/128.
+ *  - The quantization rule for every group G: amax = max |v| over G (binary32),
+ *    s = amax / 448 (IEEE binary32 division; s = 1 when amax == 0), and each
+ *    code q = E4M3(fl32(v / s)) rounded to nearest, ties to even, saturating
+ *    at +-448, sign of zero kept.  The stored scale dequantizes: v ~ q * s.
+ *  - Every call validates its arguments on the host, in this order, and returns
+ *    the first violation without launching anything: JET_ERR_NULL,
+ *    JET_ERR_SHAPE, JET_ERR_ALIGN (every pointer must be 16-byte aligned),
+ *    JET_ERR_WORKSPACE, JET_ERR_DEVICE (current device must be sm_103).
+ *    A pointer may be NULL only when its tensor is empty.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  Launch failures return JET_ERR_CUDA.  Device-side
+ *    bounded waits that give up are reported by jet_device_status().
+ *  - Non-finite inputs are outside the contract (their codes are unspecified).
+ *  - Calls are reentrant; concurrent calls must not share output buffers.
+ */
+#ifndef JET_FP8_H
+#define JET_FP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define JET_API __attribute__((visibility("default")))
+#else
+#define JET_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    JET_OK = 0,
+    JET_ERR_NULL = 1,      /* a required pointer is NULL                       */
+    JET_ERR_SHAPE = 2,     /* a size is negative or not a required multiple    */
+    JET_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned                 */
+    JET_ERR_CUDA = 4,      /* a CUDA runtime call or a kernel launch failed    */
+    JET_ERR_DEVICE = 5,    /* no current device, or it is not sm_103           */
+    JET_ERR_WORKSPACE = 6, /* workspace missing or smaller than required       */
+    JET_ERR_TIMEOUT = 7    /* a device-side bounded wait gave up (see status)  */
+} jet_status;
+
+/* Operation ids for jet_workspace_bytes(). */
+typedef enum {
+    JET_OP_QUANT_ACT_1X128 = 0,
+    JET_OP_QUANT_W_128X128 = 1,
+    JET_OP_REQUANT_128X1 = 2,
+    JET_OP_GEMM_FWD = 3,
+    JET_OP_GEMM_DGRAD = 4,
+    JET_OP_GEMM_WGRAD = 5,
+    JET_OP_TOKEN_MULT_PROB_ERROR = 6
+} jet_op;
+
+/* A cudaStream_t handle passed as an opaque pointer. */
+typedef void *jet_stream_t;
+
+/* Static, NUL-terminated name of a status code ("JET_OK", ...). */
+JET_API const char *jet_status_str(int status);
+
+/* ABI version (major * 10000 + minor * 100 + patch). */
+JET_API int jet_version(void);
+
+/*
+ * 1x128 quantization of activations or output gradients.
+ * Source: nmedialink.com page, section "为什么FP8适配线性层？" (input activations
+ * and output gradients: E4M3, [1,128], FP32 scales); gist.science summary,
+ * "Quantisierungsschema" (activations 1x128).  Used for X before the forward
+ * GEMM and for dY (with K := N) before the DGrad GEMM.
+ *   x  [M][K] BF16 bits (in).       M >= 0, K >= 0 and K % 128 == 0.
+ *   q  [M][K] E4M3 codes (out).
+ *   s  [Kb][M] FP32 scales (out): s[kb*M + m] belongs to row m, columns
+ *      128*kb .. 128*kb+127 (K-block-major so a GEMM tile's row scales are
+ *      contiguous).
+ */
+JET_API jet_status jet_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K,
+                               uint8_t *q, float *s, jet_stream_t stream);
+
+/*
+ * 128x128 block quantization of weights (run once per weight sync).
+ * Source: nmedialink.com page, quantization table (weights: E4M3, [128,128],
+ * FP32); gist.science summary, "Quantisierungsschema" (weights 128x128).
+ *   w  [N][K] BF16 bits (in).       N, K >= 0, both multiples of 128.
+ *   q  [N][K] E4M3 codes (out).
+ *   s  [Nb][Kb] FP32 scales (out), s[nb*Kb + kb].
+ */
+JET_API jet_status jet_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K,
+                               uint8_t *q, float *s, jet_stream_t stream);
+
+/*
+ * 128x1 re-quantization along the token axis, fused with the transpose that
+ * the WGrad GEMM needs.  Source: 163.com article, section 五 (1x128 forward
+ * groups re-quantized as 128x1 in backward); gist.science summary,
+ * "Quantisierungsschema" (WGrad with 1x128 and 128x1 groups).  The input is
+ * the saved FP8 form: v[m][k] = fl32(D4(q[m][k]) * s[k/128][m]); each group is
+ * tokens 128*mb .. 128*mb+127 of one column k.
+ *   q   [M][K] E4M3 codes, s [Kb][M] scales (in; the jet_quant_act_1x128 form).
+ *   qT  [K][M] E4M3 codes (out), transposed.   M, K >= 0, multiples of 128.
+ *   sT  [Mb][K] FP32 scales (out), sT[mb*K + k].
+ */
+JET_API jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M,
+                             int64_t K, uint8_t *qT, float *sT,
+                             jet_stream_t stream);
+
+/*
+ * Forward GEMM  Y = X W^T  with per-128-K-block scale promotion:
+ *   Y[m][n] = sum_kb sx[kb][m] * sw[n/128][kb] * sum_{k in kb} qx[m][k] qw[n][k]
+ * accumulated in FP32 and written as BF16 (round to nearest even).
+ * Source: gist.science summary, "Quantisierungsschema" (FP8 GEMMs of linear
+ * layers); 163.com article, section 五 (1x128 inputs times 128x128 weights).
+ *   qx [M][K], sx [Kb][M] (jet_quant_act_1x128 of X);  M >= 0.
+ *   qw [N][K], sw [Nb][Kb] (jet_quant_w_128x128 of W); N, K multiples of 128.
+ *   y  [M][N] BF16 bits (out).  K == 0 writes zeros.
+ *   ws / ws_bytes: workspace, at least jet_workspace_bytes(JET_OP_GEMM_FWD, ...)
+ *   bytes (NULL/0 allowed when that is 0).
+ */
+JET_API jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx,
+                            const uint8_t *qw, const float *sw, int64_t M,
+                            int64_t N, int64_t K, uint16_t *y, void *ws,
+                            size_t ws_bytes, jet_stream_t stream);
+
+/*
+ * DGrad GEMM  dX = dY W :
+ *   dX[m][k] = sum_nb sdy[nb][m] * sw[nb][k/128] * sum_{n in nb} qdy[m][n] qw[n][k]
+ * FP32 accumulation, BF16 out.  Source: gist.science summary,
+ * "Quantisierungsschema", "Backward-Pass" (DGrad in FP8).
+ *   qdy [M][N], sdy [Nb][M] (jet_quant_act_1x128 of dY with K := N).
+ *   qw  [N][K], sw [Nb][Kb] (the forward weight codes, read transposed).
+ *   dx  [M][K] BF16 bits (out).  N == 0 writes zeros.
+ */
+JET_API jet_status jet_gemm_fp8_dgrad(const uint8_t *qdy, const float *sdy,
+                              const uint8_t *qw, const float *sw, int64_t M,
+                              int64_t N, int64_t K, uint16_t *dx, void *ws,
+                              size_t ws_bytes, jet_stream_t stream);
+
+/*
+ * WGrad GEMM  dW = dY^T X  on the 128x1 (token-axis) groups:
+ *   dW[n][k] = sum_mb sdyT[mb][n] * sxT[mb][k] * sum_{m in mb} qdyT[n][m] qxT[k][m]
+ * FP32 accumulation, BF16 out.  Source: gist.science summary,
+ * "Quantisierungsschema", "Backward-Pass" (WGrad in FP8 with 1x128 and 128x1).
+ *   qdyT [N][M], sdyT [Mb][N]  (jet_requant_128x1 of dY's 1x128 form).
+ *   qxT  [K][M], sxT  [Mb][K]  (jet_requant_128x1 of X's 1x128 form).
+ *   dw   [N][K] BF16 bits (out).  M % 128 == 0; M == 0 writes zeros.
+ */
+JET_API jet_status jet_gemm_fp8_wgrad(const uint8_t *qdyT, const float *sdyT,
+                              const uint8_t *qxT, const float *sxT, int64_t M,
+                              int64_t N, int64_t K, uint16_t *dw, void *ws,
+                              size_t ws_bytes, jet_stream_t stream);
+
+/*
+ * Train/rollout mismatch metric
+ *   token-mult-prob-error = (1/n) * sum_i exp(|logp_train[i] - logp_rollout[i]|)
+ * Source: nmedialink.com page, section "FP8面临的关键挑战：数值分歧".  No mask:
+ * every one of the n tokens counts.  Per-thread sums in FP32, across threads
+ * and blocks in FP64 (fixed order, deterministic); result written as FP32.
+ *   logp_train, logp_rollout [n] FP32 (in), n >= 1.
+ *   out: one FP32 in device memory (out).
+ *   ws / ws_bytes: at least jet_workspace_bytes(JET_OP_TOKEN_MULT_PROB_ERROR,
+ *   n, 0, 0) bytes of device memory (per-block FP64 partial sums).
+ */
+JET_API jet_status jet_token_mult_prob_error(const float *logp_train,
+                                     const float *logp_rollout, int64_t n,
+                                     float *out, void *ws, size_t ws_bytes,
+                                     jet_stream_t stream);
+
+/*
+ * Workspace bytes an operation needs for the given sizes (0 if none).
+ * For JET_OP_TOKEN_MULT_PROB_ERROR pass n as M.  Returns 0 for negative sizes
+ * or an unknown op.  Pure host function; needs no device.
+ */
+JET_API size_t jet_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device-side status word of
+ * the current device.  Returns JET_OK, JET_ERR_TIMEOUT (a bounded wait inside
+ * a kernel gave up; the kernel skipped its remaining work and released its
+ * resources, so the context stays usable) or JET_ERR_CUDA (the synchronize
+ * itself failed).  If `detail` is not NULL it receives the raw status word
+ * (0 when clean; otherwise the code in the low byte and the wait site above).
+ */
+JET_API jet_status jet_device_status(jet_stream_t stream, uint32_t *detail);
+
+/*
+ * Self-test of the failure path every pipelined kernel uses: launches one
+ * block that waits on a barrier nothing completes, with a limit of
+ * `limit_us` microseconds (1 .. 1,000,000).  The wait gives up, records
+ * JET_ERR_TIMEOUT in the device status word and the kernel returns, so a
+ * following jet_device_status() reports JET_ERR_TIMEOUT and the context stays
+ * usable.  The pages have no counterpart; it exists to test the bounded waits.
+ */
+JET_API jet_status jet_selftest_bounded_wait(uint32_t limit_us, jet_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JET_FP8_H */

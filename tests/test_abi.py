@@ -1,0 +1,141 @@
+"""The C-ABI library builds, loads and exports every symbol of include/jet_fp8.h,
+and its host-side argument checks return the documented codes (CPU only: no
+call here reaches a kernel launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp8_block_quantized_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "jet_fp8.h")
+
+OK, NULL, SHAPE, ALIGN, CUDA, DEVICE, WORKSPACE, TIMEOUT = range(8)
+V = ctypes.c_void_p
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"JET_API\s+[\w\s\*]*?\b(jet_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return binding.load()
+
+
+def fake(addr):
+    """A non-dereferenced stand-in pointer (argument checks fail before any use)."""
+    return V(addr)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) >= set(binding.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS.items():
+        assert lib.jet_status_str(code).decode() == name
+    assert lib.jet_status_str(99).decode() == "JET_ERR_UNKNOWN"
+    assert lib.jet_version() >= 10000
+
+
+def test_workspace_bytes(lib):
+    op = binding.OP
+    for name in ("quant_act_1x128", "quant_w_128x128", "requant_128x1",
+                 "gemm_fp8_fwd", "gemm_fp8_dgrad", "gemm_fp8_wgrad"):
+        assert lib.jet_workspace_bytes(op[name], 8192, 4096, 4096) == 0
+    m = op["token_mult_prob_error"]
+    assert lib.jet_workspace_bytes(m, 1, 0, 0) == 8
+    assert lib.jet_workspace_bytes(m, 2048, 0, 0) == 8
+    assert lib.jet_workspace_bytes(m, 2049, 0, 0) == 16
+    assert lib.jet_workspace_bytes(m, 4 * 1024 * 1024, 0, 0) == 1024 * 8
+    assert lib.jet_workspace_bytes(m, 0, 0, 0) == 0
+    assert lib.jet_workspace_bytes(m, -5, 0, 0) == 0
+    assert lib.jet_workspace_bytes(42, 1, 1, 1) == 0
+
+
+A = 0x10000  # 16-byte aligned stand-ins
+B = 0x20000
+C = 0x30000
+D = 0x40000
+MIS = 0x10008  # 8-byte aligned only
+
+
+def test_quant_act_checks(lib):
+    f = lib.jet_quant_act_1x128
+    assert f(None, 4, 128, fake(B), fake(C), None) == NULL
+    assert f(fake(A), 4, 128, None, fake(C), None) == NULL
+    assert f(fake(A), 4, 128, fake(B), None, None) == NULL
+    assert f(fake(A), -1, 128, fake(B), fake(C), None) == SHAPE
+    assert f(fake(A), 4, 100, fake(B), fake(C), None) == SHAPE
+    assert f(fake(MIS), 4, 128, fake(B), fake(C), None) == ALIGN
+    assert f(fake(A), 4, 128, fake(B), fake(MIS), None) == ALIGN
+
+
+def test_quant_w_and_requant_checks(lib):
+    w = lib.jet_quant_w_128x128
+    assert w(None, 128, 128, fake(B), fake(C), None) == NULL
+    assert w(fake(A), 100, 128, fake(B), fake(C), None) == SHAPE
+    assert w(fake(A), 128, 129, fake(B), fake(C), None) == SHAPE
+    assert w(fake(A), 128, 128, fake(MIS), fake(C), None) == ALIGN
+    r = lib.jet_requant_128x1
+    assert r(fake(A), None, 128, 128, fake(C), fake(D), None) == NULL
+    assert r(fake(A), fake(B), 100, 128, fake(C), fake(D), None) == SHAPE   # M % 128
+    assert r(fake(A), fake(B), 128, 100, fake(C), fake(D), None) == SHAPE
+    assert r(fake(A), fake(B), 128, 128, fake(C), fake(MIS), None) == ALIGN
+
+
+@pytest.mark.parametrize("name", ["jet_gemm_fp8_fwd", "jet_gemm_fp8_dgrad", "jet_gemm_fp8_wgrad"])
+def test_gemm_checks(lib, name):
+    f = getattr(lib, name)
+    args = [fake(A), fake(B), fake(C), fake(D)]
+    assert f(*args, 128, 128, 128, None, None, 0, None) == NULL          # no output
+    assert f(None, fake(B), fake(C), fake(D), 128, 128, 128, fake(A), None, 0, None) == NULL
+    assert f(*args, -1, 128, 128, fake(A), None, 0, None) == SHAPE
+    assert f(*args, 128, 100, 128, fake(A), None, 0, None) == SHAPE
+    assert f(*args, 128, 128, 100, fake(A), None, 0, None) == SHAPE
+    assert f(*args, 128, 128, 128, fake(MIS), None, 0, None) == ALIGN
+    assert f(fake(MIS), fake(B), fake(C), fake(D), 128, 128, 128, fake(A), None, 0, None) == ALIGN
+    if name == "jet_gemm_fp8_wgrad":      # the token axis must hold whole 128-groups
+        assert f(*args, 100, 128, 128, fake(A), None, 0, None) == SHAPE
+
+
+def test_metric_checks(lib):
+    f = lib.jet_token_mult_prob_error
+    assert f(None, fake(B), 16, fake(C), fake(D), 8, None) == NULL
+    assert f(fake(A), fake(B), 0, fake(C), fake(D), 8, None) == SHAPE
+    assert f(fake(A), fake(B), 16, fake(MIS), fake(D), 8, None) == ALIGN
+    assert f(fake(A), fake(B), 16, fake(C), None, 0, None) == WORKSPACE
+    assert f(fake(A), fake(B), 4096, fake(C), fake(D), 8, None) == WORKSPACE  # needs 16
+
+
+def test_selftest_limit_checks(lib):
+    assert lib.jet_selftest_bounded_wait(0, None) == SHAPE
+    assert lib.jet_selftest_bounded_wait(2_000_000, None) == SHAPE
+
+
+def test_no_device_is_reported():
+    """Valid arguments on a machine without a GPU stop at the device check."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this checks the no-device path")
+    lib = binding.load()
+    assert lib.jet_quant_act_1x128(fake(A), 4, 128, fake(B), fake(C), None) == DEVICE
+    assert lib.jet_gemm_fp8_fwd(fake(A), fake(B), fake(C), fake(D), 128, 128, 128,
+                                fake(A), None, 0, None) == DEVICE
+    assert lib.jet_device_status(None, None) == DEVICE
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    """No silent fallback: a missing library raises instead of computing elsewhere."""
+    monkeypatch.setattr(binding._build, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(ImportError):
+        binding.load(build_if_missing=False)

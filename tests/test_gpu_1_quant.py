@@ -1,0 +1,157 @@
+"""GPU parity of the three quantizers against the CPU oracle: codes and scales
+bit-exact, called through the C ABI.  Inputs are the seeded workloads (and
+edge cases); the oracle quantizes the same host copy.  Large inputs are checked
+on sampled row / block-row / column-block slices, which the oracle computes
+independently because groups never straddle them."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_quantized_gb300 import workloads as wl
+from tests.gpu_util import assert_codes_equal, assert_scales_equal, bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def jet(torch_cuda):
+    import fp8_block_quantized_gb300 as j
+    j.load()
+    return j
+
+
+def check_act(jet, x_cpu, rows=None):
+    q, s = jet.quant_act_1x128(x_cpu.cuda())
+    torch.cuda.synchronize()
+    xb = bits(x_cpu)
+    if rows is None:
+        q_ref, s_ref = oracle.quant_act_1x128(xb)
+        assert_codes_equal(q, q_ref)
+        assert_scales_equal(s, s_ref)
+    else:
+        q_ref, s_ref = oracle.quant_act_1x128(xb[rows])
+        assert_codes_equal(q[torch.as_tensor(rows).cuda()], q_ref)
+        assert_scales_equal(s[:, torch.as_tensor(rows).cuda()], s_ref)
+
+
+def test_act_single_linear(jet):
+    c = wl.single_linear()
+    check_act(jet, c.x)
+    check_act(jet, c.dy)
+
+
+@pytest.mark.parametrize("M", [1, 16, 17, 64, 65, 256, 2048])
+@pytest.mark.parametrize("K", [128, 4096, 14336])
+def test_act_rollout_shapes(jet, M, K):
+    check_act(jet, wl.activations(M, K, seed=M + K, config=2))
+
+
+def test_act_edge_values(jet):
+    M, K = 70, 384
+    x = torch.zeros((M, K), dtype=torch.float32)
+    x[1] = 3.3895e38                                     # BF16 max
+    x[2, :128] = torch.linspace(-1e-38, 1e-38, 128)      # subnormal range
+    x[3] = -0.0
+    x[4, :] = 448.0
+    x[4, 7] = 17.0                                       # ties
+    x[5] = torch.arange(K) * (2.0 ** -10)
+    x[6] = -torch.arange(K).float()
+    TAB = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float()
+    codes = torch.randint(0, 0x7F, (K,), generator=torch.Generator().manual_seed(1))
+    x[7] = TAB[codes] * torch.where(torch.arange(K) % 3 == 0, -1.0, 1.0)
+    x[7, ::128] = 448.0                                  # representable, scale 1
+    x[8:] = torch.randn((M - 8, K), generator=torch.Generator().manual_seed(2)) * 1e-3
+    check_act(jet, x.to(torch.bfloat16))
+
+
+def test_act_empty(jet):
+    q, s = jet.quant_act_1x128(torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"))
+    assert q.shape == (0, 256) and s.shape == (2, 0)
+
+
+def test_act_train8b_full_sampled_rows(jet):
+    x = wl.activations(8192, 14336, seed=0, config=3, tensor_id=3)
+    rows = np.sort(np.random.default_rng(0).choice(8192, 1024, replace=False))
+    rows[-1] = 8191
+    check_act(jet, x, rows)
+
+
+def test_act_heavy_tailed_gradients(jet):
+    dy = wl.grad_output(8192, 1024, seed=0, config=3, tensor_id=201)
+    check_act(jet, dy)
+
+
+def check_w(jet, w_cpu, block_rows=None):
+    q, s = jet.quant_w_128x128(w_cpu.cuda())
+    torch.cuda.synchronize()
+    wb = bits(w_cpu)
+    if block_rows is None:
+        q_ref, s_ref = oracle.quant_w_128x128(wb)
+        assert_codes_equal(q, q_ref)
+        assert_scales_equal(s, s_ref)
+    else:
+        for nb in block_rows:
+            sl = slice(nb * 128, (nb + 1) * 128)
+            q_ref, s_ref = oracle.quant_w_128x128(wb[sl])
+            assert_codes_equal(q[sl], q_ref)
+            assert_scales_equal(s[nb:nb + 1], s_ref)
+
+
+def test_w_single_linear(jet):
+    check_w(jet, wl.single_linear().w)
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (1024, 4096), (4096, 14336), (384, 640)])
+def test_w_shapes(jet, N, K):
+    check_w(jet, wl.weights(N, K, seed=N ^ K, config=5))
+
+
+def test_w_gate_sampled_block_rows(jet):
+    check_w(jet, wl.weights(14336, 4096, seed=0, config=5, tensor_id=104), [0, 5, 57, 111])
+
+
+def test_w_identity_and_zero(jet):
+    w = torch.zeros((256, 256))
+    w[:128, :128] = torch.eye(128) * 448.0
+    check_w(jet, w.to(torch.bfloat16))
+
+
+def check_requant(jet, x_cpu, kblocks=None):
+    q_ref, s_ref = oracle.quant_act_1x128(bits(x_cpu))
+    M, K = q_ref.shape
+    qT, sT = jet.requant_128x1(to_dev(q_ref), to_dev(s_ref))
+    torch.cuda.synchronize()
+    if kblocks is None:
+        qT_ref, sT_ref = oracle.requant_128x1(q_ref, s_ref)
+        assert_codes_equal(qT, qT_ref)
+        assert_scales_equal(sT, sT_ref)
+    else:
+        for kb in kblocks:
+            sl = slice(kb * 128, (kb + 1) * 128)
+            qT_ref, sT_ref = oracle.requant_128x1(np.ascontiguousarray(q_ref[:, sl]),
+                                                  np.ascontiguousarray(s_ref[kb:kb + 1]))
+            assert_codes_equal(qT[sl], qT_ref)
+            assert_scales_equal(sT[:, sl], sT_ref)
+
+
+def test_requant_single_linear(jet):
+    c = wl.single_linear()
+    check_requant(jet, c.x)
+    check_requant(jet, c.dy)
+
+
+@pytest.mark.parametrize("M,K", [(128, 128), (384, 256), (1024, 1024)])
+def test_requant_shapes(jet, M, K):
+    check_requant(jet, wl.activations(M, K, seed=M * 7 + K, config=3, zero_group=True))
+
+
+def test_requant_gradients_train8b_sampled(jet):
+    dy = wl.grad_output(8192, 4096, seed=0, config=3, tensor_id=200)
+    check_requant(jet, dy, kblocks=[0, 13, 31])
+
+
+def test_requant_empty(jet):
+    qT, sT = jet.requant_128x1(torch.empty((0, 128), dtype=torch.uint8, device="cuda"),
+                               torch.empty((1, 0), dtype=torch.float32, device="cuda"))
+    assert qT.shape == (128, 0) and sT.shape == (0, 128)

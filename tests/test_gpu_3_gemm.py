@@ -1,0 +1,168 @@
+"""GPU parity of the forward, DGrad and WGrad FP8 GEMMs against the oracle's
+FP64 product of the same dequantized operands:
+
+    |Y - ref| <= 2^-7 |ref| + 1e-3 * rms(ref row)   elementwise
+
+The operands are the oracle's own quantization of the seeded workloads, copied
+to the device, so each GEMM is checked on exactly the codes and scales the
+oracle used.  Full-size shapes are checked on sampled output rows (the oracle
+computes those rows one by one); small shapes on every element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_quantized_gb300 import workloads as wl
+from tests.gpu_util import assert_gemm_close, bits, host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def jet(torch_cuda):
+    import fp8_block_quantized_gb300 as j
+    j.load()
+    return j
+
+
+def quant_pair(x, w):
+    qx, sx = oracle.quant_act_1x128(bits(x))
+    qw, sw = oracle.quant_w_128x128(bits(w))
+    return qx, sx, qw, sw
+
+
+def sample_rows(n, k, seed=0):
+    if n <= k:
+        return None
+    r = np.sort(np.random.default_rng(seed).choice(n, k, replace=False))
+    r[0], r[-1] = 0, n - 1
+    return np.unique(r)
+
+
+def run_fwd(jet, x, w, nrows=None):
+    qx, sx, qw, sw = quant_pair(x, w)
+    y = jet.gemm_fp8_fwd(to_dev(qx), to_dev(sx), to_dev(qw), to_dev(sw))
+    torch.cuda.synchronize()
+    rows = sample_rows(qx.shape[0], nrows) if nrows else None
+    ref = oracle.gemm_fwd(qx, sx, qw, sw, rows=rows)
+    assert_gemm_close(y if rows is None else y[torch.as_tensor(rows).cuda()], ref, "fwd")
+    return y
+
+
+def run_dgrad(jet, dy, w, nrows=None):
+    qdy, sdy = oracle.quant_act_1x128(bits(dy))
+    qw, sw = oracle.quant_w_128x128(bits(w))
+    dx = jet.gemm_fp8_dgrad(to_dev(qdy), to_dev(sdy), to_dev(qw), to_dev(sw))
+    torch.cuda.synchronize()
+    rows = sample_rows(qdy.shape[0], nrows) if nrows else None
+    ref = oracle.gemm_dgrad(qdy, sdy, qw, sw, rows=rows)
+    assert_gemm_close(dx if rows is None else dx[torch.as_tensor(rows).cuda()], ref, "dgrad")
+    return dx
+
+
+def run_wgrad(jet, dy, x, nrows=None):
+    qx, sx = oracle.quant_act_1x128(bits(x))
+    qdy, sdy = oracle.quant_act_1x128(bits(dy))
+    qxT, sxT = oracle.requant_128x1(qx, sx)
+    qdyT, sdyT = oracle.requant_128x1(qdy, sdy)
+    dw = jet.gemm_fp8_wgrad(to_dev(qdyT), to_dev(sdyT), to_dev(qxT), to_dev(sxT))
+    torch.cuda.synchronize()
+    rows = sample_rows(qdyT.shape[0], nrows) if nrows else None
+    ref = oracle.gemm_wgrad(qdyT, sdyT, qxT, sxT, rows=rows)
+    assert_gemm_close(dw if rows is None else dw[torch.as_tensor(rows).cuda()], ref, "wgrad")
+    return dw
+
+
+# ----------------------------------------------------------- small, exact --
+
+def test_fwd_single_tile(jet):
+    run_fwd(jet, wl.activations(128, 128, seed=1, config=1), wl.weights(256, 128, seed=1, config=1))
+
+
+def test_fwd_single_linear(jet):
+    c = wl.single_linear()
+    run_fwd(jet, c.x, c.w)
+
+
+def test_dgrad_single_linear(jet):
+    c = wl.single_linear()
+    run_dgrad(jet, c.dy, c.w)
+
+
+def test_wgrad_single_linear(jet):
+    c = wl.single_linear()
+    run_wgrad(jet, c.dy, c.x)
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 100, 129, 256])
+@pytest.mark.parametrize("N", [1024, 384, 128])
+def test_fwd_ragged_rows_and_widths(jet, M, N):
+    run_fwd(jet, wl.activations(M, 512, seed=M, config=2), wl.weights(N, 512, seed=N, config=2))
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 256, 384), (128, 128, 256), (256, 512, 128)])
+def test_dgrad_shapes(jet, M, N, K):
+    run_dgrad(jet, wl.grad_output(M, N, seed=M + N, config=3),
+              wl.weights(N, K, seed=K, config=3))
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 384), (384, 128, 256), (256, 512, 512)])
+def test_wgrad_shapes(jet, M, N, K):
+    run_wgrad(jet, wl.grad_output(M, N, seed=M + N, config=3),
+              wl.activations(M, K, seed=K, config=3))
+
+
+def test_zero_rows_are_exact_zero(jet):
+    x = wl.activations(256, 384, seed=5, config=1).float()
+    x[3] = 0.0
+    x[200] = 0.0
+    y = run_fwd(jet, x.to(torch.bfloat16), wl.weights(256, 384, seed=5, config=1))
+    assert (host(y[3].float()) == 0).all() and (host(y[200].float()) == 0).all()
+
+
+def test_empty_contraction_writes_zeros(jet):
+    e8 = torch.empty((64, 0), dtype=torch.uint8, device="cuda")
+    s = torch.empty((0, 64), dtype=torch.float32, device="cuda")
+    w8 = torch.empty((256, 0), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((2, 0), dtype=torch.float32, device="cuda")
+    y = torch.full((64, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    jet.jet_gemm_fp8_fwd(e8, s, w8, sw, y)
+    assert (y == 0).all()
+
+
+def test_deterministic(jet):
+    x, w = wl.activations(512, 1024, seed=9, config=2), wl.weights(1024, 1024, seed=9, config=2)
+    qx, sx, qw, sw = (to_dev(a) for a in quant_pair(x, w))
+    y1 = jet.gemm_fp8_fwd(qx, sx, qw, sw)
+    y2 = jet.gemm_fp8_fwd(qx, sx, qw, sw)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+# ----------------------------------------------- persistent, full shapes --
+
+def test_fwd_persistent_many_tiles(jet):
+    # 32 x 8 = 256 tiles > SM count: CTAs loop over several tiles
+    run_fwd(jet, wl.activations(4096, 1024, seed=2, config=2), wl.weights(2048, 1024, seed=2, config=2),
+            nrows=48)
+
+
+@pytest.mark.parametrize("name,N,K", [("kv", 1024, 4096), ("down", 4096, 14336)])
+@pytest.mark.parametrize("M", [1, 64, 2048])
+def test_fwd_rollout_shapes(jet, name, N, K, M):
+    run_fwd(jet, wl.activations(M, K, seed=M, config=2), wl.weights(N, K, seed=N, config=2),
+            nrows=24)
+
+
+def test_train8b_q_proj_fwd_dgrad_wgrad(jet):
+    layer = wl.training_layer("train8b")
+    q = layer[0]
+    assert (q.name, q.M, q.N, q.K) == ("q", 8192, 4096, 4096)
+    run_fwd(jet, q.x, q.w, nrows=24)
+    run_dgrad(jet, q.dy, q.w, nrows=24)
+    run_wgrad(jet, q.dy, q.x, nrows=16)
+
+
+def test_train32b_kv_proj_wgrad(jet):
+    M, N, K = 16384, 1024, 5120
+    run_wgrad(jet, wl.grad_output(M, N, seed=0, config=4, tensor_id=201),
+              wl.activations(M, K, seed=0, config=4), nrows=8)
