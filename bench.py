@@ -1,0 +1,507 @@
+#!/usr/bin/env python3
+"""Benchmark of the unified-precision FP8 linear layer on GB300.
+
+One step = one pass of the whole hot path over one training layer of the
+8B-shaped model (7 linears q,k,v,o,gate,up,down at M = 8192 tokens; or the
+32B-shaped layer at M = 16384 with --workload train32b):
+
+  weight sync   128x128 quantization of the 7 BF16 master weights
+  forward       1x128 quantization of the 4 distinct inputs, 7 forward GEMMs
+  backward      1x128 quantization of the 7 output gradients, 7 DGrad GEMMs,
+                128x1 re-quantization of the 4 inputs and 7 gradients,
+                7 WGrad GEMMs
+  metric        token-mult-prob-error over the step's M tokens
+
+Inputs are synthetic (seeded, resident in HBM before timing).  The step's
+working set (~1.5 GB for train8b) is far larger than the 129 MB L2, so
+consecutive steps do not hit in L2; no extra flush is done.
+
+Printed JSON (rank 0): value = GEMM FLOPs of the step / step time (TFLOP/s,
+quantization and metric time included); per-kernel rates with CUDA events
+recorded on the launch stream inside the timed region; a roofline for the
+dominant kernel; the end-to-end rate through the same C-ABI calls with pinned
+host buffers copied in and results copied out every step; the CPU oracle
+timed on a bounded sample on the host cores.
+
+--impl reference times that CPU oracle as the reference arm (on a bounded
+sample per step, see cpu_sample_step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 linear fwd+dgrad+wgrad TFLOP/s & % FP8 peak; quantize GB/s & % HBM"
+FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PFLOP/s)
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# Algorithmic bytes per element / token (what the method must move).
+BYTES_PER_ELEM = {
+    "quant_act_1x128": 2 + 1 + 4 / 128,          # BF16 in, code out, one scale per 128
+    "quant_w_128x128": 2 + 1 + 4 / (128 * 128),
+    "requant_128x1": 1 + 1 + 4 / 128 + 4 / 128,  # code in/out, row scales in, col scales out
+    "token_mult_prob_error": 8,                  # two FP32 per token
+}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in getattr(self, "lines", []):
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# the GPU step
+# --------------------------------------------------------------------------
+
+class LayerStep:
+    """Preallocated buffers and the ordered C-ABI calls of one layer step."""
+
+    def __init__(self, kind: str, device, seed: int = 0):
+        import torch
+        from fp8_block_quantized_gb300 import workloads as wl
+        import fp8_block_quantized_gb300 as jet
+
+        self.jet = jet
+        self.kind = kind
+        self.cases = wl.training_layer(kind, seed=seed, device=device)
+        self.M = self.cases[0].M
+        M = self.M
+        dev = device
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        # distinct inputs
+        self.inputs = {}
+        for c in self.cases:
+            key = wl.SHARED_INPUT[c.name]
+            if key not in self.inputs:
+                self.inputs[key] = {"x": c.x, "K": c.K,
+                                    "q": e((M, c.K), u8), "s": e((c.K // 128, M), f32),
+                                    "qT": e((c.K, M), u8), "sT": e((M // 128, c.K), f32)}
+            c.key = key
+        self.lin = []
+        for c in self.cases:
+            N, K = c.N, c.K
+            self.lin.append({
+                "case": c, "w": c.w, "dy": c.dy,
+                "qw": e((N, K), u8), "sw": e((N // 128, K // 128), f32),
+                "y": e((M, N), bf),
+                "qdy": e((M, N), u8), "sdy": e((N // 128, M), f32),
+                "dx": e((M, K), bf),
+                "qdyT": e((N, M), u8), "sdyT": e((M // 128, N), f32),
+                "dw": e((N, K), bf),
+            })
+        self.logp_train, self.logp_rollout = (t.to(dev) for t in wl.logprobs(M, seed=seed))
+        self.metric_out = e((1,), f32)
+        nb = max(jet.workspace_bytes("token_mult_prob_error", M), 16)
+        self.metric_ws = e((nb,), u8)
+        self.flops = sum(3 * 2 * M * c.N * c.K for c in self.cases)
+        # algorithmic work per kernel family per step
+        self.work = {"gemm_fp8_fwd": sum(2 * M * c.N * c.K for c in self.cases),
+                     "gemm_fp8_dgrad": sum(2 * M * c.N * c.K for c in self.cases),
+                     "gemm_fp8_wgrad": sum(2 * M * c.N * c.K for c in self.cases),
+                     "quant_w_128x128": sum(c.N * c.K for c in self.cases) * BYTES_PER_ELEM["quant_w_128x128"],
+                     "quant_act_1x128": (sum(M * v["K"] for v in self.inputs.values())
+                                         + sum(M * c.N for c in self.cases)) * BYTES_PER_ELEM["quant_act_1x128"],
+                     "requant_128x1": (sum(M * v["K"] for v in self.inputs.values())
+                                       + sum(M * c.N for c in self.cases)) * BYTES_PER_ELEM["requant_128x1"],
+                     "token_mult_prob_error": M * BYTES_PER_ELEM["token_mult_prob_error"]}
+        # per linear: weight quant, fwd, dY quant, dgrad, dY requant, wgrad;
+        # per distinct input: quant, requant; the metric: two passes
+        self.launches_per_step = len(self.lin) * 6 + len(self.inputs) * 2 + 2
+
+    def calls(self):
+        """The step as (family, thunk) pairs in launch order."""
+        j = self.jet
+        out = []
+        for L in self.lin:
+            out.append(("quant_w_128x128", lambda L=L: j.jet_quant_w_128x128(L["w"], L["qw"], L["sw"])))
+        for v in self.inputs.values():
+            out.append(("quant_act_1x128", lambda v=v: j.jet_quant_act_1x128(v["x"], v["q"], v["s"])))
+        for L in self.lin:
+            v = self.inputs[L["case"].key]
+            out.append(("gemm_fp8_fwd", lambda L=L, v=v: j.jet_gemm_fp8_fwd(v["q"], v["s"], L["qw"], L["sw"], L["y"])))
+        for L in self.lin:
+            out.append(("quant_act_1x128", lambda L=L: j.jet_quant_act_1x128(L["dy"], L["qdy"], L["sdy"])))
+            out.append(("gemm_fp8_dgrad", lambda L=L: j.jet_gemm_fp8_dgrad(L["qdy"], L["sdy"], L["qw"], L["sw"], L["dx"])))
+            out.append(("requant_128x1", lambda L=L: j.jet_requant_128x1(L["qdy"], L["sdy"], L["qdyT"], L["sdyT"])))
+        for v in self.inputs.values():
+            out.append(("requant_128x1", lambda v=v: j.jet_requant_128x1(v["q"], v["s"], v["qT"], v["sT"])))
+        for L in self.lin:
+            v = self.inputs[L["case"].key]
+            out.append(("gemm_fp8_wgrad", lambda L=L, v=v: j.jet_gemm_fp8_wgrad(L["qdyT"], L["sdyT"], v["qT"], v["sT"], L["dw"])))
+        out.append(("token_mult_prob_error", lambda: j.jet_token_mult_prob_error(
+            self.logp_train, self.logp_rollout, self.metric_out, self.metric_ws)))
+        return out
+
+    def host_io(self):
+        """Pinned host copies of the step's inputs and buffers for its results."""
+        import torch
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        self.h_in = [(pin(v["x"]), v["x"]) for v in self.inputs.values()]
+        self.h_in += [(pin(L["w"]), L["w"]) for L in self.lin]
+        self.h_in += [(pin(L["dy"]), L["dy"]) for L in self.lin]
+        self.h_in += [(pin(self.logp_train), self.logp_train), (pin(self.logp_rollout), self.logp_rollout)]
+        outs = [self.metric_out] + [L[k] for L in self.lin for k in ("y", "dx", "dw")]
+        self.h_out = [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t) for t in outs]
+        nbytes = lambda pairs: sum(h.numel() * h.element_size() for h, _ in pairs)
+        return nbytes(self.h_in), nbytes(self.h_out)
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    import fp8_block_quantized_gb300 as jet
+    jet.load()
+
+    step = LayerStep(args.workload, device, seed=args.seed + rank)
+    calls = step.calls()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        for _, f in calls:
+            f()
+    code, word = jet.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} ({word:#x}) after warm-up")
+
+    # ---- timed region: K steps, per-kernel CUDA events on the launch stream
+    fam_ms = {}
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for k in range(args.steps):
+            for (fam, f), (a, b) in zip(calls, ev[k]):
+                a.record(stream)
+                f()
+                b.record(stream)
+        t1.record(stream)
+        barrier()
+    total_ms = t0.elapsed_time(t1)
+    for k in range(args.steps):
+        for (fam, _), (a, b) in zip(calls, ev[k]):
+            fam_ms[fam] = fam_ms.get(fam, 0.0) + a.elapsed_time(b)
+    code, word = jet.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} ({word:#x}) after timing")
+    if world > 1:
+        tt = torch.tensor([total_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * step.flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs in, results out, through the same calls
+    e2e = None
+    if not args.no_e2e:
+        h2d, d2h = step.host_io()
+
+        def e2e_step():
+            for h, d in step.h_in:
+                d.copy_(h, non_blocking=True)
+            for _, f in calls:
+                f()
+            for h, d in step.h_out:
+                h.copy_(d, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(1, min(args.steps, 5))
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1) / e2e_steps
+        if world > 1:
+            tt = torch.tensor([e_ms], device=device)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": round(world * step.flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    pk, pk_kind = peaks()
+    hbm = float(pk.get("hbm_gbs", FALLBACK["hbm_gbs"]))
+    fp8_burst = FP8_OVER_BF16 * float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
+    fp8_sust = FP8_OVER_BF16 * float(pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
+    kernels = {}
+    launches = {}
+    for fam, _ in calls:
+        launches[fam] = launches.get(fam, 0) + 1
+    for fam, ms in fam_ms.items():
+        avg_ms = ms / args.steps
+        w = step.work[fam]
+        if fam.startswith("gemm"):
+            rate = w / (avg_ms * 1e-3) / 1e12
+            kernels[fam] = {"ms_per_step": round(avg_ms, 4), "launches_per_step": launches[fam],
+                            "TFLOP/s": round(rate, 1), "frac_fp8_peak": round(rate / fp8_sust, 4)}
+        else:
+            rate = w / (avg_ms * 1e-3) / 1e9
+            kernels[fam] = {"ms_per_step": round(avg_ms, 4), "launches_per_step": launches[fam],
+                            "GB/s": round(rate, 1), "frac_hbm": round(rate / hbm, 4)}
+    dom = max(fam_ms, key=fam_ms.get)
+    dom_ms_launch = fam_ms[dom] / (args.steps * launches[dom])
+    dom_work_launch = step.work[dom] / launches[dom]
+    if dom.startswith("gemm"):
+        ach = dom_work_launch / (dom_ms_launch * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_sust, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp8_sust, 4),
+                "peak_note": f"dense FP8 = {FP8_OVER_BF16:g} x {pk_kind} sustained cuBLAS BF16 "
+                             f"(burst {fp8_burst:.0f})"}
+    else:
+        ach = dom_work_launch / (dom_ms_launch * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "peak_note": f"{pk_kind} copy bandwidth"}
+    roof["traffic"] = measured_traffic(dom, args.workload)
+    quant_fams = [f for f in fam_ms if not f.startswith("gemm") and f != "token_mult_prob_error"]
+    q_bytes = sum(step.work[f] for f in quant_fams)
+    q_ms = sum(fam_ms[f] for f in quant_fams) / args.steps
+    gemm_ms = sum(fam_ms[f] for f in fam_ms if f.startswith("gemm")) / args.steps
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}_layer_M{step.M}", "tokens": step.M,
+                   "linears": [(c.name, c.N, c.K) for c in step.cases],
+                   "gemm_tflop_per_step": round(step.flops / 1e12, 4),
+                   "l2": "no flush: per-step working set > 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "gemm_only": {"TFLOP/s": round(step.flops / (gemm_ms * 1e-3) / 1e12, 1),
+                      "frac_fp8_peak": round(step.flops / (gemm_ms * 1e-3) / 1e12 / fp8_sust, 4)},
+        "quantize": {"GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+                     "frac_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / hbm, 4)},
+        "kernels": kernels,
+        "roofline": roof,
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, seconds=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the
+    current kernel source; otherwise null."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(workload, {}).get(kernel)
+        if not ent:
+            return None
+        src = os.path.join(ROOT, "fp8_block_quantized_gb300", "csrc", ent["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != ent["source_sha256_16"]:
+                return None
+        return ent["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------
+# CPU oracle: baseline and reference arm
+# --------------------------------------------------------------------------
+
+def cpu_sample_inputs(workload: str, seed: int = 0, tokens: int = 128):
+    """First `tokens` rows of the workload's q-projection chain (host copies)."""
+    from fp8_block_quantized_gb300 import workloads as wl
+    name, N, K = wl.layer_linears(workload)[0]
+    cfg = wl.CONFIG_ID[workload]
+    x = wl.activations(tokens, K, seed=seed, config=cfg, tensor_id=0)
+    w = wl.weights(N, K, seed=seed, config=cfg, tensor_id=100)
+    dy = wl.grad_output(tokens, N, seed=seed, config=cfg, tensor_id=200)
+    return (wl.bf16_bits(x), wl.bf16_bits(w), wl.bf16_bits(dy)), 3 * 2 * tokens * N * K
+
+
+def cpu_sample_step(sample, nthreads):
+    """The oracle's pass over the sample: weight sync, forward, backward."""
+    import oracle
+    xb, wb, dyb = sample
+    qw, sw = oracle.quant_w_128x128(wb, nthreads=nthreads)
+    qx, sx = oracle.quant_act_1x128(xb, nthreads=nthreads)
+    oracle.gemm_fwd(qx, sx, qw, sw, nthreads=nthreads)
+    qdy, sdy = oracle.quant_act_1x128(dyb, nthreads=nthreads)
+    oracle.gemm_dgrad(qdy, sdy, qw, sw, nthreads=nthreads)
+    qxT, sxT = oracle.requant_128x1(qx, sx, nthreads=nthreads)
+    qdyT, sdyT = oracle.requant_128x1(qdy, sdy, nthreads=nthreads)
+    oracle.gemm_wgrad(qdyT, sdyT, qxT, sxT, nthreads=nthreads)
+
+
+def cpu_baseline(workload: str, seconds: float = 12.0):
+    import oracle
+    oracle.build()
+    nthreads = os.cpu_count() or 1
+    sample, flops = cpu_sample_inputs(workload)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        cpu_sample_step(sample, nthreads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 50:
+            break
+    from fp8_block_quantized_gb300 import workloads as wl
+    name, N, K = wl.layer_linears(workload)[0]
+    return {"value": round(reps * flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": nthreads,
+            "kind": "oracle", "seconds": round(el, 2), "reps": reps,
+            "sample": f"{name} projection chain (N={N}, K={K}) at 128 tokens: 128x128 weight "
+                      f"quantization, 1x128 of X and dY, 128x1 requant of both, binary64 "
+                      f"forward/dgrad/wgrad; {reps} passes"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    nthreads = os.cpu_count() or 1
+    sample, flops = cpu_sample_inputs(args.workload)
+    for _ in range(args.warmup):
+        cpu_sample_step(sample, nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_sample_step(sample, nthreads)
+    el = time.perf_counter() - t0
+    value = args.steps * flops / el / 1e12
+    from fp8_block_quantized_gb300 import workloads as wl
+    name, N, K = wl.layer_linears(args.workload)[0]
+    sample_desc = (f"{name} projection chain (N={N}, K={K}) at 128 tokens per step: the oracle's "
+                   f"weight quantization, 1x128/128x1 quantization and binary64 GEMMs")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}_layer (CPU sample)", "tokens": 128},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": nthreads,
+                             "kind": "oracle", "sample": sample_desc},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("jet", "reference"), default="jet")
+    ap.add_argument("--workload", choices=("train8b", "train32b"), default="train8b")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # timing rule: at least 3 warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
