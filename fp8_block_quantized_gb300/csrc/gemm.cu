@@ -167,7 +167,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         mbar_arrive_expect_tx(&full_bar[s], CF::kStageBytes);
                         tma_load_2d(a_s, &tmA, &full_bar[s], kb * BK, m0);
                         if (MODE == kDgrad) {
-    #pragma unroll
+#pragma unroll
                             for (int h = 0; h < BN / 128; ++h)
                                 tma_load_2d(b_s + h * 128 * BK, &tmB, &full_bar[s], n0 + 128 * h,
                                             kb * BK);
@@ -203,13 +203,13 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         const uint32_t a_s = smem_base + s * CF::kStageBytes;
                         const uint32_t b_s = a_s + CF::kABytes;
                         const uint32_t d = tmem + buf * BN;
-    #pragma unroll
+#pragma unroll
                         for (int ks = 0; ks < BK / 32; ++ks) {
                             const uint64_t adesc = smem_desc(a_s + ks * 32, 16, 1024, kSwizzle128B);
                             if (MODE == kDgrad) {
                                 // MN-major B: 8-row contraction groups 1024 B apart; each
                                 // MMA covers one 128-column swizzle atom.
-    #pragma unroll
+#pragma unroll
                                 for (int h = 0; h < BN / 128; ++h) {
                                     const uint64_t bdesc = smem_desc(
                                         b_s + h * 128 * BK + ks * 32 * 128, 1024, 1024, kSwizzle128B);
@@ -233,81 +233,81 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
     } else {
         reg_alloc<kRegsEpilogue>();
-            // ------------------------------------------- promotion and epilogue
-            constexpr int H = CF::kHalf;
-            constexpr int NCH = H / 16;
-            const int ew = warp - 4;
-            const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
-            const int ch = ew >> 2;     // column half
-            const int cb_stride = C / 128;
-            uint32_t tc = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
-                const int row = m0 + quad * 32 + lane;
-                const bool row_ok = row < R;
-                const int col0 = n0 + ch * H;
-                float acc[H];
-    #pragma unroll
-                for (int i = 0; i < H; ++i) acc[i] = 0.0f;
+        // ------------------------------------------- promotion and epilogue
+        constexpr int H = CF::kHalf;
+        constexpr int NCH = H / 16;
+        const int ew = warp - 4;
+        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        const int ch = ew >> 2;     // column half
+        const int cb_stride = C / 128;
+        uint32_t tc = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+            const int row = m0 + quad * 32 + lane;
+            const bool row_ok = row < R;
+            const int col0 = n0 + ch * H;
+            float acc[H];
+#pragma unroll
+            for (int i = 0; i < H; ++i) acc[i] = 0.0f;
 
-                for (int kb = 0; kb < nkb; ++kb, ++tc) {
-                    const int buf = tc & 1;
-                    const uint32_t tuse = tc >> 1;
-                    const float rs = row_ok ? __ldg(sa + (size_t)kb * R + row) : 0.0f;
-                    float cbs = 0.0f;
-                    if (MODE == kFwd) cbs = __ldg(sb + (size_t)(col0 / 128) * nkb + kb);
-                    if (MODE == kDgrad) cbs = __ldg(sb + (size_t)kb * cb_stride + col0 / 128);
-                    if (!mbar_wait(&tfull_bar[buf], tuse & 1u, abort, status,
-                                   SITE_GEMM_EPI_TMEM_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * BN + ch * H;
-                    uint32_t p0[16], p1[16];
-                    tmem_ld16(taddr, p0);
-                    if (MODE != kWgrad) {
-                        const float sc = rs * cbs;
-    #pragma unroll
-                        for (int c = 0; c < NCH; c += 2) {
-                            tmem_ld_wait(p0);
-                            tmem_ld16(taddr + (c + 1) * 16, p1);
-                            promote16(acc, c * 16, p0, sc);
-                            tmem_ld_wait(p1);
-                            if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
-                            promote16(acc, (c + 1) * 16, p1, sc);
-                        }
-                    } else {
-                        const float *cs = sb + (size_t)kb * C + col0;
-    #pragma unroll
-                        for (int c = 0; c < NCH; c += 2) {
-                            tmem_ld_wait(p0);
-                            tmem_ld16(taddr + (c + 1) * 16, p1);
-                            promote16_cols(acc, c * 16, p0, rs, cs + c * 16);
-                            tmem_ld_wait(p1);
-                            if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
-                            promote16_cols(acc, (c + 1) * 16, p1, rs, cs + (c + 1) * 16);
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+            for (int kb = 0; kb < nkb; ++kb, ++tc) {
+                const int buf = tc & 1;
+                const uint32_t tuse = tc >> 1;
+                const float rs = row_ok ? __ldg(sa + (size_t)kb * R + row) : 0.0f;
+                float cbs = 0.0f;
+                if (MODE == kFwd) cbs = __ldg(sb + (size_t)(col0 / 128) * nkb + kb);
+                if (MODE == kDgrad) cbs = __ldg(sb + (size_t)kb * cb_stride + col0 / 128);
+                if (!mbar_wait(&tfull_bar[buf], tuse & 1u, abort, status,
+                               SITE_GEMM_EPI_TMEM_FULL)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
-                if (row_ok) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)row * C + col0);
-    #pragma unroll
-                    for (int i = 0; i < H / 8; ++i) {
-                        uint4 v;
-                        v.x = pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]);
-                        v.y = pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]);
-                        v.z = pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]);
-                        v.w = pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]);
-                        dst[i] = v;
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * BN + ch * H;
+                uint32_t p0[16], p1[16];
+                tmem_ld16(taddr, p0);
+                if (MODE != kWgrad) {
+                    const float sc = rs * cbs;
+#pragma unroll
+                    for (int c = 0; c < NCH; c += 2) {
+                        tmem_ld_wait(p0);
+                        tmem_ld16(taddr + (c + 1) * 16, p1);
+                        promote16(acc, c * 16, p0, sc);
+                        tmem_ld_wait(p1);
+                        if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
+                        promote16(acc, (c + 1) * 16, p1, sc);
                     }
+                } else {
+                    const float *cs = sb + (size_t)kb * C + col0;
+#pragma unroll
+                    for (int c = 0; c < NCH; c += 2) {
+                        tmem_ld_wait(p0);
+                        tmem_ld16(taddr + (c + 1) * 16, p1);
+                        promote16_cols(acc, c * 16, p0, rs, cs + c * 16);
+                        tmem_ld_wait(p1);
+                        if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
+                        promote16_cols(acc, (c + 1) * 16, p1, rs, cs + (c + 1) * 16);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+            }
+            if (!ok) break;
+            if (row_ok) {
+                uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)row * C + col0);
+#pragma unroll
+                for (int i = 0; i < H / 8; ++i) {
+                    uint4 v;
+                    v.x = pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]);
+                    v.y = pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]);
+                    v.z = pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]);
+                    v.w = pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]);
+                    dst[i] = v;
                 }
             }
+        }
     }
 
     tc_fence_before();
