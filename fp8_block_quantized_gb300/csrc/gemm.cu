@@ -16,14 +16,17 @@
 // Kernel organisation (persistent, one CTA per SM, 384 threads = 3 warpgroups):
 //   warp 0     TMA producer: per 128-slice, one 128x128 A box and one 128xBN
 //              B box (two 128x128 boxes for dgrad) into a ring of shared
-//              memory stages with 128-byte swizzle.
+//              memory stages with 128-byte swizzle, and the slice's FP32
+//              scales (128 row scales, the column scales) into an 8-slot
+//              ring by cp.async, so promotion never waits on global memory.
 //   warp 1     allocates TMEM and issues tcgen05.mma (K = 32 per instruction,
 //              four per slice) into one of two TMEM accumulators of BN
 //              columns, then commits to the stage's "empty" and the
 //              accumulator's "full" barriers.
 //   warps 2-3  idle.  Warpgroup 0 (warps 0-3) gives registers back
-//              (setmaxnreg 56) so that the epilogue warpgroups can hold their
-//              accumulators (setmaxnreg 224): 128*56 + 256*224 = 384 * 168.
+//              (setmaxnreg 72) so that the epilogue warpgroups can hold their
+//              accumulators (setmaxnreg 200): 128*72 + 256*200 <= 384 * 168,
+//              the allocation the block is launched with.
 //   warps 4-11 promotion/epilogue: two warpgroups split the tile's columns;
 //              each thread owns one output row (its TMEM lane) and BN/2 FP32
 //              accumulators, loads each slice from TMEM, applies the scales,
@@ -52,8 +55,8 @@ using namespace jet::ptx;
 enum Mode { kFwd = 0, kDgrad = 1, kWgrad = 2 };
 
 constexpr int kThreads = 384;
-constexpr uint32_t kRegsControl = 56;    // warpgroup 0 after setmaxnreg
-constexpr uint32_t kRegsEpilogue = 224;  // warpgroups 1-2 after setmaxnreg
+constexpr uint32_t kRegsControl = 72;    // warpgroup 0 after setmaxnreg
+constexpr uint32_t kRegsEpilogue = 200;  // warpgroups 1-2 after setmaxnreg
 static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr int BM = 128;  // output rows per tile (TMEM lanes)
@@ -65,10 +68,43 @@ struct Cfg {
     static constexpr int kABytes = BM * BK;
     static constexpr int kBBytes = BN * BK;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + 1 KB alignment slack
-    static constexpr int kTmemCols = 2 * BN;                          // two accumulators
-    static constexpr int kHalf = BN / 2;                              // columns per epilogue thread
+    // Scale ring: per slice, the tile's 128 row scales and its column scales
+    // (BN per-column values for wgrad, BN/128 block values otherwise).
+    static constexpr int kScaleSlots = 8;
+    static constexpr int kScaleRowBytes = BM * 4;
+    static constexpr int kScaleSlotBytes = kScaleRowBytes + BN * 4;
+    static constexpr int kSmemBytes =
+        kStages * kStageBytes + kScaleSlots * kScaleSlotBytes + 1024;  // + alignment slack
+    static constexpr int kTmemCols = 2 * BN;                           // two accumulators
+    static constexpr int kHalf = BN / 2;  // columns per epilogue thread
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
+
+// Tile order: 0 = column tiles fastest (B stays in L2, A read once),
+// 1 = row tiles fastest (A stays in L2), 2 = groups of `gm` row tiles, column
+// tiles fastest inside a group (A group stays in L2, B re-read per group).
+struct Raster {
+    int mode;
+    int gm;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, Raster r, int &mt,
+                                            int &nt) {
+    if (r.mode == 0) {
+        mt = t / tiles_n;
+        nt = t - mt * tiles_n;
+    } else if (r.mode == 1) {
+        nt = t / tiles_m;
+        mt = t - nt * tiles_m;
+    } else {
+        const int per_group = r.gm * tiles_n;
+        const int g = t / per_group;
+        const int within = t - g * per_group;
+        const int rows = min(r.gm, tiles_m - g * r.gm);
+        nt = within / rows;
+        mt = g * r.gm + (within - nt * rows);
+    }
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -80,21 +116,25 @@ template <int N>
 __device__ __forceinline__ void promote16(float (&acc)[N], int base, const uint32_t (&p)[16],
                                           float sc) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[base + j] = fmaf(__uint_as_float(p[j]), sc, acc[base + j]);
+    for (int j = 0; j < 16; j += 2)
+        ffma2(acc[base + j], acc[base + j + 1], __uint_as_float(p[j]), __uint_as_float(p[j + 1]),
+              sc, sc);
 }
 
-// acc[base .. base+15] += (p[j] * rs) * cs[j]   (per-column scales, wgrad)
+// acc[base .. base+15] += (p[j] * rs) * cs[j]   (per-column scales, wgrad);
+// cs points to shared memory.
 template <int N>
 __device__ __forceinline__ void promote16_cols(float (&acc)[N], int base, const uint32_t (&p)[16],
-                                               float rs, const float *__restrict__ cs) {
+                                               float rs, const float *cs) {
     const float4 *c4 = reinterpret_cast<const float4 *>(cs);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float4 c = __ldg(c4 + q);
-        acc[base + 4 * q + 0] = fmaf(__uint_as_float(p[4 * q + 0]) * rs, c.x, acc[base + 4 * q + 0]);
-        acc[base + 4 * q + 1] = fmaf(__uint_as_float(p[4 * q + 1]) * rs, c.y, acc[base + 4 * q + 1]);
-        acc[base + 4 * q + 2] = fmaf(__uint_as_float(p[4 * q + 2]) * rs, c.z, acc[base + 4 * q + 2]);
-        acc[base + 4 * q + 3] = fmaf(__uint_as_float(p[4 * q + 3]) * rs, c.w, acc[base + 4 * q + 3]);
+        const float4 c = c4[q];
+        float t0, t1, t2, t3;
+        fmul2(t0, t1, __uint_as_float(p[4 * q + 0]), __uint_as_float(p[4 * q + 1]), rs, rs);
+        fmul2(t2, t3, __uint_as_float(p[4 * q + 2]), __uint_as_float(p[4 * q + 3]), rs, rs);
+        ffma2(acc[base + 4 * q + 0], acc[base + 4 * q + 1], t0, t1, c.x, c.y);
+        ffma2(acc[base + 4 * q + 2], acc[base + 4 * q + 3], t2, t3, c.z, c.w);
     }
 }
 
@@ -102,18 +142,23 @@ template <int BN, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const float *__restrict__ sa, const float *__restrict__ sb,
-                uint16_t *__restrict__ out, int R, int C, int D, unsigned *status) {
+                uint16_t *__restrict__ out, int R, int C, int D, Raster raster,
+                unsigned *status) {
     using CF = Cfg<BN>;
     constexpr int S = CF::kStages;
+    constexpr int SS = CF::kScaleSlots;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ uint64_t full_bar[S], empty_bar[S], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint64_t sfull_bar[SS], sempty_bar[SS];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t smem_base = (smem_u32(dyn_smem) + 1023u) & ~1023u;
+    const uint32_t scale_base = smem_base + S * CF::kStageBytes;
     const int tiles_m = (R + BM - 1) / BM;
-    const int total = tiles_m * (C / BN);
+    const int tiles_n = C / BN;
+    const int total = tiles_m * tiles_n;
     const int nkb = D / BK;
     volatile int *abort = &abort_sh;
 
@@ -121,6 +166,10 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         for (int s = 0; s < S; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
+        }
+        for (int s = 0; s < SS; ++s) {
+            mbar_init(&sfull_bar[s], 32);  // one cp.async arrival per producer lane
+            mbar_init(&sempty_bar[s], 8);  // one arrival per epilogue warp
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull_bar[b], 1);
@@ -148,19 +197,47 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (warp < 4) {
         reg_dealloc<kRegsControl>();
         if (warp == 0) {
-            // ------------------------------------------------------ TMA producer
+            // -------------------------------------------------- TMA producer
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+                int mt, nt;
+                tile_coords(t, tiles_m, tiles_n, raster, mt, nt);
+                const int m0 = mt * BM, n0 = nt * BN;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
+                    const int ss = it % SS;
+                    const uint32_t suse = it / SS;
                     if (!mbar_wait(&empty_bar[s], (use & 1u) ^ 1u, abort, status,
+                                   SITE_GEMM_PRODUCER_EMPTY) ||
+                        !mbar_wait(&sempty_bar[ss], (suse & 1u) ^ 1u, abort, status,
                                    SITE_GEMM_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
+                    // Scales of this slice -> scale slot ss (all 32 lanes).
+                    const uint32_t slot = scale_base + ss * CF::kScaleSlotBytes;
+                    const float *srow = sa + (size_t)kb * R;
+#pragma unroll
+                    for (int j = 0; j < BM / 32; ++j) {
+                        const int r = m0 + lane + 32 * j;
+                        cp_async4(slot + (lane + 32 * j) * 4, srow + (r < R ? r : R - 1),
+                                  r < R ? 4u : 0u);
+                    }
+                    const uint32_t scol = slot + CF::kScaleRowBytes;
+                    if (MODE == kWgrad) {
+                        const float *src = sb + (size_t)kb * C + n0;
+#pragma unroll
+                        for (int j = 0; j < BN / 128; ++j)
+                            cp_async16(scol + (lane + 32 * j) * 16, src + 4 * (lane + 32 * j));
+                    } else if (lane < BN / 128) {
+                        const float *src = MODE == kFwd
+                                               ? sb + (size_t)(n0 / 128 + lane) * nkb + kb
+                                               : sb + (size_t)kb * (C / 128) + n0 / 128 + lane;
+                        cp_async4(scol + lane * 4, src, 4u);
+                    }
+                    cp_async_arrive_noinc(&sfull_bar[ss]);
                     if (lane == 0) {
                         const uint32_t a_s = smem_base + s * CF::kStageBytes;
                         const uint32_t b_s = a_s + CF::kABytes;
@@ -181,17 +258,20 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // Every issued load must have landed before the CTA can exit.
             for (uint32_t j = it > (uint32_t)S ? it - S : 0u; j < it; ++j)
                 mbar_wait(&full_bar[j % S], (j / S) & 1u, nullptr, status, SITE_GEMM_DRAIN);
+            for (uint32_t j = it > (uint32_t)SS ? it - SS : 0u; j < it; ++j)
+                mbar_wait(&sfull_bar[j % SS], (j / SS) & 1u, nullptr, status, SITE_GEMM_DRAIN);
         } else if (warp == 1) {
-            // ------------------------------------------------------- MMA issuer
-            constexpr uint32_t kIdesc = idesc_e4m3_f32(BM, MODE == kDgrad ? 128 : BN, MODE == kDgrad);
-            uint32_t it = 0, tc = 0;
+            // --------------------------------------------------- MMA issuer
+            constexpr uint32_t kIdesc =
+                idesc_e4m3_f32(BM, MODE == kDgrad ? 128 : BN, MODE == kDgrad);
+            uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                for (int kb = 0; kb < nkb; ++kb, ++it, ++tc) {
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
-                    const int buf = tc & 1;
-                    const uint32_t tuse = tc >> 1;
+                    const int buf = it & 1;
+                    const uint32_t tuse = it >> 1;
                     if (!mbar_wait(&tempty_bar[buf], (tuse & 1u) ^ 1u, abort, status,
                                    SITE_GEMM_MMA_TMEM_EMPTY) ||
                         !mbar_wait(&full_bar[s], use & 1u, abort, status, SITE_GEMM_MMA_FULL)) {
@@ -207,16 +287,18 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         for (int ks = 0; ks < BK / 32; ++ks) {
                             const uint64_t adesc = smem_desc(a_s + ks * 32, 16, 1024, kSwizzle128B);
                             if (MODE == kDgrad) {
-                                // MN-major B: 8-row contraction groups 1024 B apart; each
-                                // MMA covers one 128-column swizzle atom.
+                                // MN-major B: 8-row contraction groups 1024 B apart;
+                                // each MMA covers one 128-column swizzle atom.
 #pragma unroll
                                 for (int h = 0; h < BN / 128; ++h) {
-                                    const uint64_t bdesc = smem_desc(
-                                        b_s + h * 128 * BK + ks * 32 * 128, 1024, 1024, kSwizzle128B);
+                                    const uint64_t bdesc =
+                                        smem_desc(b_s + h * 128 * BK + ks * 32 * 128, 1024, 1024,
+                                                  kSwizzle128B);
                                     mma_e4m3(d + h * 128, adesc, bdesc, kIdesc, ks > 0);
                                 }
                             } else {
-                                const uint64_t bdesc = smem_desc(b_s + ks * 32, 16, 1024, kSwizzle128B);
+                                const uint64_t bdesc =
+                                    smem_desc(b_s + ks * 32, 16, 1024, kSwizzle128B);
                                 mma_e4m3(d, adesc, bdesc, kIdesc, ks > 0);
                             }
                         }
@@ -233,17 +315,18 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
     } else {
         reg_alloc<kRegsEpilogue>();
-        // ------------------------------------------- promotion and epilogue
+        // ----------------------------------------- promotion and epilogue
         constexpr int H = CF::kHalf;
         constexpr int NCH = H / 16;
         const int ew = warp - 4;
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
         const int ch = ew >> 2;     // column half
-        const int cb_stride = C / 128;
-        uint32_t tc = 0;
+        uint32_t it = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+            int mt, nt;
+            tile_coords(t, tiles_m, tiles_n, raster, mt, nt);
+            const int m0 = mt * BM, n0 = nt * BN;
             const int row = m0 + quad * 32 + lane;
             const bool row_ok = row < R;
             const int col0 = n0 + ch * H;
@@ -251,13 +334,26 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
             for (int i = 0; i < H; ++i) acc[i] = 0.0f;
 
-            for (int kb = 0; kb < nkb; ++kb, ++tc) {
-                const int buf = tc & 1;
-                const uint32_t tuse = tc >> 1;
-                const float rs = row_ok ? __ldg(sa + (size_t)kb * R + row) : 0.0f;
-                float cbs = 0.0f;
-                if (MODE == kFwd) cbs = __ldg(sb + (size_t)(col0 / 128) * nkb + kb);
-                if (MODE == kDgrad) cbs = __ldg(sb + (size_t)kb * cb_stride + col0 / 128);
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int buf = it & 1;
+                const uint32_t tuse = it >> 1;
+                const int ss = it % SS;
+                const uint32_t suse = it / SS;
+                if (!mbar_wait(&sfull_bar[ss], suse & 1u, abort, status,
+                               SITE_GEMM_EPI_TMEM_FULL)) {
+                    ok = false;
+                    break;
+                }
+                const float *slot = reinterpret_cast<const float *>(
+                    dyn_smem + (scale_base - smem_u32(dyn_smem)) + ss * CF::kScaleSlotBytes);
+                const float rs = slot[quad * 32 + lane];
+                const float *scol = slot + BM;
+                float sc = 0.0f;
+                if (MODE != kWgrad) {
+                    sc = rs * scol[(ch * H) / 128];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sempty_bar[ss]);
+                }
                 if (!mbar_wait(&tfull_bar[buf], tuse & 1u, abort, status,
                                SITE_GEMM_EPI_TMEM_FULL)) {
                     ok = false;
@@ -268,7 +364,6 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 uint32_t p0[16], p1[16];
                 tmem_ld16(taddr, p0);
                 if (MODE != kWgrad) {
-                    const float sc = rs * cbs;
 #pragma unroll
                     for (int c = 0; c < NCH; c += 2) {
                         tmem_ld_wait(p0);
@@ -279,7 +374,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         promote16(acc, (c + 1) * 16, p1, sc);
                     }
                 } else {
-                    const float *cs = sb + (size_t)kb * C + col0;
+                    const float *cs = scol + ch * H;
 #pragma unroll
                     for (int c = 0; c < NCH; c += 2) {
                         tmem_ld_wait(p0);
@@ -292,7 +387,10 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                if (lane == 0) {
+                    mbar_arrive(&tempty_bar[buf]);
+                    if (MODE == kWgrad) mbar_arrive(&sempty_bar[ss]);
+                }
             }
             if (!ok) break;
             if (row_ok) {
@@ -369,6 +467,15 @@ bool make_map_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t oute
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Keep in L2 whichever operand every tile row (or column) walks: B when it
+// fits, else A, else groups of 16 row tiles.
+Raster choose_raster(int64_t R, int64_t C, int64_t D) {
+    const int64_t kL2Budget = 96ll << 20;
+    if (C * D <= kL2Budget) return Raster{0, 0};
+    if (R * D <= kL2Budget) return Raster{1, 0};
+    return Raster{2, 16};
+}
+
 template <int BN, int MODE>
 jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, const uint8_t *b,
                   const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D,
@@ -396,7 +503,7 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     const int64_t tiles = ((R + BM - 1) / BM) * (C / BN);
     const int grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
     gemm_fp8_kernel<BN, MODE><<<grid, kThreads, CF::kSmemBytes, stream>>>(
-        ta, tb, sa, sb, out, (int)R, (int)C, (int)D, dev.status_word);
+        ta, tb, sa, sb, out, (int)R, (int)C, (int)D, choose_raster(R, C, D), dev.status_word);
     return launch_status();
 }
 
