@@ -36,6 +36,7 @@ SIGNATURES = {
     "jet_gemm_fp8_dgrad": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_gemm_fp8_wgrad": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_token_mult_prob_error": [P, P, I, P, P, Z, P],
+    "jet_token_mult_prob_error_noalloc": [P, P, I, P, P],
     "jet_workspace_bytes": [ctypes.c_int, I, I, I],
     "jet_device_status": [P, ctypes.POINTER(ctypes.c_uint32)],
     "jet_selftest_bounded_wait": [ctypes.c_uint32, P],
@@ -203,6 +204,17 @@ def jet_token_mult_prob_error(logp_train, logp_rollout, out, ws, stream=None):
     _check("jet_token_mult_prob_error", load().jet_token_mult_prob_error(
         _ptr(logp_train), _ptr(logp_rollout), n, _ptr(out), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def jet_token_mult_prob_error_noalloc(logp_train, logp_rollout, out, stream=None):
+    """Same metric with the library's static scratch instead of a workspace."""
+    import torch
+    n = logp_train.numel()
+    _need(logp_train, torch.float32, (n,), "logp_train")
+    _need(logp_rollout, torch.float32, (n,), "logp_rollout")
+    _need(out, torch.float32, (1,), "out")
+    _check("jet_token_mult_prob_error_noalloc", load().jet_token_mult_prob_error_noalloc(
+        _ptr(logp_train), _ptr(logp_rollout), n, _ptr(out), _stream(stream)))
 
 
 # --------------------------------------------------------------------------

@@ -5,6 +5,8 @@
 // FP64 across the block, and stores one FP64 partial per block in the
 // workspace; one block then adds the G partials in a fixed order (so the
 // result is deterministic) and writes the mean as FP32.
+#include <mutex>
+
 #include "jet_common.cuh"
 
 namespace {
@@ -96,4 +98,64 @@ extern "C" jet_status jet_token_mult_prob_error(const float *logp_train,
     if (st != JET_OK) return st;
     return jet_metric_launch(logp_train, logp_rollout, n, out, static_cast<double *>(ws),
                              jet::as_stream(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Variant that allocates nothing: the per-block partial sums live in a
+// file-scope device array instead of a caller-supplied workspace.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// Capacity of the static scratch: one FP64 partial per first-pass block.
+constexpr int kNoAllocPartials = 1024;
+// Largest n this variant accepts: the first pass uses one block per 2048
+// tokens, so 1024 partials cover 2,097,152 tokens.
+constexpr int64_t kNoAllocMaxTokens = (int64_t)kNoAllocPartials * kElemsPerBlockTarget;
+
+// 8 KB on every device that loads the library, kept until the process exits.
+// In host code this name is only a host-side stand-in for the device array;
+// its device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) double g_tmpe_scratch[kNoAllocPartials];
+
+std::mutex g_scratch_mu;
+double *g_scratch_ptr[64] = {};
+
+// Device address of g_tmpe_scratch on the current device `dev`, looked up once
+// per device (with that device current) and cached.
+jet_status scratch_address(int dev, double **out) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (dev < 0 || dev >= 64) return JET_ERR_DEVICE;
+    if (g_scratch_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_tmpe_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return JET_ERR_CUDA;
+        }
+        g_scratch_ptr[dev] = static_cast<double *>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return JET_OK;
+}
+
+}  // namespace
+
+extern "C" jet_status jet_token_mult_prob_error_noalloc(const float *logp_train,
+                                                        const float *logp_rollout, int64_t n,
+                                                        float *out, jet_stream_t stream) {
+    JET_REQUIRE(logp_train && logp_rollout && out, JET_ERR_NULL);
+    JET_REQUIRE(n >= 1 && n <= kNoAllocMaxTokens, JET_ERR_SHAPE);
+    JET_REQUIRE(jet::aligned16(logp_train) && jet::aligned16(logp_rollout) &&
+                    jet::aligned16(out),
+                JET_ERR_ALIGN);
+    jet::DeviceInfo dev;
+    jet_status st = jet::current_device(&dev);
+    if (st != JET_OK) return st;
+    if (jet_metric_blocks(n) > kNoAllocPartials) return JET_ERR_SHAPE;
+    double *partial = nullptr;
+    st = scratch_address(dev.ordinal, &partial);
+    if (st != JET_OK) return st;
+    // Every slot the second pass reads is written by the first pass of this
+    // call, so the array needs no clearing between calls.
+    return jet_metric_launch(logp_train, logp_rollout, n, out, partial, jet::as_stream(stream));
 }

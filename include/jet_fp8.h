@@ -185,6 +185,33 @@ JET_API jet_status jet_token_mult_prob_error(const float *logp_train,
                                      jet_stream_t stream);
 
 /*
+ * token-mult-prob-error without a workspace argument, for callers that cannot
+ * allocate device memory: a plain C host that only receives device pointers
+ * from another runtime and has no allocator of its own, or a latency-bound
+ * loop that must not call cudaMalloc (it can synchronize the whole device and
+ * is not ordered on a stream).  The pages have no counterpart; this is a
+ * convenience of this library.  Same arithmetic, grid and result as
+ * jet_token_mult_prob_error.
+ *   logp_train, logp_rollout [n] FP32 (in), out: one FP32 (out); device
+ *   pointers owned by the caller, as everywhere else.
+ *   1 <= n <= 2,097,152; larger n returns JET_ERR_SHAPE before any launch.
+ * The per-block partial sums go to a static 8 KB device array inside the
+ * library (1024 FP64 slots; every device that loads the library keeps it until
+ * the process exits).  The library allocates and frees nothing here.  The first
+ * call on a device looks up that array's device address (with the device
+ * current) and caches it; make that first call before any stream capture.
+ * All calls share the one array: calls whose kernels overlap on the GPU (e.g.
+ * on two streams at once) race on it and may return wrong values - order them
+ * on one stream or use jet_token_mult_prob_error with separate workspaces.
+ * Nothing needs clearing between calls: every slot a call reads is written
+ * earlier in the same call.
+ */
+JET_API jet_status jet_token_mult_prob_error_noalloc(const float *logp_train,
+                                                     const float *logp_rollout,
+                                                     int64_t n, float *out,
+                                                     jet_stream_t stream);
+
+/*
  * Workspace bytes an operation needs for the given sizes (0 if none).
  * For JET_OP_TOKEN_MULT_PROB_ERROR pass n as M.  Returns 0 for negative sizes
  * or an unknown op.  Pure host function; needs no device.

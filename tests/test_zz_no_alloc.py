@@ -1,0 +1,65 @@
+"""jet_token_mult_prob_error_noalloc: the metric for callers that cannot
+allocate device memory (the library keeps the partial sums in its own static
+device array).  Called through the C ABI with raw device pointers and checked
+against jet_token_mult_prob_error (caller-supplied workspace) within the
+metric's test tolerance, on two calls in a row with different inputs so that
+the second call runs over the first call's leftover scratch contents.
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it also passes alone in a fresh process."""
+import ctypes
+
+import pytest
+import torch
+
+from fp8_block_quantized_gb300 import binding
+from fp8_block_quantized_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+RTOL = 1e-5
+MAX_TOKENS = 2_097_152
+
+
+def raw(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def reference_value(lib, a, b, stream):
+    n = a.numel()
+    ws = torch.empty((max(lib.jet_workspace_bytes(6, n, 0, 0), 16),), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty((1,), dtype=torch.float32, device="cuda")
+    assert lib.jet_token_mult_prob_error(raw(a), raw(b), n, raw(out), raw(ws),
+                                         ws.numel(), stream) == 0
+    return out
+
+
+def test_noalloc_matches_workspace_version_twice(torch_cuda):
+    lib = binding.load()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    cases = [wl.logprobs(MAX_TOKENS, seed=11), wl.logprobs(300_001, seed=12)]
+    outs = []
+    for a, b in cases:                       # two calls in a row
+        a, b = a.cuda(), b.cuda()
+        out = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+        code = lib.jet_token_mult_prob_error_noalloc(raw(a), raw(b), a.numel(), raw(out), stream)
+        assert code == 0, binding.STATUS.get(code, code)
+        ref = reference_value(lib, a, b, stream)
+        torch.cuda.synchronize()
+        got, want = float(out.cpu()[0]), float(ref.cpu()[0])
+        assert abs(got - want) <= RTOL * want, (got, want)
+        outs.append(got)
+    assert outs[0] != outs[1]
+    code, word = binding.device_status()
+    assert code == 0, (code, word)
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(torch_cuda):
+    lib = binding.load()
+    a, b = (t.cuda() for t in wl.logprobs(64))
+    out = torch.empty((1,), dtype=torch.float32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.jet_token_mult_prob_error_noalloc(raw(a), raw(b), MAX_TOKENS + 1, raw(out),
+                                                 stream) == 2          # JET_ERR_SHAPE
+    assert lib.jet_token_mult_prob_error_noalloc(raw(a), raw(b), 0, raw(out), stream) == 2
