@@ -179,27 +179,35 @@ class LayerStep:
         self.launches_per_step = len(self.lin) * 6 + len(self.inputs) * 2 + 2
 
     def calls(self):
-        """The step as (family, thunk) pairs in launch order."""
+        """The step as (family, thunk, shape label) in launch order."""
         j = self.jet
         out = []
         for L in self.lin:
-            out.append(("quant_w_128x128", lambda L=L: j.jet_quant_w_128x128(L["w"], L["qw"], L["sw"])))
+            out.append(("quant_w_128x128", lambda L=L: j.jet_quant_w_128x128(L["w"], L["qw"], L["sw"]),
+                        L["case"].name))
         for v in self.inputs.values():
-            out.append(("quant_act_1x128", lambda v=v: j.jet_quant_act_1x128(v["x"], v["q"], v["s"])))
+            out.append(("quant_act_1x128", lambda v=v: j.jet_quant_act_1x128(v["x"], v["q"], v["s"]),
+                        "x%d" % v["K"]))
         for L in self.lin:
             v = self.inputs[L["case"].key]
-            out.append(("gemm_fp8_fwd", lambda L=L, v=v: j.jet_gemm_fp8_fwd(v["q"], v["s"], L["qw"], L["sw"], L["y"])))
+            out.append(("gemm_fp8_fwd", lambda L=L, v=v: j.jet_gemm_fp8_fwd(v["q"], v["s"], L["qw"], L["sw"], L["y"]),
+                        L["case"].name))
         for L in self.lin:
-            out.append(("quant_act_1x128", lambda L=L: j.jet_quant_act_1x128(L["dy"], L["qdy"], L["sdy"])))
-            out.append(("gemm_fp8_dgrad", lambda L=L: j.jet_gemm_fp8_dgrad(L["qdy"], L["sdy"], L["qw"], L["sw"], L["dx"])))
-            out.append(("requant_128x1", lambda L=L: j.jet_requant_128x1(L["qdy"], L["sdy"], L["qdyT"], L["sdyT"])))
+            out.append(("quant_act_1x128", lambda L=L: j.jet_quant_act_1x128(L["dy"], L["qdy"], L["sdy"]),
+                        "dy_" + L["case"].name))
+            out.append(("gemm_fp8_dgrad", lambda L=L: j.jet_gemm_fp8_dgrad(L["qdy"], L["sdy"], L["qw"], L["sw"], L["dx"]),
+                        L["case"].name))
+            out.append(("requant_128x1", lambda L=L: j.jet_requant_128x1(L["qdy"], L["sdy"], L["qdyT"], L["sdyT"]),
+                        "dy_" + L["case"].name))
         for v in self.inputs.values():
-            out.append(("requant_128x1", lambda v=v: j.jet_requant_128x1(v["q"], v["s"], v["qT"], v["sT"])))
+            out.append(("requant_128x1", lambda v=v: j.jet_requant_128x1(v["q"], v["s"], v["qT"], v["sT"]),
+                        "x%d" % v["K"]))
         for L in self.lin:
             v = self.inputs[L["case"].key]
-            out.append(("gemm_fp8_wgrad", lambda L=L, v=v: j.jet_gemm_fp8_wgrad(L["qdyT"], L["sdyT"], v["qT"], v["sT"], L["dw"])))
+            out.append(("gemm_fp8_wgrad", lambda L=L, v=v: j.jet_gemm_fp8_wgrad(L["qdyT"], L["sdyT"], v["qT"], v["sT"], L["dw"]),
+                        L["case"].name))
         out.append(("token_mult_prob_error", lambda: j.jet_token_mult_prob_error(
-            self.logp_train, self.logp_rollout, self.metric_out, self.metric_ws)))
+            self.logp_train, self.logp_rollout, self.metric_out, self.metric_ws), "n%d" % self.M))
         return out
 
     def host_io(self):
@@ -242,7 +250,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
 
     for _ in range(args.warmup):
-        for _, f in calls:
+        for _, f, _ in calls:
             f()
     code, word = jet.device_status()
     if code != 0:
@@ -250,6 +258,7 @@ def run_gpu(args):
 
     # ---- timed region: K steps, per-kernel CUDA events on the launch stream
     fam_ms = {}
+    detail_ms = {}
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in calls] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -257,7 +266,7 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         t0.record(stream)
         for k in range(args.steps):
-            for (fam, f), (a, b) in zip(calls, ev[k]):
+            for (fam, f, _), (a, b) in zip(calls, ev[k]):
                 a.record(stream)
                 f()
                 b.record(stream)
@@ -265,8 +274,10 @@ def run_gpu(args):
         barrier()
     total_ms = t0.elapsed_time(t1)
     for k in range(args.steps):
-        for (fam, _), (a, b) in zip(calls, ev[k]):
-            fam_ms[fam] = fam_ms.get(fam, 0.0) + a.elapsed_time(b)
+        for (fam, _, label), (a, b) in zip(calls, ev[k]):
+            ms = a.elapsed_time(b)
+            fam_ms[fam] = fam_ms.get(fam, 0.0) + ms
+            detail_ms[(fam, label)] = detail_ms.get((fam, label), 0.0) + ms
     code, word = jet.device_status()
     if code != 0:
         raise RuntimeError(f"device status {code} ({word:#x}) after timing")
@@ -285,7 +296,7 @@ def run_gpu(args):
         def e2e_step():
             for h, d in step.h_in:
                 d.copy_(h, non_blocking=True)
-            for _, f in calls:
+            for _, f, _ in calls:
                 f()
             for h, d in step.h_out:
                 h.copy_(d, non_blocking=True)
@@ -320,7 +331,7 @@ def run_gpu(args):
     fp8_sust = FP8_OVER_BF16 * float(pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
     kernels = {}
     launches = {}
-    for fam, _ in calls:
+    for fam, _, _ in calls:
         launches[fam] = launches.get(fam, 0) + 1
     for fam, ms in fam_ms.items():
         avg_ms = ms / args.steps
@@ -373,6 +384,9 @@ def run_gpu(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if args.detail:
+        line["detail_ms_per_step"] = {f"{fam}/{label}": round(ms / args.steps, 4)
+                                      for (fam, label), ms in detail_ms.items()}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, seconds=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -495,6 +509,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--detail", action="store_true",
+                    help="also report per-launch-site kernel times")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # timing rule: at least 3 warm-up steps
     if args.impl == "reference":

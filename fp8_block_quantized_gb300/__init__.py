@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     quant_w_128x128,
     requant_128x1,
     selftest_bounded_wait,
+    selftest_quotient,
     token_mult_prob_error,
     workspace_bytes,
 )

@@ -40,6 +40,7 @@ SIGNATURES = {
     "jet_workspace_bytes": [ctypes.c_int, I, I, I],
     "jet_device_status": [P, ctypes.POINTER(ctypes.c_uint32)],
     "jet_selftest_bounded_wait": [ctypes.c_uint32, P],
+    "jet_selftest_quotient": [P, P, I, P, P],
 }
 _RESTYPE = {"jet_status_str": ctypes.c_char_p, "jet_version": ctypes.c_int,
             "jet_workspace_bytes": ctypes.c_size_t}
@@ -109,6 +110,18 @@ def workspace_bytes(op: str, M=0, N=0, K=0) -> int:
 def selftest_bounded_wait(limit_us: int, stream=None):
     """Run the library's bounded-wait self-test kernel (records a timeout)."""
     _check("jet_selftest_bounded_wait", load().jet_selftest_bounded_wait(limit_us, _stream(stream)))
+
+
+def selftest_quotient(x, s, stream=None):
+    """x / s elementwise through the quantizers' division routine."""
+    import torch
+    n = x.numel()
+    _need(x, torch.float32, (n,), "x")
+    _need(s, torch.float32, (n,), "s")
+    q = torch.empty_like(x)
+    _check("jet_selftest_quotient", load().jet_selftest_quotient(_ptr(x), _ptr(s), n, _ptr(q),
+                                                                  _stream(stream)))
+    return q
 
 
 def device_status(stream=None):

@@ -62,12 +62,14 @@ static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168,
 constexpr int BM = 128;  // output rows per tile (TMEM lanes)
 constexpr int BK = 128;  // contraction slice = one scale block
 
-template <int BN>
+template <int BN, int CL>
 struct Cfg {
-    static constexpr int kStages = BN == 256 ? 4 : 6;
+    // Per CTA and stage: A's 128 rows and B's BN (CL = 1) or BN/2 (pair) rows.
+    static constexpr int kBRows = BN / CL;
     static constexpr int kABytes = BM * BK;
-    static constexpr int kBBytes = BN * BK;
+    static constexpr int kBBytes = kBRows * BK;
     static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = kStageBytes <= 32 * 1024 ? 6 : 4;
     // Scale ring: per slice, the tile's 128 row scales and its column scales
     // (BN per-column values for wgrad, BN/128 block values otherwise).
     static constexpr int kScaleSlots = 8;
@@ -111,42 +113,61 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// acc[base .. base+15] += p[j] * sc
+// acc[base .. base+7] += p[2j .. 2j+1] * sc  (pairs, fma.rn.f32x2)
 template <int N>
-__device__ __forceinline__ void promote16(float (&acc)[N], int base, const uint32_t (&p)[16],
-                                          float sc) {
+__device__ __forceinline__ void promote16(float2 (&acc)[N], int base, const uint32_t (&p)[16],
+                                          float2 sc) {
 #pragma unroll
-    for (int j = 0; j < 16; j += 2)
-        ffma2(acc[base + j], acc[base + j + 1], __uint_as_float(p[j]), __uint_as_float(p[j + 1]),
-              sc, sc);
+    for (int j = 0; j < 8; ++j)
+        acc[base + j] = __ffma2_rn(
+            make_float2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1])), sc,
+            acc[base + j]);
 }
 
-// acc[base .. base+15] += (p[j] * rs) * cs[j]   (per-column scales, wgrad);
-// cs points to shared memory.
+// acc[base .. base+7] += (p * rs) * cs   (per-column scales, wgrad; cs holds
+// this chunk's 16 column scales)
 template <int N>
-__device__ __forceinline__ void promote16_cols(float (&acc)[N], int base, const uint32_t (&p)[16],
-                                               float rs, const float *cs) {
-    const float4 *c4 = reinterpret_cast<const float4 *>(cs);
+__device__ __forceinline__ void promote16_cols(float2 (&acc)[N], int base,
+                                               const uint32_t (&p)[16], float2 rs,
+                                               const float4 (&cs)[4]) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float4 c = c4[q];
-        float t0, t1, t2, t3;
-        fmul2(t0, t1, __uint_as_float(p[4 * q + 0]), __uint_as_float(p[4 * q + 1]), rs, rs);
-        fmul2(t2, t3, __uint_as_float(p[4 * q + 2]), __uint_as_float(p[4 * q + 3]), rs, rs);
-        ffma2(acc[base + 4 * q + 0], acc[base + 4 * q + 1], t0, t1, c.x, c.y);
-        ffma2(acc[base + 4 * q + 2], acc[base + 4 * q + 3], t2, t3, c.z, c.w);
+        const float2 t0 = __fmul2_rn(
+            make_float2(__uint_as_float(p[4 * q + 0]), __uint_as_float(p[4 * q + 1])), rs);
+        const float2 t1 = __fmul2_rn(
+            make_float2(__uint_as_float(p[4 * q + 2]), __uint_as_float(p[4 * q + 3])), rs);
+        acc[base + 2 * q] = __ffma2_rn(t0, make_float2(cs[q].x, cs[q].y), acc[base + 2 * q]);
+        acc[base + 2 * q + 1] =
+            __ffma2_rn(t1, make_float2(cs[q].z, cs[q].w), acc[base + 2 * q + 1]);
     }
 }
 
-template <int BN, int MODE>
+__device__ __forceinline__ void load_cs(float4 (&cs)[4], const float *src) {
+    const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cs[q] = s4[q];
+}
+
+// CL = 1: one CTA computes a 128 x BN tile with tcgen05.mma.cta_group::1.
+// CL = 2: a cluster of two CTAs computes a 256 x BN tile with the pair MMA
+// (tcgen05.mma.cta_group::2) issued by the even CTA ("leader"): each CTA loads
+// its own 128 rows of A and half of B's BN rows, so each SM takes in 32 KB per
+// 128-slice instead of 48 KB and six stages fit in shared memory instead of
+// four.  Both CTAs' TMA loads signal the leader's "full" barrier; the
+// leader's commits arrive on both CTAs' "empty" and "TMEM full" barriers; both
+// CTAs' promotion warps release the leader's "TMEM empty" barrier; each CTA
+// promotes and stores its own 128 rows from its own TMEM.
+template <int BN, int MODE, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const float *__restrict__ sa, const float *__restrict__ sb,
                 uint16_t *__restrict__ out, int R, int C, int D, Raster raster,
                 unsigned *status) {
-    using CF = Cfg<BN>;
+    using CF = Cfg<BN, CL>;
     constexpr int S = CF::kStages;
     constexpr int SS = CF::kScaleSlots;
+    constexpr bool kPair = CL == 2;
+    constexpr uint16_t kPairMask = 0x3;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ uint64_t full_bar[S], empty_bar[S], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint64_t sfull_bar[SS], sempty_bar[SS];
@@ -158,8 +179,12 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t scale_base = smem_base + S * CF::kStageBytes;
     const int tiles_m = (R + BM - 1) / BM;
     const int tiles_n = C / BN;
-    const int total = tiles_m * tiles_n;
+    const int units_m = (tiles_m + CL - 1) / CL;  // row tiles per cluster step
+    const int total = units_m * tiles_n;
     const int nkb = D / BK;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
     volatile int *abort = &abort_sh;
 
     if (threadIdx.x == 0) {
@@ -173,7 +198,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull_bar[b], 1);
-            mbar_init(&tempty_bar[b], 8);
+            mbar_init(&tempty_bar[b], 8 * CL);  // epilogue warps of every CTA of the pair
         }
         mbar_init(&drain_bar, 1);
         abort_sh = 0;
@@ -184,11 +209,19 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_base_sh, CF::kTmemCols);
-        tmem_relinquish();
+        if (kPair) {
+            tmem_alloc_pair(&tmem_base_sh, CF::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&tmem_base_sh, CF::kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if (kPair)
+        cluster_sync();  // the peer's barriers are initialised before any remote use
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
@@ -200,10 +233,10 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // -------------------------------------------------- TMA producer
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                int mt, nt;
-                tile_coords(t, tiles_m, tiles_n, raster, mt, nt);
-                const int m0 = mt * BM, n0 = nt * BN;
+            for (int t = unit0; ok && t < total; t += unit_step) {
+                int mu, nt;
+                tile_coords(t, units_m, tiles_n, raster, mu, nt);
+                const int m0 = (mu * CL + (int)rank) * BM, n0 = nt * BN;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
@@ -241,32 +274,50 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if (lane == 0) {
                         const uint32_t a_s = smem_base + s * CF::kStageBytes;
                         const uint32_t b_s = a_s + CF::kABytes;
-                        mbar_arrive_expect_tx(&full_bar[s], CF::kStageBytes);
-                        tma_load_2d(a_s, &tmA, &full_bar[s], kb * BK, m0);
-                        if (MODE == kDgrad) {
-#pragma unroll
-                            for (int h = 0; h < BN / 128; ++h)
-                                tma_load_2d(b_s + h * 128 * BK, &tmB, &full_bar[s], n0 + 128 * h,
-                                            kb * BK);
+                        if (kPair) {
+                            // Both CTAs' boxes complete on the leader's barrier,
+                            // which expects the pair's bytes.
+                            const uint32_t fb = map_to_cta(&full_bar[s], 0);
+                            if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * CF::kStageBytes);
+                            tma_load_2d_pair(a_s, &tmA, fb, kb * BK, m0);
+                            if (MODE == kDgrad)
+                                tma_load_2d_pair(b_s, &tmB, fb, n0 + CF::kBRows * (int)rank,
+                                                 kb * BK);
+                            else
+                                tma_load_2d_pair(b_s, &tmB, fb, kb * BK,
+                                                 n0 + CF::kBRows * (int)rank);
                         } else {
-                            tma_load_2d(b_s, &tmB, &full_bar[s], kb * BK, n0);
+                            mbar_arrive_expect_tx(&full_bar[s], CF::kStageBytes);
+                            tma_load_2d(a_s, &tmA, &full_bar[s], kb * BK, m0);
+                            if (MODE == kDgrad) {
+#pragma unroll
+                                for (int h = 0; h < BN / 128; ++h)
+                                    tma_load_2d(b_s + h * 128 * BK, &tmB, &full_bar[s],
+                                                n0 + 128 * h, kb * BK);
+                            } else {
+                                tma_load_2d(b_s, &tmB, &full_bar[s], kb * BK, n0);
+                            }
                         }
                     }
                     __syncwarp();
                 }
             }
-            // Every issued load must have landed before the CTA can exit.
-            for (uint32_t j = it > (uint32_t)S ? it - S : 0u; j < it; ++j)
-                mbar_wait(&full_bar[j % S], (j / S) & 1u, nullptr, status, SITE_GEMM_DRAIN);
+            // Every issued load must have landed before the CTA can exit (the
+            // pair's loads are tracked by the leader's barriers).
+            if (!kPair || leader)
+                for (uint32_t j = it > (uint32_t)S ? it - S : 0u; j < it; ++j)
+                    mbar_wait(&full_bar[j % S], (j / S) & 1u, nullptr, status, SITE_GEMM_DRAIN);
             for (uint32_t j = it > (uint32_t)SS ? it - SS : 0u; j < it; ++j)
                 mbar_wait(&sfull_bar[j % SS], (j / SS) & 1u, nullptr, status, SITE_GEMM_DRAIN);
-        } else if (warp == 1) {
+        } else if (warp == 1 && leader) {
             // --------------------------------------------------- MMA issuer
+            // (in a pair only the leader issues; the MMA spans both CTAs)
+            constexpr bool kMN = MODE == kDgrad;
             constexpr uint32_t kIdesc =
-                idesc_e4m3_f32(BM, MODE == kDgrad ? 128 : BN, MODE == kDgrad);
+                kPair ? idesc_e4m3_f32(2 * BM, BN, kMN) : idesc_e4m3_f32(BM, kMN ? 128 : BN, kMN);
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for (int t = unit0; ok && t < total; t += unit_step) {
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
@@ -286,7 +337,14 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                         for (int ks = 0; ks < BK / 32; ++ks) {
                             const uint64_t adesc = smem_desc(a_s + ks * 32, 16, 1024, kSwizzle128B);
-                            if (MODE == kDgrad) {
+                            if (kPair) {
+                                // per CTA: B holds BN/2 rows (K-major) or one
+                                // 128-column MN-major atom (dgrad)
+                                const uint64_t bdesc =
+                                    kMN ? smem_desc(b_s + ks * 32 * 128, 1024, 1024, kSwizzle128B)
+                                        : smem_desc(b_s + ks * 32, 16, 1024, kSwizzle128B);
+                                mma_e4m3_pair(d, adesc, bdesc, kIdesc, ks > 0);
+                            } else if (kMN) {
                                 // MN-major B: 8-row contraction groups 1024 B apart;
                                 // each MMA covers one 128-column swizzle atom.
 #pragma unroll
@@ -302,14 +360,24 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                 mma_e4m3(d, adesc, bdesc, kIdesc, ks > 0);
                             }
                         }
-                        mma_commit(&empty_bar[s]);
-                        mma_commit(&tfull_bar[buf]);
+                        if (kPair) {
+                            mma_commit_pair_mc(&empty_bar[s], kPairMask);
+                            mma_commit_pair_mc(&tfull_bar[buf], kPairMask);
+                        } else {
+                            mma_commit(&empty_bar[s]);
+                            mma_commit(&tfull_bar[buf]);
+                        }
                     }
                     __syncwarp();
                 }
             }
             // All issued MMAs must complete before TMEM is released.
-            if (lane == 0) mma_commit(&drain_bar);
+            if (lane == 0) {
+                if (kPair)
+                    mma_commit_pair_mc(&drain_bar, 0x1);
+                else
+                    mma_commit(&drain_bar);
+            }
             __syncwarp();
             mbar_wait(&drain_bar, 0, nullptr, status, SITE_GEMM_DRAIN);
         }
@@ -321,18 +389,23 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int ew = warp - 4;
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
         const int ch = ew >> 2;     // column half
+        uint32_t tempty_remote[2] = {0u, 0u};
+        if (kPair) {
+            tempty_remote[0] = map_to_cta(&tempty_bar[0], 0);
+            tempty_remote[1] = map_to_cta(&tempty_bar[1], 0);
+        }
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            int mt, nt;
-            tile_coords(t, tiles_m, tiles_n, raster, mt, nt);
-            const int m0 = mt * BM, n0 = nt * BN;
+        for (int t = unit0; ok && t < total; t += unit_step) {
+            int mu, nt;
+            tile_coords(t, units_m, tiles_n, raster, mu, nt);
+            const int m0 = (mu * CL + (int)rank) * BM, n0 = nt * BN;
             const int row = m0 + quad * 32 + lane;
             const bool row_ok = row < R;
             const int col0 = n0 + ch * H;
-            float acc[H];
+            float2 acc[H / 2];
 #pragma unroll
-            for (int i = 0; i < H; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < H / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int buf = it & 1;
@@ -364,31 +437,42 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 uint32_t p0[16], p1[16];
                 tmem_ld16(taddr, p0);
                 if (MODE != kWgrad) {
+                    const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
                     for (int c = 0; c < NCH; c += 2) {
                         tmem_ld_wait(p0);
                         tmem_ld16(taddr + (c + 1) * 16, p1);
-                        promote16(acc, c * 16, p0, sc);
+                        promote16(acc, c * 8, p0, sc2);
                         tmem_ld_wait(p1);
                         if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
-                        promote16(acc, (c + 1) * 16, p1, sc);
+                        promote16(acc, (c + 1) * 8, p1, sc2);
                     }
                 } else {
+                    // Column scales are loaded one chunk ahead of their use so
+                    // that shared-memory latency overlaps the previous chunk.
                     const float *cs = scol + ch * H;
+                    const float2 rs2 = make_float2(rs, rs);
+                    float4 csa[4], csb[4];
+                    load_cs(csa, cs);
 #pragma unroll
                     for (int c = 0; c < NCH; c += 2) {
+                        load_cs(csb, cs + (c + 1) * 16);
                         tmem_ld_wait(p0);
                         tmem_ld16(taddr + (c + 1) * 16, p1);
-                        promote16_cols(acc, c * 16, p0, rs, cs + c * 16);
+                        promote16_cols(acc, c * 8, p0, rs2, csa);
+                        if (c + 2 < NCH) load_cs(csa, cs + (c + 2) * 16);
                         tmem_ld_wait(p1);
                         if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
-                        promote16_cols(acc, (c + 1) * 16, p1, rs, cs + (c + 1) * 16);
+                        promote16_cols(acc, (c + 1) * 8, p1, rs2, csb);
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&tempty_bar[buf]);
+                    if (kPair)
+                        mbar_arrive_cluster_relaxed(tempty_remote[buf]);
+                    else
+                        mbar_arrive(&tempty_bar[buf]);
                     if (MODE == kWgrad) mbar_arrive(&sempty_bar[ss]);
                 }
             }
@@ -398,10 +482,10 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                 for (int i = 0; i < H / 8; ++i) {
                     uint4 v;
-                    v.x = pack_bf16x2(acc[8 * i + 0], acc[8 * i + 1]);
-                    v.y = pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]);
-                    v.z = pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]);
-                    v.w = pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]);
+                    v.x = pack_bf16x2(acc[4 * i + 0].x, acc[4 * i + 0].y);
+                    v.y = pack_bf16x2(acc[4 * i + 1].x, acc[4 * i + 1].y);
+                    v.z = pack_bf16x2(acc[4 * i + 2].x, acc[4 * i + 2].y);
+                    v.w = pack_bf16x2(acc[4 * i + 3].x, acc[4 * i + 3].y);
                     dst[i] = v;
                 }
             }
@@ -409,16 +493,24 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 
     tc_fence_before();
-    __syncthreads();
+    // Neither CTA of a pair may exit or free TMEM while the other can still
+    // use its barriers, shared memory or the pair's TMEM allocation.
+    if (kPair)
+        cluster_sync();
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, CF::kTmemCols);
+        if (kPair)
+            tmem_dealloc_pair(tmem, CF::kTmemCols);
+        else
+            tmem_dealloc(tmem, CF::kTmemCols);
     }
 }
 
 // Self-test of the bounded-wait path: waits on an mbarrier that nothing
-// arrives at, so the wait gives up after `limit_ns` and records a timeout.
-__global__ void selftest_wait_kernel(unsigned *status, uint64_t limit_ns) {
+// arrives at, so the wait gives up after `limit_cycles` and records a timeout.
+__global__ void selftest_wait_kernel(unsigned *status, uint64_t limit_cycles) {
     __shared__ uint64_t bar;
     __shared__ volatile int abort_flag;
     if (threadIdx.x == 0) {
@@ -427,7 +519,7 @@ __global__ void selftest_wait_kernel(unsigned *status, uint64_t limit_ns) {
         fence_mbar_init();
     }
     __syncthreads();
-    mbar_wait(&bar, 0, &abort_flag, status, SITE_TEST_NEVER_SET, limit_ns);
+    mbar_wait(&bar, 0, &abort_flag, status, SITE_TEST_NEVER_SET, limit_cycles);
 }
 
 // ------------------------------------------------------------------- host --
@@ -476,34 +568,62 @@ Raster choose_raster(int64_t R, int64_t C, int64_t D) {
     return Raster{2, 16};
 }
 
-template <int BN, int MODE>
+// Kernel arguments are passed by value; a CUtensorMap goes as is.
+inline const CUtensorMap &tmA_arg(const CUtensorMap &m) { return m; }
+
+template <int BN, int MODE, int CL>
 jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, const uint8_t *b,
                   const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D,
                   cudaStream_t stream) {
-    using CF = Cfg<BN>;
+    using CF = Cfg<BN, CL>;
+    auto kernel = gemm_fp8_kernel<BN, MODE, CL>;
     static std::mutex mu;
-    static bool attr_set[64] = {};
+    static int max_units[64] = {};  // co-resident CTAs (CL = 1) or clusters (CL = 2)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = CF::kSmemBytes;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!attr_set[dev.ordinal]) {
-            if (cudaFuncSetAttribute(gemm_fp8_kernel<BN, MODE>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (max_units[dev.ordinal] == 0) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      CF::kSmemBytes) != cudaSuccess) {
                 cudaGetLastError();
                 return JET_ERR_CUDA;
             }
-            attr_set[dev.ordinal] = true;
+            int n = dev.num_sms / CL;
+            if (CL > 1) {
+                cfg.gridDim = dim3(dev.num_sms - dev.num_sms % CL);
+                int clusters = 0;
+                if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess &&
+                    clusters > 0)
+                    n = clusters;
+                cudaGetLastError();
+            }
+            max_units[dev.ordinal] = n;
         }
     }
     CUtensorMap ta, tb;
     if (!make_map_u8(&ta, a, (uint64_t)D, (uint64_t)R, BK, BM)) return JET_ERR_CUDA;
     bool okb = MODE == kDgrad ? make_map_u8(&tb, b, (uint64_t)C, (uint64_t)D, 128, BK)
-                              : make_map_u8(&tb, b, (uint64_t)D, (uint64_t)C, BK, BN);
+                              : make_map_u8(&tb, b, (uint64_t)D, (uint64_t)C, BK, CF::kBRows);
     if (!okb) return JET_ERR_CUDA;
-    const int64_t tiles = ((R + BM - 1) / BM) * (C / BN);
-    const int grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
-    gemm_fp8_kernel<BN, MODE><<<grid, kThreads, CF::kSmemBytes, stream>>>(
-        ta, tb, sa, sb, out, (int)R, (int)C, (int)D, choose_raster(R, C, D), dev.status_word);
+    const int64_t units = ((R + BM * CL - 1) / (BM * CL)) * (C / BN);
+    const int64_t grid_units = units < max_units[dev.ordinal] ? units : max_units[dev.ordinal];
+    cfg.gridDim = dim3((unsigned)(grid_units * CL));
+    const Raster raster = choose_raster(R, C, D);
+    if (cudaLaunchKernelEx(&cfg, kernel, tmA_arg(ta), tmA_arg(tb), sa, sb, out, (int)R, (int)C,
+                           (int)D, raster, dev.status_word) != cudaSuccess) {
+        cudaGetLastError();
+        return JET_ERR_CUDA;
+    }
     return launch_status();
 }
 
@@ -519,8 +639,13 @@ jet_status run_gemm(const uint8_t *a, const float *sa, const uint8_t *b, const f
         return cudaMemsetAsync(out, 0, (size_t)R * C * 2, stream) == cudaSuccess ? JET_OK
                                                                                : JET_ERR_CUDA;
     }
-    if (C % 256 == 0) return launch<256, MODE>(dev, a, sa, b, sb, out, R, C, D, stream);
-    return launch<128, MODE>(dev, a, sa, b, sb, out, R, C, D, stream);
+    // The pair MMA (256 x 256 per CTA pair) whenever there are at least two
+    // row tiles and the output is a multiple of 256 wide.
+    if (C % 256 == 0) {
+        if (R > BM) return launch<256, MODE, 2>(dev, a, sa, b, sb, out, R, C, D, stream);
+        return launch<256, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, stream);
+    }
+    return launch<128, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, stream);
 }
 
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
@@ -586,8 +711,9 @@ jet_status jet_selftest_bounded_wait(uint32_t limit_us, jet_stream_t stream) {
     DeviceInfo dev;
     jet_status st = current_device(&dev);
     if (st != JET_OK) return st;
+    // limit in SM cycles at the 2.07 GHz maximum clock (longer at lower clocks)
     selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(dev.status_word,
-                                                          (uint64_t)limit_us * 1000ull);
+                                                          (uint64_t)limit_us * 2070ull);
     return launch_status();
 }
 

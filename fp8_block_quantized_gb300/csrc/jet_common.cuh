@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/jet_fp8.h"
+#include "jet_fp8.h"
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -66,9 +66,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Waits longer than this are treated as a hang: the waiting role records a
-// timeout and abandons its work.  Healthy waits in these kernels last
-// microseconds; the limit is far above any of them.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Waits longer than this many SM cycles (~2 s at 2 GHz) are treated as a
+// hang: the waiting role records a timeout and abandons its work.  Healthy
+// waits in these kernels last microseconds; the limit is far above them.
+constexpr uint64_t kWaitLimitCycles = 4000000000ull;
 
 }  // namespace jet

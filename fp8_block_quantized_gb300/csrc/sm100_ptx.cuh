@@ -49,20 +49,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete, giving up after
-// `limit_ns` of wall time or as soon as *abort is set by another role (abort
-// may be null for a wait that must not be cut short, e.g. a drain).  On a
-// time-out it records JET_ERR_TIMEOUT with `site` in the status word and sets
-// *abort.  Returns true when the phase completed.
+// `limit_cycles` SM clock cycles or as soon as *abort is set by another role
+// (abort may be null for a wait that must not be cut short, e.g. a drain).
+// On a time-out it records JET_ERR_TIMEOUT with `site` in the status word and
+// sets *abort.  Returns true when the phase completed.  The SM cycle counter
+// is cheap to read; the default limit, 4e9 cycles, is about 2 s at the
+// maximum SM clock.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           unsigned *status, unsigned site,
-                                          uint64_t limit_ns = kWaitLimitNs) {
+                                          uint64_t limit_cycles = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const uint64_t t0 = clock64();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((n & 31) == 0) {
             if (abort && *abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
+            if ((uint64_t)(clock64() - t0) > limit_cycles) {
                 report_timeout(status, site);
                 if (abort) *abort = 1;
                 return false;
@@ -120,6 +122,49 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
                  : "memory");
 }
 
+// Same load for a CTA pair (tcgen05 cta_group::2): the box lands in this
+// CTA's shared memory and its transaction bytes are signalled on `bar`, a
+// shared::cluster address that may belong to the peer CTA.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const CUtensorMap *m,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_dst),
+        "l"(m), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+
+// ------------------------------------------------------------------ cluster
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_cta(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Relaxed arrive on an mbarrier given by its shared::cluster address (any
+// CTA of the cluster).  No memory ordering is implied: callers use it only to
+// hand back a TMEM buffer whose reads have completed (tcgen05.wait::ld) and
+// are ordered by tcgen05.fence::before_thread_sync.  (A release at cluster
+// scope would make every arrival wait for the thread's outstanding global
+// stores.)
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
+// All threads of all CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t *smem_result, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -143,6 +188,46 @@ __device__ __forceinline__ void tc_fence_before() {
 
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Pair (cta_group::2) allocation: executed by one warp in each CTA of the
+// pair; the same columns are allocated in both CTAs' TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *smem_result, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(smem_result)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// Pair MMA issued by the even CTA: A's 256 rows are split 128/128 over the
+// two CTAs' shared memory, B's N rows N/2 / N/2, both at the same offsets
+// the descriptors give; each CTA's TMEM receives its own 128 rows of D.
+__device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Commit of the pair's MMAs, arriving on the mbarrier at the same offset in
+// every CTA named in cta_mask.
+__device__ __forceinline__ void mma_commit_pair_mc(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)), "h"(cta_mask)
+        : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, E4M3 x E4M3 -> F32, issued by one thread.
@@ -187,26 +272,6 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
                    "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                  :
                  : "memory");
-}
-
-// Packed FP32 pair FMA (Blackwell f32x2): (d0, d1) += (a0, a1) * (b0, b1).
-__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0,
-                                      float b1) {
-    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%0, %1};\n\t"
-        "fma.rn.f32x2 rc, ra, rb, rc;\n\tmov.b64 {%0, %1}, rc;\n\t}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
-// Packed FP32 pair multiply: (d0, d1) = (a0, a1) * (b0, b1).
-__device__ __forceinline__ void fmul2(float &d0, float &d1, float a0, float a1, float b0,
-                                      float b1) {
-    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rc, ra, rb;\n\tmov.b64 {%0, %1}, rc;\n\t}"
-        : "=f"(d0), "=f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading

@@ -231,12 +231,25 @@ JET_API jet_status jet_device_status(jet_stream_t stream, uint32_t *detail);
 /*
  * Self-test of the failure path every pipelined kernel uses: launches one
  * block that waits on a barrier nothing completes, with a limit of
- * `limit_us` microseconds (1 .. 1,000,000).  The wait gives up, records
+ * `limit_us` microseconds at the maximum SM clock (1 .. 1,000,000; the wait
+ * is counted in SM cycles, so it lasts longer at lower clocks).  The wait gives up, records
  * JET_ERR_TIMEOUT in the device status word and the kernel returns, so a
  * following jet_device_status() reports JET_ERR_TIMEOUT and the context stays
  * usable.  The pages have no counterpart; it exists to test the bounded waits.
  */
 JET_API jet_status jet_selftest_bounded_wait(uint32_t limit_us, jet_stream_t stream);
+
+/*
+ * Self-test of the division the quantizers use: q[i] = x[i] / s[i] computed
+ * exactly as a quantizer divides a value x by its group scale s (a
+ * reciprocal of s shared by the group and Markstein's correction steps).  It
+ * equals the IEEE binary32 quotient whenever s >= 2^-90 and |x/s| >= 2^-11,
+ * and for every pair when s < 2^-90; smaller quotients agree in sign and lie
+ * below 2^-10, so their E4M3 codes are the same.  x, s, q: [n] FP32 device
+ * arrays.  The pages have no counterpart; it exists to test that division.
+ */
+JET_API jet_status jet_selftest_quotient(const float *x, const float *s, int64_t n, float *q,
+                                         jet_stream_t stream);
 
 #ifdef __cplusplus
 }

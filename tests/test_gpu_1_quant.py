@@ -155,3 +155,54 @@ def test_requant_empty(jet):
     qT, sT = jet.requant_128x1(torch.empty((0, 128), dtype=torch.uint8, device="cuda"),
                                torch.empty((1, 0), dtype=torch.float32, device="cuda"))
     assert qT.shape == (128, 0) and sT.shape == (0, 128)
+
+
+def _ieee_quotients(x, s):
+    with np.errstate(all="ignore"):
+        return (x.astype(np.float32) / s.astype(np.float32)).astype(np.float32)
+
+
+def test_division_routine_matches_ieee(jet):
+    """The quantizers' group division equals IEEE binary32 x / s where codes
+    can depend on it (and always in sign, with tiny quotients below 2^-10)."""
+    rng = np.random.default_rng(42)
+    n = 4_000_000
+    # x across the whole binary32 range, signed, with zeros and subnormals
+    x = (rng.standard_normal(n) * np.exp2(rng.uniform(-150, 100, n))).astype(np.float32)
+    x[::97] = 0.0
+    x[1::97] = -0.0
+    # s = fl32(amax / 448) with amax >= |x| in the same group sense
+    amax = (np.abs(x).astype(np.float64) * np.exp2(rng.uniform(0, 20, n))).astype(np.float32)
+    amax = np.maximum(amax, np.float32(1e-44))
+    s = (amax / np.float32(448)).astype(np.float32)
+    s[s == 0] = np.float32(1.0)
+    # boundary cases: quotients within a few ulps of every E4M3 rounding midpoint
+    tab = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()[:0x7F]
+    mids = ((tab[:-1] + tab[1:]) / 2).astype(np.float32)
+    sb = (np.exp2(rng.uniform(-80, 100, mids.size * 64)) / 448).astype(np.float32)
+    mb = np.repeat(mids, 64)
+    xb = (mb.astype(np.float64) * sb.astype(np.float64)).astype(np.float32)
+    steps = rng.integers(-3, 4, xb.size).astype(np.int32)
+    xb = (xb.view(np.int32) + steps).view(np.float32)
+    x = np.concatenate([x, xb, -xb])
+    s = np.concatenate([s, sb, sb])
+    q = jet.selftest_quotient(torch.from_numpy(x).cuda(), torch.from_numpy(s).cuda())
+    got = q.cpu().numpy()
+    want = _ieee_quotients(x, s)
+    exact_region = (s < np.float32(2.0 ** -90)) | (np.abs(want) >= np.float32(2.0 ** -11))
+    bad = np.flatnonzero(exact_region & (got.view(np.uint32) != want.view(np.uint32)))
+    assert bad.size == 0, (bad.size, x[bad[:3]], s[bad[:3]], got[bad[:3]], want[bad[:3]])
+    tiny = ~exact_region
+    assert (np.signbit(got[tiny]) == np.signbit(want[tiny])).all()
+    assert (np.abs(got[tiny]) < np.float32(2.0 ** -10)).all()
+    assert exact_region.sum() > 0.3 * x.size
+
+
+def test_act_near_division_fast_path_threshold(jet):
+    """Groups whose scale sits on either side of the fast-path threshold."""
+    M, K = 64, 256
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    amax_target = np.float32(448.0 * 2.0 ** -90) * np.exp2(rng.uniform(-3, 3, (M, 1))).astype(np.float32)
+    x = x / np.abs(x).max(axis=1, keepdims=True) * amax_target
+    check_act(jet, torch.from_numpy(x).to(torch.bfloat16))

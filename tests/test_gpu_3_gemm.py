@@ -94,19 +94,21 @@ def test_wgrad_single_linear(jet):
     run_wgrad(jet, c.dy, c.x)
 
 
-@pytest.mark.parametrize("M", [1, 16, 64, 100, 129, 256])
+@pytest.mark.parametrize("M", [1, 16, 64, 100, 129, 256, 300, 385])
 @pytest.mark.parametrize("N", [1024, 384, 128])
 def test_fwd_ragged_rows_and_widths(jet, M, N):
     run_fwd(jet, wl.activations(M, 512, seed=M, config=2), wl.weights(N, 512, seed=N, config=2))
 
 
-@pytest.mark.parametrize("M,N,K", [(200, 256, 384), (128, 128, 256), (256, 512, 128)])
+@pytest.mark.parametrize("M,N,K", [(200, 256, 384), (128, 128, 256), (256, 512, 128),
+                                   (384, 512, 512), (300, 256, 512)])
 def test_dgrad_shapes(jet, M, N, K):
     run_dgrad(jet, wl.grad_output(M, N, seed=M + N, config=3),
               wl.weights(N, K, seed=K, config=3))
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 384), (384, 128, 256), (256, 512, 512)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 384), (384, 128, 256), (256, 512, 512),
+                                   (256, 384, 512)])
 def test_wgrad_shapes(jet, M, N, K):
     run_wgrad(jet, wl.grad_output(M, N, seed=M + N, config=3),
               wl.activations(M, K, seed=K, config=3))
