@@ -231,6 +231,11 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         reg_dealloc<kRegsControl>();
         if (warp == 0) {
             // -------------------------------------------------- TMA producer
+            // The operand that every tile row (mode 0: B) or tile column
+            // (modes 1, 2: A) walks again is kept in L2; the other streams.
+            const uint64_t keep = policy_evict_last(), stream_once = policy_evict_first();
+            const uint64_t pol_a = raster.mode == 0 ? stream_once : keep;
+            const uint64_t pol_b = raster.mode == 0 ? keep : stream_once;
             uint32_t it = 0;
             bool ok = true;
             for (int t = unit0; ok && t < total; t += unit_step) {
@@ -279,23 +284,23 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             // which expects the pair's bytes.
                             const uint32_t fb = map_to_cta(&full_bar[s], 0);
                             if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * CF::kStageBytes);
-                            tma_load_2d_pair(a_s, &tmA, fb, kb * BK, m0);
+                            tma_load_2d_pair(a_s, &tmA, fb, kb * BK, m0, pol_a);
                             if (MODE == kDgrad)
                                 tma_load_2d_pair(b_s, &tmB, fb, n0 + CF::kBRows * (int)rank,
-                                                 kb * BK);
+                                                 kb * BK, pol_b);
                             else
                                 tma_load_2d_pair(b_s, &tmB, fb, kb * BK,
-                                                 n0 + CF::kBRows * (int)rank);
+                                                 n0 + CF::kBRows * (int)rank, pol_b);
                         } else {
                             mbar_arrive_expect_tx(&full_bar[s], CF::kStageBytes);
-                            tma_load_2d(a_s, &tmA, &full_bar[s], kb * BK, m0);
+                            tma_load_2d(a_s, &tmA, &full_bar[s], kb * BK, m0, pol_a);
                             if (MODE == kDgrad) {
 #pragma unroll
                                 for (int h = 0; h < BN / 128; ++h)
                                     tma_load_2d(b_s + h * 128 * BK, &tmB, &full_bar[s],
-                                                n0 + 128 * h, kb * BK);
+                                                n0 + 128 * h, kb * BK, pol_b);
                             } else {
-                                tma_load_2d(b_s, &tmB, &full_bar[s], kb * BK, n0);
+                                tma_load_2d(b_s, &tmB, &full_bar[s], kb * BK, n0, pol_b);
                             }
                         }
                     }
@@ -389,6 +394,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const int ew = warp - 4;
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
         const int ch = ew >> 2;     // column half
+        const uint64_t pol_out = policy_evict_first();  // outputs are not re-read here
         uint32_t tempty_remote[2] = {0u, 0u};
         if (kPair) {
             tempty_remote[0] = map_to_cta(&tempty_bar[0], 0);
@@ -486,7 +492,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     v.y = pack_bf16x2(acc[4 * i + 1].x, acc[4 * i + 1].y);
                     v.z = pack_bf16x2(acc[4 * i + 2].x, acc[4 * i + 2].y);
                     v.w = pack_bf16x2(acc[4 * i + 3].x, acc[4 * i + 3].y);
-                    dst[i] = v;
+                    st_global_v4_hint(dst + i, v, pol_out);
                 }
             }
         }

@@ -52,6 +52,7 @@ enum WaitSite : unsigned {
     SITE_GEMM_MMA_TMEM_EMPTY = 3,
     SITE_GEMM_EPI_TMEM_FULL = 4,
     SITE_GEMM_DRAIN = 5,
+    SITE_QUANT_STAGE = 6,
     SITE_TEST_NEVER_SET = 99,
 };
 

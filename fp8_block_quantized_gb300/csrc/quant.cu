@@ -9,7 +9,10 @@
 // group's amax by warp shuffles or shared memory, a correctly rounded divide
 // by the group scale (Markstein, below) and the saturating E4M3 conversion,
 // 8- or 16-byte stores.
+#include <cuda.h>
 #include <cuda_fp8.h>
+
+#include <mutex>
 
 #include "jet_common.cuh"
 #include "sm100_ptx.cuh"
@@ -135,70 +138,106 @@ __device__ __forceinline__ uint2 encode8(const float f[8], const Divisor &d) {
     return r;
 }
 
+// All three kernels stage their input tile in shared memory with one 2D TMA
+// load (box = the whole tile, no swizzle; rows past the end of the tensor are
+// zero-filled) completing on one mbarrier, then compute from shared memory.
+// Loads in flight cost no registers, so several tiles are in flight per SM.
+using jet::ptx::bulk_g2s;
+using jet::ptx::tma_load_2d;
+using jet::ptx::mbar_arrive_expect_tx;
+using jet::ptx::mbar_init;
+using jet::ptx::mbar_wait;
+using jet::ptx::smem_u32;
+
+// Inputs are read once: a plain (evict-normal) policy value for the hinted
+// TMA load.  createpolicy with fraction 0 yields the default policy.
+#define kStreamPolicy jet::ptx::policy_evict_first()
+
+__device__ __forceinline__ void stage_init(uint64_t *bar) {
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        jet::ptx::fence_mbar_init();
+    }
+    __syncthreads();
+}
+
 // ------------------------------------------------------------------ 1x128 --
-// CTA = 256 threads = 16 teams of 16 lanes; a team owns one 1x128 group at a
-// time (16 lanes x 8 BF16).  A CTA covers 64 rows of one K-block, four groups
-// per team, all four 16-byte loads issued before any arithmetic.  K-blocks are
-// the fast grid index, so CTAs running together read whole rows.
+// CTA = 256 threads = 16 teams of 16 lanes and one tile of 64 rows x one
+// K-block (16 KB of BF16, up to eight CTAs per SM).  A team owns one 1x128
+// group at a time (16 lanes x 8 BF16 read from shared memory); the group's
+// amax by shuffles within the team.  K-blocks are the fast grid index, so
+// CTAs running together read whole rows.
 constexpr int kActRowsPerCta = 64;
 
 __global__ void __launch_bounds__(256)
-quant_act_1x128_kernel(const uint16_t *__restrict__ x, int64_t M, int64_t K,
-                       uint8_t *__restrict__ q, float *__restrict__ s) {
-    const int team = threadIdx.x >> 4;
-    const int tl = threadIdx.x & 15;
+quant_act_1x128_kernel(const __grid_constant__ CUtensorMap tmx, int64_t M, int64_t K,
+                       uint8_t *__restrict__ q, float *__restrict__ s, unsigned *status) {
+    __shared__ __align__(128) uint16_t tile[kActRowsPerCta][128];
+    __shared__ uint64_t bar;
+    const int team = threadIdx.x >> 4, tl = threadIdx.x & 15;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t kb = blockIdx.x;
-    const int64_t m0 = (int64_t)blockIdx.y * kActRowsPerCta + team;
-    const int64_t col = kb * 128 + tl * 8;
-
-    uint4 v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int64_t m = m0 + 16 * j;
-        v[j] = m < M ? ld_stream16(x + m * K + col) : make_uint4(0, 0, 0, 0);
+    const int64_t mbase = (int64_t)blockIdx.y * kActRowsPerCta;
+    const int rows = (int)(M - mbase < kActRowsPerCta ? M - mbase : kActRowsPerCta);
+    stage_init(&bar);
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bar, (uint32_t)sizeof(tile));
+        tma_load_2d(smem_u32(&tile[0][0]), &tmx, &bar, (int32_t)(kb * 128), (int32_t)mbase,
+                    kStreamPolicy);
     }
+    (void)warp;
+    (void)lane;
+    if (!mbar_wait(&bar, 0, nullptr, status, jet::SITE_QUANT_STAGE)) return;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int64_t m = m0 + 16 * j;
+    for (int j = 0; j < kActRowsPerCta / 16; ++j) {
+        const int r = team + 16 * j;
+        const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r][tl * 8]);
         float f[8];
-        unpack8(v[j], f);
+        unpack8(v, f);
         float a = absmax8(f);
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-        const float sc = group_scale(a);
-        const Divisor d = make_divisor(sc);
-        if (m < M) {
-            *reinterpret_cast<uint2 *>(q + m * K + col) = encode8(f, d);
+        if (r < rows) {
+            const float sc = group_scale(a);
+            const Divisor d = make_divisor(sc);
+            const int64_t m = mbase + r;
+            *reinterpret_cast<uint2 *>(q + m * K + kb * 128 + tl * 8) = encode8(f, d);
             if (tl == 0) s[kb * M + m] = sc;
         }
     }
 }
 
 // ---------------------------------------------------------------- 128x128 --
-// One CTA per 128x128 block; each thread holds 64 values (eight 16-byte
-// loads); block amax by warp shuffle then shared memory.
+// One CTA per 128x128 block (32 KB of BF16 in shared memory, six CTAs per
+// SM).  Pass 1: each thread's 64 values -> block amax (shuffles, then
+// shared memory).  Pass 2: the same values re-read, quantized, stored.
 __global__ void __launch_bounds__(256)
-quant_w_128x128_kernel(const uint16_t *__restrict__ w, int64_t N, int64_t K,
-                       uint8_t *__restrict__ q, float *__restrict__ s) {
+quant_w_128x128_kernel(const __grid_constant__ CUtensorMap tmw, int64_t N, int64_t K,
+                       uint8_t *__restrict__ q, float *__restrict__ s, unsigned *status) {
+    extern __shared__ __align__(128) uint8_t wsm[];
+    uint16_t(*tile)[128] = reinterpret_cast<uint16_t(*)[128]>(wsm);
+    __shared__ uint64_t bar;
     __shared__ float warp_max[8];
     const int64_t kb = blockIdx.x, nb = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r0 = threadIdx.x >> 4, tl = threadIdx.x & 15;
-    const int64_t col = kb * 128 + tl * 8;
-    const int64_t row0 = nb * 128 + r0;
-
-    uint4 v[8];
-#pragma unroll
-    for (int p = 0; p < 8; ++p) v[p] = ld_stream16(w + (row0 + 16 * p) * K + col);
+    stage_init(&bar);
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bar, 128u * 256u);
+        tma_load_2d(smem_u32(&tile[0][0]), &tmw, &bar, (int32_t)(kb * 128), (int32_t)(nb * 128),
+                    kStreamPolicy);
+    }
+    if (!mbar_wait(&bar, 0, nullptr, status, jet::SITE_QUANT_STAGE)) return;
     float a = 0.0f;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
         float f[8];
-        unpack8(v[p], f);
+        unpack8(*reinterpret_cast<const uint4 *>(&tile[r0 + 16 * p][tl * 8]), f);
         a = fmaxf(a, absmax8(f));
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = a;
+    if (lane == 0) warp_max[warp] = a;
     __syncthreads();
     a = warp_max[0];
 #pragma unroll
@@ -208,56 +247,58 @@ quant_w_128x128_kernel(const uint16_t *__restrict__ w, int64_t N, int64_t K,
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
         float f[8];
-        unpack8(v[p], f);
-        *reinterpret_cast<uint2 *>(q + (row0 + 16 * p) * K + col) = encode8(f, d);
+        unpack8(*reinterpret_cast<const uint4 *>(&tile[r0 + 16 * p][tl * 8]), f);
+        *reinterpret_cast<uint2 *>(q + (nb * 128 + r0 + 16 * p) * K + kb * 128 + tl * 8) =
+            encode8(f, d);
     }
     if (threadIdx.x == 0) s[nb * (K / 128) + kb] = sc;
     (void)N;
 }
 
 // ------------------------------------------------------------------ 128x1 --
-// One CTA (8 warps) per (128 tokens x 128 columns) tile.  Lane l of warp w
-// owns columns 4l .. 4l+3 and tokens 16w .. 16w+15: it reads its 16 rows as
-// 4-byte words (each warp instruction reads one contiguous 128-byte row
-// segment), dequantizes v = fl32(D4(q) * s_row), reduces its column maxima
-// over its 16 tokens, meets the other 7 warps in shared memory for the
-// 128-token column amax, re-quantizes, and writes each column's 16 codes as
-// one 16-byte store into the transposed output.
-__global__ void __launch_bounds__(256)
-requant_128x1_kernel(const uint8_t *__restrict__ q, const float *__restrict__ s,
+// One CTA (8 warps) per (128 tokens x 128 columns) tile: 16 KB of codes and
+// the 128 row scales in shared memory (four CTAs per SM at 64 registers).  Lane l of
+// warp w owns columns 4l .. 4l+3 and tokens 16w .. 16w+15.  Pass 1 reads its
+// 16 words, dequantizes v = fl32(D4(q) * s_row) and reduces the column maxima
+// over its tokens; the 8 warps meet in shared memory for the 128-token
+// column amax.  Pass 2 re-reads, dequantizes two columns x 8 tokens at a
+// time, re-quantizes and writes each column's 8 codes as one 8-byte store
+// into the transposed output.
+__global__ void __launch_bounds__(256, 4)
+requant_128x1_kernel(const __grid_constant__ CUtensorMap tmq, const float *__restrict__ s,
                      int64_t M, int64_t K, uint8_t *__restrict__ qT,
-                     float *__restrict__ sT) {
+                     float *__restrict__ sT, unsigned *status) {
+    __shared__ __align__(128) uint32_t tile[128][32];  // [token][4 codes]
+    __shared__ __align__(16) float srow[128];
     __shared__ __align__(16) float col_max[8][128];
+    __shared__ uint64_t bar;
     const int64_t kb = blockIdx.x, mb = blockIdx.y;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t m0 = mb * 128 + w * 16;
-    const int64_t col = kb * 128 + lane * 4;
-
-    uint32_t code[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) code[i] = ld_stream4(q + (m0 + i) * K + col);
-    float srow[16];
-    const float4 *s4 = reinterpret_cast<const float4 *>(s + kb * M + m0);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 t = __ldg(s4 + i);
-        srow[4 * i + 0] = t.x; srow[4 * i + 1] = t.y;
-        srow[4 * i + 2] = t.z; srow[4 * i + 3] = t.w;
+    stage_init(&bar);
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bar, 128u * 128u + 512u);
+        tma_load_2d(smem_u32(&tile[0][0]), &tmq, &bar, (int32_t)(kb * 128), (int32_t)(mb * 128),
+                    kStreamPolicy);
+        bulk_g2s(smem_u32(srow), s + kb * M + mb * 128, 512u, &bar);
     }
+    if (!mbar_wait(&bar, 0, nullptr, status, jet::SITE_QUANT_STAGE)) return;
+    const int t0 = w * 16;
 
-    float v[4][16];  // [column][token]
+    // pass 1: column maxima of v = fl32(D4(q) * s_row)
     float amax[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
+        const uint32_t code = tile[t0 + i][lane];
         float d0, d1, d2, d3;
-        e4m3x2_to_f32(code[i], d0, d1);
-        e4m3x2_to_f32(code[i] >> 16, d2, d3);
-        const float2 sr = make_float2(srow[i], srow[i]);
+        e4m3x2_to_f32(code, d0, d1);
+        e4m3x2_to_f32(code >> 16, d2, d3);
+        const float2 sr = make_float2(srow[t0 + i], srow[t0 + i]);
         const float2 v01 = __fmul2_rn(make_float2(d0, d1), sr);
         const float2 v23 = __fmul2_rn(make_float2(d2, d3), sr);
-        v[0][i] = v01.x; v[1][i] = v01.y; v[2][i] = v23.x; v[3][i] = v23.y;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) amax[c] = fmaxf(amax[c], fabsf(v[c][i]));
+        amax[0] = fmaxf(amax[0], fabsf(v01.x));
+        amax[1] = fmaxf(amax[1], fabsf(v01.y));
+        amax[2] = fmaxf(amax[2], fabsf(v23.x));
+        amax[3] = fmaxf(amax[3], fabsf(v23.y));
     }
     *reinterpret_cast<float4 *>(&col_max[w][lane * 4]) =
         make_float4(amax[0], amax[1], amax[2], amax[3]);
@@ -270,19 +311,42 @@ requant_128x1_kernel(const uint8_t *__restrict__ q, const float *__restrict__ s,
     }
     float sc[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        sc[c] = group_scale(amax[c]);
-        const Divisor d = make_divisor(sc[c]);
-        uint32_t out[4];
+    for (int c = 0; c < 4; ++c) sc[c] = group_scale(amax[c]);
+
+    // pass 2: two columns x 8 tokens at a time
+    const int64_t col = kb * 128 + lane * 4;
+    const int64_t m0 = mb * 128 + t0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float q0, q1, q2, q3;
-            qdiv2(v[c][4 * j + 0], v[c][4 * j + 1], d, q0, q1);
-            qdiv2(v[c][4 * j + 2], v[c][4 * j + 3], d, q2, q3);
-            out[j] = e4m3x2(q0, q1) | (e4m3x2(q2, q3) << 16);
+    for (int cp = 0; cp < 2; ++cp) {
+        const Divisor d0 = make_divisor(sc[2 * cp]), d1 = make_divisor(sc[2 * cp + 1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float va[8], vb[8];  // column 2cp and 2cp+1, tokens 8h .. 8h+7
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = t0 + 8 * h + i;
+                float x0, x1;
+                e4m3x2_to_f32(tile[t][lane] >> (16 * cp), x0, x1);
+                const float2 v = __fmul2_rn(make_float2(x0, x1), make_float2(srow[t], srow[t]));
+                va[i] = v.x;
+                vb[i] = v.y;
+            }
+            uint32_t oa[2], ob[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float q0, q1, q2, q3;
+                qdiv2(va[4 * j + 0], va[4 * j + 1], d0, q0, q1);
+                qdiv2(va[4 * j + 2], va[4 * j + 3], d0, q2, q3);
+                oa[j] = e4m3x2(q0, q1) | (e4m3x2(q2, q3) << 16);
+                qdiv2(vb[4 * j + 0], vb[4 * j + 1], d1, q0, q1);
+                qdiv2(vb[4 * j + 2], vb[4 * j + 3], d1, q2, q3);
+                ob[j] = e4m3x2(q0, q1) | (e4m3x2(q2, q3) << 16);
+            }
+            *reinterpret_cast<uint2 *>(qT + (col + 2 * cp) * M + m0 + 8 * h) =
+                make_uint2(oa[0], oa[1]);
+            *reinterpret_cast<uint2 *>(qT + (col + 2 * cp + 1) * M + m0 + 8 * h) =
+                make_uint2(ob[0], ob[1]);
         }
-        *reinterpret_cast<uint4 *>(qT + (col + c) * M + m0) =
-            make_uint4(out[0], out[1], out[2], out[3]);
     }
     if (w == 0)
         *reinterpret_cast<float4 *>(sT + mb * K + col) = make_float4(sc[0], sc[1], sc[2], sc[3]);
@@ -295,6 +359,43 @@ __global__ void selftest_quotient_kernel(const float *__restrict__ x, const floa
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
         q[i] = qdiv(x[i], make_divisor(s[i]));
+}
+
+constexpr int kWTileBytes = 128 * 128 * 2;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// Row-major [outer][inner] tensor of 1- or 2-byte elements, box box_outer x
+// box_inner, no swizzle, zero fill outside.
+bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, uint32_t esize,
+              uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * esize};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -312,8 +413,13 @@ jet_status jet_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, uint8_t 
     jet_status st = jet::current_device(&dev);
     if (st != JET_OK) return st;
     if (empty) return JET_OK;
+    CUtensorMap tm;
+    if (!make_map(&tm, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)M, 128,
+                  kActRowsPerCta))
+        return JET_ERR_CUDA;
     dim3 grid((unsigned)(K / 128), (unsigned)((M + kActRowsPerCta - 1) / kActRowsPerCta));
-    quant_act_1x128_kernel<<<grid, 256, 0, jet::as_stream(stream)>>>(x, M, K, q, s);
+    quant_act_1x128_kernel<<<grid, 256, 0, jet::as_stream(stream)>>>(tm, M, K, q, s,
+                                                                     dev.status_word);
     return jet::launch_status();
 }
 
@@ -328,8 +434,22 @@ jet_status jet_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K, uint8_t 
     jet_status st = jet::current_device(&dev);
     if (st != JET_OK) return st;
     if (empty) return JET_OK;
+    static bool attr_set[64] = {};
+    if (!attr_set[dev.ordinal]) {
+        if (cudaFuncSetAttribute(quant_w_128x128_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kWTileBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return JET_ERR_CUDA;
+        }
+        attr_set[dev.ordinal] = true;
+    }
+    CUtensorMap tm;
+    if (!make_map(&tm, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)N, 128, 128))
+        return JET_ERR_CUDA;
     dim3 grid((unsigned)(K / 128), (unsigned)(N / 128));
-    quant_w_128x128_kernel<<<grid, 256, 0, jet::as_stream(stream)>>>(w, N, K, q, s);
+    quant_w_128x128_kernel<<<grid, 256, kWTileBytes, jet::as_stream(stream)>>>(tm, N, K, q, s,
+                                                                               dev.status_word);
     return jet::launch_status();
 }
 
@@ -346,8 +466,12 @@ jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M, int64_
     jet_status st = jet::current_device(&dev);
     if (st != JET_OK) return st;
     if (empty) return JET_OK;
+    CUtensorMap tm;
+    if (!make_map(&tm, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K, (uint64_t)M, 128, 128))
+        return JET_ERR_CUDA;
     dim3 grid((unsigned)(K / 128), (unsigned)(M / 128));
-    requant_128x1_kernel<<<grid, 256, 0, jet::as_stream(stream)>>>(q, s, M, K, qT, sT);
+    requant_128x1_kernel<<<grid, 256, 0, jet::as_stream(stream)>>>(tm, s, M, K, qT, sT,
+                                                                   dev.status_word);
     return jet::launch_status();
 }
 

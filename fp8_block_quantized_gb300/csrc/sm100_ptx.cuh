@@ -91,14 +91,59 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
 }
 
-// 2D tiled load of one box into shared memory; completion is signalled on
-// `bar` as transaction bytes.  x is the innermost coordinate.
+// L2 eviction policies for cache-hinted loads and stores.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 2D tiled load of one box into shared memory with an L2 eviction policy;
+// completion is signalled on `bar` as transaction bytes.  x is the
+// innermost coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap *m, uint64_t *bar,
-                                            int32_t x, int32_t y) {
+                                            int32_t x, int32_t y, uint64_t policy) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_dst),
-        "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_dst),
+        "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// Same load for a CTA pair (tcgen05 cta_group::2): the box lands in this
+// CTA's shared memory and its transaction bytes are signalled on `bar`, a
+// shared::cluster address that may belong to the peer CTA.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const CUtensorMap *m,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_dst),
+        "l"(m), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// 16-byte global store with an L2 eviction policy.
+__device__ __forceinline__ void st_global_v4_hint(void *p, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
+
+// 1D bulk copy global -> shared by the TMA engine; `bytes` (a multiple of
+// 16) complete as transaction bytes on `bar`.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_g2s(uint32_t smem_dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -120,18 +165,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
-}
-
-// Same load for a CTA pair (tcgen05 cta_group::2): the box lands in this
-// CTA's shared memory and its transaction bytes are signalled on `bar`, a
-// shared::cluster address that may belong to the peer CTA.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const CUtensorMap *m,
-                                                 uint32_t bar_cluster, int32_t x, int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_dst),
-        "l"(m), "r"(bar_cluster), "r"(x), "r"(y)
-        : "memory");
 }
 
 // ------------------------------------------------------------------ cluster
