@@ -69,14 +69,18 @@ struct Cfg {
     static constexpr int kABytes = BM * BK;
     static constexpr int kBBytes = kBRows * BK;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = kStageBytes <= 32 * 1024 ? 6 : 4;
+    static constexpr int kStages = 4;
     // Scale ring: per slice, the tile's 128 row scales and its column scales
     // (BN per-column values for wgrad, BN/128 block values otherwise).
     static constexpr int kScaleSlots = 8;
     static constexpr int kScaleRowBytes = BM * 4;
     static constexpr int kScaleSlotBytes = kScaleRowBytes + BN * 4;
-    static constexpr int kSmemBytes =
-        kStages * kStageBytes + kScaleSlots * kScaleSlotBytes + 1024;  // + alignment slack
+    // Output staging (pair kernel): each promotion warp's 32 x 128 BF16 block,
+    // 128-byte swizzled, written out by TMA stores.
+    static constexpr int kOutWarpBytes = 32 * 128 * 2;
+    static constexpr int kOutBytes = CL == 2 ? 8 * kOutWarpBytes : 0;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes +
+                                      kScaleSlots * kScaleSlotBytes + 1024;  // + alignment slack
     static constexpr int kTmemCols = 2 * BN;                           // two accumulators
     static constexpr int kHalf = BN / 2;  // columns per epilogue thread
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -160,7 +164,8 @@ __device__ __forceinline__ void load_cs(float4 (&cs)[4], const float *src) {
 template <int BN, int MODE, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const float *__restrict__ sa, const float *__restrict__ sb,
+                const __grid_constant__ CUtensorMap tmY, const float *__restrict__ sa,
+                const float *__restrict__ sb,
                 uint16_t *__restrict__ out, int R, int C, int D, Raster raster,
                 unsigned *status) {
     using CF = Cfg<BN, CL>;
@@ -176,7 +181,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t smem_base = (smem_u32(dyn_smem) + 1023u) & ~1023u;
-    const uint32_t scale_base = smem_base + S * CF::kStageBytes;
+    const uint32_t out_base = smem_base + S * CF::kStageBytes;  // 1024-aligned
+    const uint32_t scale_base = out_base + CF::kOutBytes;
     const int tiles_m = (R + BM - 1) / BM;
     const int tiles_n = C / BN;
     const int units_m = (tiles_m + CL - 1) / CL;  // row tiles per cluster step
@@ -483,7 +489,34 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
             }
             if (!ok) break;
-            if (row_ok) {
+            if (kPair) {
+                // Stage this warp's 32 rows x 128 columns (two 64-column boxes,
+                // 128-byte swizzle: 16-byte chunk j of row r goes to j ^ (r % 8))
+                // and hand them to the TMA; rows past R are clipped by it.
+                const uint32_t wbuf = out_base + ew * CF::kOutWarpBytes;
+                if (lane == 0) bulk_wait_group_read0();  // previous tile's stores have read it
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < H / 8; ++i) {
+                    uint4 v;
+                    v.x = pack_bf16x2(acc[4 * i + 0].x, acc[4 * i + 0].y);
+                    v.y = pack_bf16x2(acc[4 * i + 1].x, acc[4 * i + 1].y);
+                    v.z = pack_bf16x2(acc[4 * i + 2].x, acc[4 * i + 2].y);
+                    v.w = pack_bf16x2(acc[4 * i + 3].x, acc[4 * i + 3].y);
+                    const int half = i >> 3, chunk = i & 7;
+                    const uint32_t a = wbuf + half * 4096 + lane * 128 + ((chunk ^ (lane & 7)) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x),
+                                 "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmY, wbuf, col0, m0 + quad * 32);
+                    tma_store_2d(&tmY, wbuf + 4096, col0 + 64, m0 + quad * 32);
+                    bulk_commit_group();
+                }
+            } else if (row_ok) {
                 uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)row * C + col0);
 #pragma unroll
                 for (int i = 0; i < H / 8; ++i) {
@@ -498,6 +531,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
     }
 
+    // Outstanding TMA stores must finish reading shared memory before exit.
+    if (kPair && warp >= 4 && (threadIdx.x & 31) == 0) bulk_wait_group0();
     tc_fence_before();
     // Neither CTA of a pair may exit or free TMEM while the other can still
     // use its barriers, shared memory or the pair's TMEM allocation.
@@ -548,6 +583,20 @@ EncodeTiledFn encode_fn() {
         cudaGetLastError();
     });
     return fn;
+}
+
+// Row-major BF16 matrix [outer][inner] for the pair kernel's output stores:
+// box 32 rows x 64 columns (128 bytes), 128-byte swizzle.
+bool make_map_out(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Row-major uint8 matrix [outer][inner] with a box of box_outer x box_inner
@@ -616,8 +665,10 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
             max_units[dev.ordinal] = n;
         }
     }
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ty;
     if (!make_map_u8(&ta, a, (uint64_t)D, (uint64_t)R, BK, BM)) return JET_ERR_CUDA;
+    if (CL == 2 && !make_map_out(&ty, out, (uint64_t)C, (uint64_t)R)) return JET_ERR_CUDA;
+    if (CL == 1) ty = ta;  // unused by the single-CTA kernel
     bool okb = MODE == kDgrad ? make_map_u8(&tb, b, (uint64_t)C, (uint64_t)D, 128, BK)
                               : make_map_u8(&tb, b, (uint64_t)D, (uint64_t)C, BK, CF::kBRows);
     if (!okb) return JET_ERR_CUDA;
@@ -625,7 +676,8 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     const int64_t grid_units = units < max_units[dev.ordinal] ? units : max_units[dev.ordinal];
     cfg.gridDim = dim3((unsigned)(grid_units * CL));
     const Raster raster = choose_raster(R, C, D);
-    if (cudaLaunchKernelEx(&cfg, kernel, tmA_arg(ta), tmA_arg(tb), sa, sb, out, (int)R, (int)C,
+    if (cudaLaunchKernelEx(&cfg, kernel, tmA_arg(ta), tmA_arg(tb), tmA_arg(ty), sa, sb, out,
+                           (int)R, (int)C,
                            (int)D, raster, dev.status_word) != cudaSuccess) {
         cudaGetLastError();
         return JET_ERR_CUDA;
