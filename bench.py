@@ -67,6 +67,24 @@ def peaks():
 # clocks sampled during the timed region
 # --------------------------------------------------------------------------
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Maximum of a per-rank value over all ranks (the job's time is the slowest
+    rank's); identity for one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, amount_per_rank: float, ms_per_step_max: float, scale: float) -> float:
+    """Whole-job throughput of N replicas: every rank does `amount_per_rank`
+    per step; the step takes the slowest rank's time."""
+    return world * amount_per_rank / (ms_per_step_max * 1e-3) / scale
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -177,6 +195,11 @@ class LayerStep:
         # per linear: weight quant, fwd, dY quant, dgrad, dY requant, wgrad;
         # per distinct input: quant, requant; the metric: two passes
         self.launches_per_step = len(self.lin) * 6 + len(self.inputs) * 2 + 2
+        self.primary = ("TFLOP/s", self.flops)
+        self.config = {"workload": f"{kind}_layer_M{M}", "tokens": M,
+                       "linears": [(c.name, c.N, c.K) for c in self.cases],
+                       "gemm_tflop_per_step": round(self.flops / 1e12, 4),
+                       "l2": "no flush: per-step working set > 129 MB L2"}
 
     def calls(self):
         """The step as (family, thunk, shape label) in launch order."""
@@ -224,6 +247,150 @@ class LayerStep:
         return nbytes(self.h_in), nbytes(self.h_out)
 
 
+class RolloutStep:
+    """Forward only (rollout): 1x128 quantization of the 4 distinct inputs and
+    the 7 forward GEMMs of the 8B layer at M tokens; the weights are quantized
+    once beforehand (per weight sync) and not timed."""
+
+    def __init__(self, M: int, device, seed: int = 0):
+        import torch
+        from fp8_block_quantized_gb300 import workloads as wl
+        import fp8_block_quantized_gb300 as jet
+
+        self.jet, self.M = jet, M
+        self.cases = wl.training_layer("train8b", seed=seed, device=device, M=M, with_grad=False)
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        self.inputs, self.lin = {}, []
+        for c in self.cases:
+            key = wl.SHARED_INPUT[c.name]
+            if key not in self.inputs:
+                self.inputs[key] = {"x": c.x, "K": c.K, "q": e((M, c.K), torch.uint8),
+                                    "s": e((c.K // 128, M), torch.float32)}
+            c.key = key
+            qw, sw = jet.quant_w_128x128(c.w)
+            self.lin.append({"case": c, "qw": qw, "sw": sw,
+                             "y": e((M, c.N), torch.bfloat16)})
+        torch.cuda.synchronize()
+        self.flops = sum(2 * M * c.N * c.K for c in self.cases)
+        gemm_bytes = sum(M * c.K + c.N * c.K + 4 * (M * c.K // 128 + c.N * c.K // 16384)
+                         + 2 * M * c.N for c in self.cases)
+        self.work = {"gemm_fp8_fwd": self.flops, "gemm_fp8_fwd_bytes": gemm_bytes,
+                     "quant_act_1x128": sum(M * v["K"] for v in self.inputs.values())
+                     * BYTES_PER_ELEM["quant_act_1x128"]}
+        self.launches_per_step = len(self.lin) + len(self.inputs)
+        self.primary = ("TFLOP/s", self.flops)
+        self.config = {"workload": f"rollout8b_M{M}", "tokens": M,
+                       "linears": [(c.name, c.N, c.K) for c in self.cases],
+                       "gemm_tflop_per_step": round(self.flops / 1e12, 6),
+                       "l2": "weights (218 M codes) > 129 MB L2; activations may stay in L2"}
+
+    def calls(self):
+        j, out = self.jet, []
+        for v in self.inputs.values():
+            out.append(("quant_act_1x128", lambda v=v: j.jet_quant_act_1x128(v["x"], v["q"], v["s"]),
+                        "x%d" % v["K"]))
+        for L in self.lin:
+            v = self.inputs[L["case"].key]
+            out.append(("gemm_fp8_fwd", lambda L=L, v=v: j.jet_gemm_fp8_fwd(
+                v["q"], v["s"], L["qw"], L["sw"], L["y"]), L["case"].name))
+        return out
+
+    def host_io(self):
+        import torch
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        self.h_in = [(pin(v["x"]), v["x"]) for v in self.inputs.values()]
+        self.h_out = [(torch.empty(L["y"].shape, dtype=L["y"].dtype, pin_memory=True), L["y"])
+                      for L in self.lin]
+        nbytes = lambda pairs: sum(h.numel() * h.element_size() for h, _ in pairs)
+        return nbytes(self.h_in), nbytes(self.h_out)
+
+
+class SyncStep:
+    """Weight sync: 128x128 quantization of 32 layers of the 8B layer's 7
+    weights (6.98e9 parameters) and 1x128 quantization of a 16384 x 14336
+    Student-t(3) activation matrix."""
+
+    LAYERS = 32
+
+    def __init__(self, device, seed: int = 0):
+        import torch
+        from fp8_block_quantized_gb300 import workloads as wl
+        import fp8_block_quantized_gb300 as jet
+
+        self.jet, self.M = jet, 16384
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        self.w = []
+        for layer in range(self.LAYERS):
+            for i, (name, N, K) in enumerate(wl.LLAMA8B_LINEARS):
+                w = wl.weights(N, K, seed=seed, config=5, tensor_id=1000 + 10 * layer + i,
+                               device=device)
+                self.w.append({"name": f"L{layer}.{name}", "w": w,
+                               "q": e((N, K), torch.uint8),
+                               "s": e((N // 128, K // 128), torch.float32)})
+        self.x = wl.heavy_activations(16384, 14336, seed=seed, device=device)
+        self.xq = e((16384, 14336), torch.uint8)
+        self.xs = e((14336 // 128, 16384), torch.float32)
+        params = sum(t["w"].numel() for t in self.w)
+        self.work = {"quant_w_128x128": params * BYTES_PER_ELEM["quant_w_128x128"],
+                     "quant_act_1x128": self.x.numel() * BYTES_PER_ELEM["quant_act_1x128"]}
+        self.bytes = sum(self.work.values())
+        self.flops = 0
+        self.launches_per_step = len(self.w) + 1
+        self.primary = ("GB/s", self.bytes)
+        self.config = {"workload": "sync8b_32layers", "parameters": params,
+                       "activation": [16384, 14336],
+                       "l2": "no flush: 21 GB of weights and codes per step"}
+
+    def calls(self):
+        j = self.jet
+        out = [("quant_w_128x128", lambda t=t: j.jet_quant_w_128x128(t["w"], t["q"], t["s"]),
+                t["name"].split(".")[1]) for t in self.w]
+        out.append(("quant_act_1x128", lambda: j.jet_quant_act_1x128(self.x, self.xq, self.xs),
+                    "x16384x14336"))
+        return out
+
+
+class MetricStep:
+    """token-mult-prob-error over n = 4,194,304 tokens."""
+
+    def __init__(self, device, seed: int = 0, n: int = 4_194_304):
+        import torch
+        from fp8_block_quantized_gb300 import workloads as wl
+        import fp8_block_quantized_gb300 as jet
+
+        self.jet, self.M = jet, n
+        self.a, self.b = (t.to(device) for t in wl.logprobs(n, seed=seed))
+        self.out = torch.empty((1,), dtype=torch.float32, device=device)
+        self.ws = torch.empty((max(jet.workspace_bytes("token_mult_prob_error", n), 16),),
+                              dtype=torch.uint8, device=device)
+        # an L2-sized scratch written between steps so the 33.5 MB inputs are
+        # read from HBM every step
+        self.flush = torch.empty((256 << 20,), dtype=torch.uint8, device=device)
+        self.work = {"token_mult_prob_error": n * BYTES_PER_ELEM["token_mult_prob_error"]}
+        self.bytes = self.work["token_mult_prob_error"]
+        self.flops = 0
+        self.launches_per_step = 2
+        self.primary = ("GB/s", self.bytes)
+        self.config = {"workload": f"metric_n{n}", "tokens": n,
+                       "l2": "flushed: 256 MB written between steps, outside the kernel's events"}
+
+    def calls(self):
+        j = self.jet
+        return [("l2_flush", lambda: self.flush.fill_(1), "flush"),
+                ("token_mult_prob_error", lambda: j.jet_token_mult_prob_error(
+                    self.a, self.b, self.out, self.ws), "n")]
+
+
+def make_step(args, device, rank):
+    if args.workload in ("train8b", "train32b"):
+        return LayerStep(args.workload, device, seed=args.seed + rank)
+    if args.workload == "rollout":
+        return RolloutStep(args.tokens, device, seed=args.seed + rank)
+    if args.workload == "sync":
+        return SyncStep(device, seed=args.seed + rank)
+    return MetricStep(device, seed=args.seed + rank)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -240,7 +407,7 @@ def run_gpu(args):
     import fp8_block_quantized_gb300 as jet
     jet.load()
 
-    step = LayerStep(args.workload, device, seed=args.seed + rank)
+    step = make_step(args, device, rank)
     calls = step.calls()
     stream = torch.cuda.current_stream()
 
@@ -281,16 +448,20 @@ def run_gpu(args):
     code, word = jet.device_status()
     if code != 0:
         raise RuntimeError(f"device status {code} ({word:#x}) after timing")
-    if world > 1:
-        tt = torch.tensor([total_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world, device)
+    # the L2 flush between metric steps is excluded from the step time
+    flush_ms = fam_ms.pop("l2_flush", 0.0)
+    if flush_ms:
+        total_ms -= max_over_ranks(flush_ms, world, device)
+        detail_ms = {k: v for k, v in detail_ms.items() if k[0] != "l2_flush"}
     ms_per_step = total_ms / args.steps
-    value = world * step.flops / (ms_per_step * 1e-3) / 1e12
+    unit, amount = step.primary
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    value = job_rate(world, amount, ms_per_step, scale)
 
     # ---- end to end: pinned host inputs in, results out, through the same calls
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and hasattr(step, "host_io"):
         h2d, d2h = step.host_io()
 
         def e2e_step():
@@ -310,12 +481,8 @@ def run_gpu(args):
             e2e_step()
         e1.record(stream)
         barrier()
-        e_ms = e0.elapsed_time(e1) / e2e_steps
-        if world > 1:
-            tt = torch.tensor([e_ms], device=device)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": round(world * step.flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, device)
+        e2e = {"value": round(job_rate(world, amount, e_ms, scale), 2), "unit": unit,
                "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": e2e_steps}
 
@@ -336,7 +503,13 @@ def run_gpu(args):
     for fam, ms in fam_ms.items():
         avg_ms = ms / args.steps
         w = step.work[fam]
-        if fam.startswith("gemm"):
+        if fam.startswith("gemm") and fam + "_bytes" in step.work:
+            rate = w / (avg_ms * 1e-3) / 1e12
+            grate = step.work[fam + "_bytes"] / (avg_ms * 1e-3) / 1e9
+            kernels[fam] = {"ms_per_step": round(avg_ms, 4), "launches_per_step": launches[fam],
+                            "TFLOP/s": round(rate, 1), "frac_fp8_peak": round(rate / fp8_sust, 4),
+                            "GB/s": round(grate, 1), "frac_hbm": round(grate / hbm, 4)}
+        elif fam.startswith("gemm"):
             rate = w / (avg_ms * 1e-3) / 1e12
             kernels[fam] = {"ms_per_step": round(avg_ms, 4), "launches_per_step": launches[fam],
                             "TFLOP/s": round(rate, 1), "frac_fp8_peak": round(rate / fp8_sust, 4)}
@@ -347,7 +520,16 @@ def run_gpu(args):
     dom = max(fam_ms, key=fam_ms.get)
     dom_ms_launch = fam_ms[dom] / (args.steps * launches[dom])
     dom_work_launch = step.work[dom] / launches[dom]
-    if dom.startswith("gemm"):
+    # a GEMM whose arithmetic intensity is below the ridge point (dense FP8 /
+    # HBM) is bounded by streaming its operands: report it against HBM
+    hbm_bound_gemm = (dom.startswith("gemm") and dom + "_bytes" in step.work
+                      and step.work[dom] / step.work[dom + "_bytes"] < fp8_sust * 1e3 / hbm)
+    if hbm_bound_gemm:
+        ach = step.work[dom + "_bytes"] / launches[dom] / (dom_ms_launch * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(ach / hbm, 4),
+                "peak_note": f"{pk_kind} copy bandwidth; algorithmic bytes = codes + scales + BF16 out"}
+    elif dom.startswith("gemm"):
         ach = dom_work_launch / (dom_ms_launch * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_sust, 1),
                 "unit": "TFLOP/s", "frac": round(ach / fp8_sust, 4),
@@ -364,30 +546,28 @@ def run_gpu(args):
     gemm_ms = sum(fam_ms[f] for f in fam_ms if f.startswith("gemm")) / args.steps
 
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}_layer_M{step.M}", "tokens": step.M,
-                   "linears": [(c.name, c.N, c.K) for c in step.cases],
-                   "gemm_tflop_per_step": round(step.flops / 1e12, 4),
-                   "l2": "no flush: per-step working set > 129 MB L2",
-                   "parallelism": "replicas" if world > 1 else "single"},
-        "gemm_only": {"TFLOP/s": round(step.flops / (gemm_ms * 1e-3) / 1e12, 1),
-                      "frac_fp8_peak": round(step.flops / (gemm_ms * 1e-3) / 1e12 / fp8_sust, 4)},
-        "quantize": {"GB/s": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
-                     "frac_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / hbm, 4)},
+        "config": dict(step.config, parallelism="replicas" if world > 1 else "single"),
         "kernels": kernels,
         "roofline": roof,
         "gpu_launches": step.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if gemm_ms > 0:
+        g = step.flops / (gemm_ms * 1e-3) / 1e12
+        line["gemm_only"] = {"TFLOP/s": round(g, 1), "frac_fp8_peak": round(g / fp8_sust, 4)}
+    if q_ms > 0:
+        qr = q_bytes / (q_ms * 1e-3) / 1e9
+        line["quantize"] = {"GB/s": round(qr, 1), "frac_hbm": round(qr / hbm, 4)}
     if e2e is not None:
         line["e2e"] = e2e
     if args.detail:
         line["detail_ms_per_step"] = {f"{fam}/{label}": round(ms / args.steps, 4)
                                       for (fam, label), ms in detail_ms.items()}
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and args.workload in ("train8b", "train32b"):
         line["cpu_baseline"] = cpu_baseline(args.workload, seconds=args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -504,7 +684,11 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("jet", "reference"), default="jet")
-    ap.add_argument("--workload", choices=("train8b", "train32b"), default="train8b")
+    ap.add_argument("--workload", choices=("train8b", "train32b", "rollout", "sync", "metric"),
+                    default="train8b",
+                    help="train8b (default, the benchmark's workload), train32b, or the "
+                         "rollout / weight-sync / metric configurations")
+    ap.add_argument("--tokens", type=int, default=2048, help="M for --workload rollout")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
