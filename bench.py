@@ -268,8 +268,11 @@ class RolloutStep:
                                     "s": e((c.K // 128, M), torch.float32)}
             c.key = key
             qw, sw = jet.quant_w_128x128(c.w)
+            # split-contraction partials (M <= 128), allocated once, outside the timing
+            nws = jet.workspace_bytes("gemm_fp8_fwd", M, c.N, c.K)
             self.lin.append({"case": c, "qw": qw, "sw": sw,
-                             "y": e((M, c.N), torch.bfloat16)})
+                             "y": e((M, c.N), torch.bfloat16),
+                             "ws": e((nws,), torch.uint8) if nws else None})
         torch.cuda.synchronize()
         self.flops = sum(2 * M * c.N * c.K for c in self.cases)
         gemm_bytes = sum(M * c.K + c.N * c.K + 4 * (M * c.K // 128 + c.N * c.K // 16384)
@@ -277,7 +280,9 @@ class RolloutStep:
         self.work = {"gemm_fp8_fwd": self.flops, "gemm_fp8_fwd_bytes": gemm_bytes,
                      "quant_act_1x128": sum(M * v["K"] for v in self.inputs.values())
                      * BYTES_PER_ELEM["quant_act_1x128"]}
-        self.launches_per_step = len(self.lin) + len(self.inputs)
+        # a split GEMM is two launches: the partial tiles and their reduction
+        self.launches_per_step = (len(self.lin) + len(self.inputs)
+                                  + sum(L["ws"] is not None for L in self.lin))
         self.primary = ("TFLOP/s", self.flops)
         self.config = {"workload": f"rollout8b_M{M}", "tokens": M,
                        "linears": [(c.name, c.N, c.K) for c in self.cases],
@@ -292,7 +297,7 @@ class RolloutStep:
         for L in self.lin:
             v = self.inputs[L["case"].key]
             out.append(("gemm_fp8_fwd", lambda L=L, v=v: j.jet_gemm_fp8_fwd(
-                v["q"], v["s"], L["qw"], L["sw"], L["y"]), L["case"].name))
+                v["q"], v["s"], L["qw"], L["sw"], L["y"], ws=L["ws"]), L["case"].name))
         return out
 
     def host_io(self):

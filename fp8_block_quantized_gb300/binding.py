@@ -167,6 +167,8 @@ def jet_requant_128x1(q, s, qT, sT, stream=None):
 
 
 def _gemm(name, a, sa, b, sb, M, N, K, out, ws, stream):
+    if ws is None:  # the split-contraction partials of small-M products
+        ws = _ws(name[4:], M, N, K, out.device)
     ws_ptr, ws_bytes = (_ptr(ws), ws.numel() * ws.element_size()) if ws is not None else (ctypes.c_void_p(0), 0)
     _check(name, getattr(load(), name)(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K,
                                        _ptr(out), ws_ptr, ws_bytes, _stream(stream)))

@@ -36,6 +36,12 @@
 // K-major for forward and wgrad; for dgrad the weight codes qw[N][K] are read
 // as they are, MN-major (the output column contiguous), so no transposed copy
 // of the weights is needed.
+// Split contraction (one row tile only, i.e. at most 128 output rows, as in
+// rollout decode): a 128-row problem has only C/BN tiles, far fewer than the
+// 152 SMs, so the contraction is cut into `splits` contiguous ranges of
+// 128-slices, one work unit per (tile, range).  Each unit writes its FP32
+// partial tile to a caller-provided workspace [splits][R][C]; a second kernel
+// adds the partials in split order (deterministic) and rounds once to BF16.
 // Every mbarrier wait is bounded (see jet_common.cuh); a role that gives up
 // records JET_ERR_TIMEOUT, the others stop at their next wait, in-flight
 // copies and MMAs are drained and TMEM is freed before the kernel returns.
@@ -112,6 +118,17 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, Ras
     }
 }
 
+// Work unit t -> its tile and its range [kb0, kb1) of 128-slices.  The
+// `splits` ranges of one tile are consecutive units; each range is non-empty
+// because splits <= nkb.
+__device__ __forceinline__ void unit_coords(int t, int splits, int nkb, int tiles_m, int tiles_n,
+                                            Raster r, int &mt, int &nt, int &kb0, int &kb1) {
+    const int tile = t / splits, sp = t - tile * splits;
+    tile_coords(tile, tiles_m, tiles_n, r, mt, nt);
+    kb0 = sp * nkb / splits;
+    kb1 = (sp + 1) * nkb / splits;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -166,8 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const float *__restrict__ sa,
                 const float *__restrict__ sb,
-                uint16_t *__restrict__ out, int R, int C, int D, Raster raster,
-                unsigned *status) {
+                uint16_t *__restrict__ out, int R, int C, int D, Raster raster, int splits,
+                float *__restrict__ partial, unsigned *status) {
     using CF = Cfg<BN, CL>;
     constexpr int S = CF::kStages;
     constexpr int SS = CF::kScaleSlots;
@@ -186,7 +203,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int tiles_m = (R + BM - 1) / BM;
     const int tiles_n = C / BN;
     const int units_m = (tiles_m + CL - 1) / CL;  // row tiles per cluster step
-    const int total = units_m * tiles_n;
+    const int total = units_m * tiles_n * splits;  // work units: (tile, contraction range)
     const int nkb = D / BK;
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
@@ -245,10 +262,10 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t it = 0;
             bool ok = true;
             for (int t = unit0; ok && t < total; t += unit_step) {
-                int mu, nt;
-                tile_coords(t, units_m, tiles_n, raster, mu, nt);
+                int mu, nt, kb0, kb1;
+                unit_coords(t, splits, nkb, units_m, tiles_n, raster, mu, nt, kb0, kb1);
                 const int m0 = (mu * CL + (int)rank) * BM, n0 = nt * BN;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
                     const int ss = it % SS;
@@ -329,7 +346,9 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t it = 0;
             bool ok = true;
             for (int t = unit0; ok && t < total; t += unit_step) {
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                int mu, nt, kb0, kb1;
+                unit_coords(t, splits, nkb, units_m, tiles_n, raster, mu, nt, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
                     const int buf = it & 1;
@@ -409,8 +428,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         uint32_t it = 0;
         bool ok = true;
         for (int t = unit0; ok && t < total; t += unit_step) {
-            int mu, nt;
-            tile_coords(t, units_m, tiles_n, raster, mu, nt);
+            int mu, nt, kb0, kb1;
+            unit_coords(t, splits, nkb, units_m, tiles_n, raster, mu, nt, kb0, kb1);
             const int m0 = (mu * CL + (int)rank) * BM, n0 = nt * BN;
             const int row = m0 + quad * 32 + lane;
             const bool row_ok = row < R;
@@ -419,7 +438,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
             for (int i = 0; i < H / 2; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
-            for (int kb = 0; kb < nkb; ++kb, ++it) {
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int buf = it & 1;
                 const uint32_t tuse = it >> 1;
                 const int ss = it % SS;
@@ -516,6 +535,17 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     tma_store_2d(&tmY, wbuf + 4096, col0 + 64, m0 + quad * 32);
                     bulk_commit_group();
                 }
+            } else if (splits > 1) {
+                // FP32 partial of this contraction range (single-CTA kernel only)
+                if (row_ok) {
+                    const int sp = t % splits;
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        partial + ((size_t)sp * R + row) * C + col0);
+#pragma unroll
+                    for (int i = 0; i < H / 4; ++i)
+                        dst[i] = make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x,
+                                             acc[2 * i + 1].y);
+                }
             } else if (row_ok) {
                 uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)row * C + col0);
 #pragma unroll
@@ -546,6 +576,25 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             tmem_dealloc_pair(tmem, CF::kTmemCols);
         else
             tmem_dealloc(tmem, CF::kTmemCols);
+    }
+}
+
+// out[i] = BF16(sum over sp = 0 .. splits-1 of partial[sp][i]), summed in that
+// order; four elements per thread (R * C is a multiple of 128).
+__global__ void __launch_bounds__(256)
+splitk_reduce_kernel(const float4 *__restrict__ partial, int splits, int64_t n4,
+                     uint2 *__restrict__ out) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float4 a = partial[i];
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 b = partial[sp * n4 + i];
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        out[i] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
     }
 }
 
@@ -628,8 +677,8 @@ inline const CUtensorMap &tmA_arg(const CUtensorMap &m) { return m; }
 
 template <int BN, int MODE, int CL>
 jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, const uint8_t *b,
-                  const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D,
-                  cudaStream_t stream) {
+                  const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D, int splits,
+                  float *partial, cudaStream_t stream) {
     using CF = Cfg<BN, CL>;
     auto kernel = gemm_fp8_kernel<BN, MODE, CL>;
     static std::mutex mu;
@@ -672,22 +721,51 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     bool okb = MODE == kDgrad ? make_map_u8(&tb, b, (uint64_t)C, (uint64_t)D, 128, BK)
                               : make_map_u8(&tb, b, (uint64_t)D, (uint64_t)C, BK, CF::kBRows);
     if (!okb) return JET_ERR_CUDA;
-    const int64_t units = ((R + BM * CL - 1) / (BM * CL)) * (C / BN);
+    const int64_t units = ((R + BM * CL - 1) / (BM * CL)) * (C / BN) * splits;
     const int64_t grid_units = units < max_units[dev.ordinal] ? units : max_units[dev.ordinal];
     cfg.gridDim = dim3((unsigned)(grid_units * CL));
     const Raster raster = choose_raster(R, C, D);
     if (cudaLaunchKernelEx(&cfg, kernel, tmA_arg(ta), tmA_arg(tb), tmA_arg(ty), sa, sb, out,
-                           (int)R, (int)C,
-                           (int)D, raster, dev.status_word) != cudaSuccess) {
+                           (int)R, (int)C, (int)D, raster, splits, partial,
+                           dev.status_word) != cudaSuccess) {
         cudaGetLastError();
         return JET_ERR_CUDA;
+    }
+    if (splits > 1) {
+        const int64_t n4 = R * C / 4;
+        const int64_t want = (n4 + 255) / 256, cap = (int64_t)dev.num_sms * 8;
+        splitk_reduce_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, stream>>>(
+            reinterpret_cast<const float4 *>(partial), splits, n4, reinterpret_cast<uint2 *>(out));
     }
     return launch_status();
 }
 
+// Number of contraction ranges for an R x C x D product (1 = no split).  Only
+// a single row tile (R <= 128) is split, into at most as many ranges as fill
+// 152 SMs with one unit each, at most one range per 128-slice, and at most
+// D / (8 R) ranges so that the FP32 partials (written and read back:
+// 8 * splits * R * C bytes) cost no more traffic than the C x D codes.  It
+// depends only on the sizes, never on the device, so the workspace size and
+// the summation order (hence the result) are the same on every GPU.
+int splitk_splits(int64_t R, int64_t C, int64_t D) {
+    constexpr int64_t kUnits = 152;
+    if (R <= 0 || R > BM || C <= 0 || D <= 0 || C % 128 != 0 || D % BK != 0) return 1;
+    const int64_t tiles = C / (C % 256 == 0 ? 256 : 128);
+    int64_t s = kUnits / tiles;
+    const int64_t nkb = D / BK, by_bytes = D / (8 * R);
+    if (s > nkb) s = nkb;
+    if (s > by_bytes) s = by_bytes;
+    return s >= 2 ? (int)s : 1;
+}
+
+size_t splitk_workspace(int64_t R, int64_t C, int64_t D) {
+    const int s = splitk_splits(R, C, D);
+    return s > 1 ? (size_t)s * (size_t)R * (size_t)C * sizeof(float) : 0;
+}
+
 template <int MODE>
 jet_status run_gemm(const uint8_t *a, const float *sa, const uint8_t *b, const float *sb,
-                    uint16_t *out, int64_t R, int64_t C, int64_t D, jet_stream_t s) {
+                    uint16_t *out, int64_t R, int64_t C, int64_t D, void *ws, jet_stream_t s) {
     DeviceInfo dev;
     jet_status st = current_device(&dev);
     if (st != JET_OK) return st;
@@ -699,24 +777,32 @@ jet_status run_gemm(const uint8_t *a, const float *sa, const uint8_t *b, const f
     }
     // The pair MMA (256 x 256 per CTA pair) whenever there are at least two
     // row tiles and the output is a multiple of 256 wide.
+    const int splits = MODE == kWgrad ? 1 : splitk_splits(R, C, D);
+    float *partial = splits > 1 ? static_cast<float *>(ws) : nullptr;
     if (C % 256 == 0) {
-        if (R > BM) return launch<256, MODE, 2>(dev, a, sa, b, sb, out, R, C, D, stream);
-        return launch<256, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, stream);
+        if (R > BM) return launch<256, MODE, 2>(dev, a, sa, b, sb, out, R, C, D, 1, nullptr, stream);
+        return launch<256, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, splits, partial, stream);
     }
-    return launch<128, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, stream);
+    return launch<128, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, splits, partial, stream);
 }
 
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
 }  // namespace
 
+// Workspace bytes of a GEMM (JET_OP_GEMM_*), for jet_workspace_bytes().
+size_t jet_gemm_workspace(int op, int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return 0;
+    if (op == JET_OP_GEMM_FWD) return splitk_workspace(M, N, K);
+    if (op == JET_OP_GEMM_DGRAD) return splitk_workspace(M, K, N);
+    return 0;
+}
+
 extern "C" {
 
 jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx, const uint8_t *qw,
                             const float *sw, int64_t M, int64_t N, int64_t K, uint16_t *y,
                             void *ws, size_t ws_bytes, jet_stream_t stream) {
-    (void)ws;
-    (void)ws_bytes;
     JET_REQUIRE(M >= 0 && N >= 0 && K >= 0, JET_ERR_SHAPE);
     const bool out_empty = (M == 0 || N == 0), in_empty = out_empty || K == 0;
     JET_REQUIRE(out_empty || y, JET_ERR_NULL);
@@ -726,14 +812,15 @@ jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx, const uint8_t *q
     JET_REQUIRE(aligned16(qx) && aligned16(sx) && aligned16(qw) && aligned16(sw) &&
                     aligned16(y),
                 JET_ERR_ALIGN);
-    return run_gemm<kFwd>(qx, sx, qw, sw, y, M, N, K, stream);
+    JET_REQUIRE(aligned16(ws), JET_ERR_ALIGN);
+    const size_t need = splitk_workspace(M, N, K);
+    JET_REQUIRE(need == 0 || (ws && ws_bytes >= need), JET_ERR_WORKSPACE);
+    return run_gemm<kFwd>(qx, sx, qw, sw, y, M, N, K, ws, stream);
 }
 
 jet_status jet_gemm_fp8_dgrad(const uint8_t *qdy, const float *sdy, const uint8_t *qw,
                               const float *sw, int64_t M, int64_t N, int64_t K, uint16_t *dx,
                               void *ws, size_t ws_bytes, jet_stream_t stream) {
-    (void)ws;
-    (void)ws_bytes;
     JET_REQUIRE(M >= 0 && N >= 0 && K >= 0, JET_ERR_SHAPE);
     const bool out_empty = (M == 0 || K == 0), in_empty = out_empty || N == 0;
     JET_REQUIRE(out_empty || dx, JET_ERR_NULL);
@@ -743,13 +830,15 @@ jet_status jet_gemm_fp8_dgrad(const uint8_t *qdy, const float *sdy, const uint8_
     JET_REQUIRE(aligned16(qdy) && aligned16(sdy) && aligned16(qw) && aligned16(sw) &&
                     aligned16(dx),
                 JET_ERR_ALIGN);
-    return run_gemm<kDgrad>(qdy, sdy, qw, sw, dx, M, K, N, stream);
+    JET_REQUIRE(aligned16(ws), JET_ERR_ALIGN);
+    const size_t need = splitk_workspace(M, K, N);
+    JET_REQUIRE(need == 0 || (ws && ws_bytes >= need), JET_ERR_WORKSPACE);
+    return run_gemm<kDgrad>(qdy, sdy, qw, sw, dx, M, K, N, ws, stream);
 }
 
 jet_status jet_gemm_fp8_wgrad(const uint8_t *qdyT, const float *sdyT, const uint8_t *qxT,
                               const float *sxT, int64_t M, int64_t N, int64_t K, uint16_t *dw,
                               void *ws, size_t ws_bytes, jet_stream_t stream) {
-    (void)ws;
     (void)ws_bytes;
     JET_REQUIRE(M >= 0 && N >= 0 && K >= 0, JET_ERR_SHAPE);
     const bool out_empty = (N == 0 || K == 0), in_empty = out_empty || M == 0;
@@ -761,7 +850,7 @@ jet_status jet_gemm_fp8_wgrad(const uint8_t *qdyT, const float *sdyT, const uint
     JET_REQUIRE(aligned16(qdyT) && aligned16(sdyT) && aligned16(qxT) && aligned16(sxT) &&
                     aligned16(dw),
                 JET_ERR_ALIGN);
-    return run_gemm<kWgrad>(qdyT, sdyT, qxT, sxT, dw, N, K, M, stream);
+    return run_gemm<kWgrad>(qdyT, sdyT, qxT, sxT, dw, N, K, M, ws, stream);
 }
 
 jet_status jet_selftest_bounded_wait(uint32_t limit_us, jet_stream_t stream) {

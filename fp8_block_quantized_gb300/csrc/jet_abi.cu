@@ -60,6 +60,8 @@ jet_status current_device(DeviceInfo *info) {
 
 // Size of the per-block partial-sum array of the metric's first pass.
 int jet_metric_blocks(int64_t n);
+// FP32 partial tiles of a split-contraction GEMM (0 when it is not split).
+size_t jet_gemm_workspace(int op, int64_t M, int64_t N, int64_t K);
 
 extern "C" {
 
@@ -84,6 +86,9 @@ size_t jet_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
     switch (op) {
     case JET_OP_TOKEN_MULT_PROB_ERROR:
         return M > 0 ? (size_t)jet_metric_blocks(M) * sizeof(double) : 0;
+    case JET_OP_GEMM_FWD:
+    case JET_OP_GEMM_DGRAD:
+        return jet_gemm_workspace(op, M, N, K);
     default:
         return 0;
     }

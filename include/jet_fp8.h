@@ -132,8 +132,14 @@ JET_API jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M
  *   qx [M][K], sx [Kb][M] (jet_quant_act_1x128 of X);  M >= 0.
  *   qw [N][K], sw [Nb][Kb] (jet_quant_w_128x128 of W); N, K multiples of 128.
  *   y  [M][N] BF16 bits (out).  K == 0 writes zeros.
- *   ws / ws_bytes: workspace, at least jet_workspace_bytes(JET_OP_GEMM_FWD, ...)
- *   bytes (NULL/0 allowed when that is 0).
+ *   ws / ws_bytes: device workspace of at least
+ *   jet_workspace_bytes(JET_OP_GEMM_FWD, M, N, K) bytes, else JET_ERR_WORKSPACE
+ *   (NULL/0 allowed when that is 0).  It is non-zero only for M <= 128, where
+ *   the contraction is split into ranges whose FP32 partial tiles
+ *   [splits][M][N] go to ws and are then summed in a fixed order and rounded
+ *   once to BF16; the split depends only on (M, N, K), so results are the same
+ *   on every call and every device.  Its contents need no initialisation and
+ *   are scratch after the call; concurrent calls need separate workspaces.
  */
 JET_API jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx,
                             const uint8_t *qw, const float *sw, int64_t M,
@@ -148,6 +154,8 @@ JET_API jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx,
  *   qdy [M][N], sdy [Nb][M] (jet_quant_act_1x128 of dY with K := N).
  *   qw  [N][K], sw [Nb][Kb] (the forward weight codes, read transposed).
  *   dx  [M][K] BF16 bits (out).  N == 0 writes zeros.
+ *   ws / ws_bytes: as for the forward GEMM, with
+ *   jet_workspace_bytes(JET_OP_GEMM_DGRAD, M, N, K) (partials [splits][M][K]).
  */
 JET_API jet_status jet_gemm_fp8_dgrad(const uint8_t *qdy, const float *sdy,
                               const uint8_t *qw, const float *sw, int64_t M,
@@ -162,6 +170,7 @@ JET_API jet_status jet_gemm_fp8_dgrad(const uint8_t *qdy, const float *sdy,
  *   qdyT [N][M], sdyT [Mb][N]  (jet_requant_128x1 of dY's 1x128 form).
  *   qxT  [K][M], sxT  [Mb][K]  (jet_requant_128x1 of X's 1x128 form).
  *   dw   [N][K] BF16 bits (out).  M % 128 == 0; M == 0 writes zeros.
+ *   ws / ws_bytes: unused (jet_workspace_bytes(JET_OP_GEMM_WGRAD, ...) is 0).
  */
 JET_API jet_status jet_gemm_fp8_wgrad(const uint8_t *qdyT, const float *sdyT,
                               const uint8_t *qxT, const float *sxT, int64_t M,

@@ -51,6 +51,18 @@ def test_workspace_bytes(lib):
     for name in ("quant_act_1x128", "quant_w_128x128", "requant_128x1",
                  "gemm_fp8_fwd", "gemm_fp8_dgrad", "gemm_fp8_wgrad"):
         assert lib.jet_workspace_bytes(op[name], 8192, 4096, 4096) == 0
+    # split contraction for at most 128 output rows: FP32 partials [splits][R][C]
+    fwd, dgrad, wgrad = op["gemm_fp8_fwd"], op["gemm_fp8_dgrad"], op["gemm_fp8_wgrad"]
+    assert lib.jet_workspace_bytes(fwd, 1, 4096, 4096) == 9 * 1 * 4096 * 4      # 16 tiles
+    assert lib.jet_workspace_bytes(fwd, 64, 4096, 4096) == 8 * 64 * 4096 * 4    # K/(8M) = 8
+    assert lib.jet_workspace_bytes(fwd, 64, 14336, 4096) == 2 * 64 * 14336 * 4  # 56 tiles
+    assert lib.jet_workspace_bytes(fwd, 1, 1024, 4096) == 32 * 1024 * 4         # one per slice
+    assert lib.jet_workspace_bytes(fwd, 128, 128, 128) == 0                     # one slice
+    assert lib.jet_workspace_bytes(fwd, 129, 4096, 4096) == 0                   # two row tiles
+    assert lib.jet_workspace_bytes(fwd, 128, 4096, 1024) == 0                   # K/(8M) = 1
+    assert lib.jet_workspace_bytes(dgrad, 16, 4096, 1024) == 32 * 16 * 1024 * 4  # C = K = 1024
+    assert lib.jet_workspace_bytes(dgrad, 16, 1024, 4096) == 8 * 16 * 4096 * 4   # K/(8M) = 8
+    assert lib.jet_workspace_bytes(wgrad, 128, 128, 4096) == 0
     m = op["token_mult_prob_error"]
     assert lib.jet_workspace_bytes(m, 1, 0, 0) == 8
     assert lib.jet_workspace_bytes(m, 2048, 0, 0) == 8
@@ -105,6 +117,12 @@ def test_gemm_checks(lib, name):
     assert f(fake(MIS), fake(B), fake(C), fake(D), 128, 128, 128, fake(A), None, 0, None) == ALIGN
     if name == "jet_gemm_fp8_wgrad":      # the token axis must hold whole 128-groups
         assert f(*args, 100, 128, 128, fake(A), None, 0, None) == SHAPE
+    else:                                 # a split small-M product needs its partials
+        need = lib.jet_workspace_bytes(binding.OP[name[4:]], 16, 1024, 1024)
+        assert need > 0
+        assert f(*args, 16, 1024, 1024, fake(A), None, 0, None) == WORKSPACE
+        assert f(*args, 16, 1024, 1024, fake(A), fake(B), need - 16, None) == WORKSPACE
+        assert f(*args, 16, 1024, 1024, fake(A), fake(MIS), need, None) == ALIGN
 
 
 def test_metric_checks(lib):
@@ -130,6 +148,9 @@ def test_no_device_is_reported():
     assert lib.jet_quant_act_1x128(fake(A), 4, 128, fake(B), fake(C), None) == DEVICE
     assert lib.jet_gemm_fp8_fwd(fake(A), fake(B), fake(C), fake(D), 128, 128, 128,
                                 fake(A), None, 0, None) == DEVICE
+    need = lib.jet_workspace_bytes(binding.OP["gemm_fp8_fwd"], 16, 1024, 1024)
+    assert lib.jet_gemm_fp8_fwd(fake(A), fake(B), fake(C), fake(D), 16, 1024, 1024,
+                                fake(A), fake(B), need, None) == DEVICE
     assert lib.jet_device_status(None, None) == DEVICE
 
 

@@ -114,6 +114,34 @@ def test_wgrad_shapes(jet, M, N, K):
               wl.activations(M, K, seed=K, config=3))
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 512, 1024), (1, 4096, 1024), (100, 2048, 384),
+                                   (128, 4096, 1024)])
+def test_dgrad_small_rows_split_contraction(jet, M, N, K):
+    # at most 128 rows: the contraction (N) is split into ranges of 128-slices
+    assert jet.workspace_bytes("gemm_fp8_dgrad", M, N, K) > 0
+    run_dgrad(jet, wl.grad_output(M, N, seed=M + N, config=3), wl.weights(N, K, seed=K, config=3))
+
+
+def test_split_contraction_deterministic_and_workspace_agnostic(jet):
+    """Same bits on repeated calls, whatever the workspace held before."""
+    M, N, K = 16, 1024, 4096
+    need = jet.workspace_bytes("gemm_fp8_fwd", M, N, K)
+    assert need == 32 * M * N * 4
+    x, w = wl.activations(M, K, seed=11, config=2), wl.weights(N, K, seed=11, config=2)
+    qx, sx, qw, sw = (to_dev(a) for a in quant_pair(x, w))
+    outs = []
+    for fill in (0.0, float("nan"), 1e30):
+        ws = torch.full((need // 4,), fill, dtype=torch.float32, device="cuda")
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        jet.jet_gemm_fp8_fwd(qx, sx, qw, sw, y, ws=ws)
+        outs.append(y)
+    torch.cuda.synchronize()
+    for y in outs[1:]:
+        assert torch.equal(outs[0].view(torch.int16), y.view(torch.int16))
+    ref = oracle.gemm_fwd(*quant_pair(x, w))
+    assert_gemm_close(outs[0], ref, "fwd split")
+
+
 def test_zero_rows_are_exact_zero(jet):
     x = wl.activations(256, 384, seed=5, config=1).float()
     x[3] = 0.0
