@@ -396,6 +396,32 @@ def make_step(args, device, rank):
     return MetricStep(device, seed=args.seed + rank)
 
 
+def make_graphs(calls, steps, torch):
+    """(one-step graph, K-step graph with timing events, its events), or None
+    when this PyTorch cannot record events as graph nodes."""
+    try:
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
+        mk()
+    except TypeError:
+        return None
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g_step, g_detail = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=side):
+        for _, f, _ in calls:
+            f()
+    ev = [[(mk(), mk()) for _ in calls] for _ in range(steps)]
+    with torch.cuda.graph(g_detail, stream=side):
+        cur = torch.cuda.current_stream()
+        for k in range(steps):
+            for (_, f, _), (a, b) in zip(calls, ev[k]):
+                a.record(cur)
+                f()
+                b.record(cur)
+    torch.cuda.current_stream().wait_stream(side)
+    return g_step, g_detail, ev
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -428,22 +454,45 @@ def run_gpu(args):
     if code != 0:
         raise RuntimeError(f"device status {code} ({word:#x}) after warm-up")
 
-    # ---- timed region: K steps, per-kernel CUDA events on the launch stream
+    # ---- timed region.  The step's launches are captured once into a CUDA
+    # graph: host-side enqueue work (argument checks, tensor-map encoding,
+    # ctypes) then stays out of the timing, which matters for decode-sized
+    # steps whose kernels last a few microseconds.  `value` = K back-to-back
+    # replays of the one-step graph between two events; per-kernel times come
+    # from a second graph of K unrolled steps with an event-record node before
+    # and after every call (CUDA events recorded as graph nodes).
     fam_ms = {}
     detail_ms = {}
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in calls] for _ in range(args.steps)]
+    graphs = make_graphs(calls, args.steps, torch) if not args.no_graph else None
+    if graphs is not None:
+        g_step, g_detail, ev = graphs
+        launch_mode = "cuda_graph"
+    else:
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in calls] for _ in range(args.steps)]
+        launch_mode = "stream"
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     with ClockSampler(local) as clk:
-        t0.record(stream)
-        for k in range(args.steps):
-            for (fam, f, _), (a, b) in zip(calls, ev[k]):
-                a.record(stream)
-                f()
-                b.record(stream)
-        t1.record(stream)
-        barrier()
+        if graphs is not None:
+            g_step.replay()          # one untimed replay: graph upload
+            barrier()
+            t0.record(stream)
+            for k in range(args.steps):
+                g_step.replay()
+            t1.record(stream)
+            barrier()
+            g_detail.replay()
+            barrier()
+        else:
+            t0.record(stream)
+            for k in range(args.steps):
+                for (fam, f, _), (a, b) in zip(calls, ev[k]):
+                    a.record(stream)
+                    f()
+                    b.record(stream)
+            t1.record(stream)
+            barrier()
     total_ms = t0.elapsed_time(t1)
     for k in range(args.steps):
         for (fam, _, label), (a, b) in zip(calls, ev[k]):
@@ -555,7 +604,8 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
         "data": "synthetic",
-        "config": dict(step.config, parallelism="replicas" if world > 1 else "single"),
+        "config": dict(step.config, parallelism="replicas" if world > 1 else "single",
+                       launch=launch_mode),
         "kernels": kernels,
         "roofline": roof,
         "gpu_launches": step.launches_per_step * args.steps,
@@ -696,6 +746,9 @@ def main():
     ap.add_argument("--tokens", type=int, default=2048, help="M for --workload rollout")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every call from the host inside the timed region "
+                         "instead of replaying a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--detail", action="store_true",
