@@ -396,8 +396,10 @@ def make_step(args, device, rank):
     return MetricStep(device, seed=args.seed + rank)
 
 
-def make_graphs(calls, steps, torch):
-    """(one-step graph, K-step graph with timing events, its events), or None
+def make_graphs(calls, steps, torch, detail):
+    """The step captured as CUDA graphs: (one-step graph, {family: graph of
+    that family's calls of one step, in step order}, K-step graph with a
+    timing event around every call (only with `detail`), its events), or None
     when this PyTorch cannot record events as graph nodes."""
     try:
         mk = lambda: torch.cuda.Event(enable_timing=True, external=True)
@@ -406,20 +408,36 @@ def make_graphs(calls, steps, torch):
         return None
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
-    g_step, g_detail = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=side):
         for _, f, _ in calls:
             f()
-    ev = [[(mk(), mk()) for _ in calls] for _ in range(steps)]
-    with torch.cuda.graph(g_detail, stream=side):
-        cur = torch.cuda.current_stream()
-        for k in range(steps):
-            for (_, f, _), (a, b) in zip(calls, ev[k]):
-                a.record(cur)
-                f()
-                b.record(cur)
+    # A step that flushes L2 between its calls keeps the flush in front of
+    # every call of the other families' graphs too; its time is subtracted.
+    flush = [c[1] for c in calls if c[0] == "l2_flush"][:1]
+    g_fam = {}
+    for fam in dict.fromkeys(c[0] for c in calls):
+        g_fam[fam] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_fam[fam], stream=side):
+            for c in calls:
+                if c[0] == fam:
+                    if fam != "l2_flush":
+                        for f in flush:
+                            f()
+                    c[1]()
+    g_detail, ev = None, None
+    if detail:
+        g_detail = torch.cuda.CUDAGraph()
+        ev = [[(mk(), mk()) for _ in calls] for _ in range(steps)]
+        with torch.cuda.graph(g_detail, stream=side):
+            cur = torch.cuda.current_stream()
+            for k in range(steps):
+                for (_, f, _), (a, b) in zip(calls, ev[k]):
+                    a.record(cur)
+                    f()
+                    b.record(cur)
     torch.cuda.current_stream().wait_stream(side)
-    return g_step, g_detail, ev
+    return g_step, g_fam, g_detail, ev
 
 
 def run_gpu(args):
@@ -458,14 +476,18 @@ def run_gpu(args):
     # graph: host-side enqueue work (argument checks, tensor-map encoding,
     # ctypes) then stays out of the timing, which matters for decode-sized
     # steps whose kernels last a few microseconds.  `value` = K back-to-back
-    # replays of the one-step graph between two events; per-kernel times come
-    # from a second graph of K unrolled steps with an event-record node before
-    # and after every call (CUDA events recorded as graph nodes).
+    # replays of the one-step graph between two events.  Each kernel family's
+    # time = K replays of a graph holding that family's calls of one step (in
+    # step order, back to back) between two events: an event recorded between
+    # every pair of calls would itself add microseconds per call.  With
+    # --detail, a third graph of K unrolled steps with an event-record node
+    # around every call gives the per-call split (those include the nodes'
+    # own overhead).
     fam_ms = {}
     detail_ms = {}
-    graphs = make_graphs(calls, args.steps, torch) if not args.no_graph else None
+    graphs = make_graphs(calls, args.steps, torch, args.detail) if not args.no_graph else None
     if graphs is not None:
-        g_step, g_detail, ev = graphs
+        g_step, g_fam, g_detail, ev = graphs
         launch_mode = "cuda_graph"
     else:
         ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -476,13 +498,29 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         if graphs is not None:
             g_step.replay()          # one untimed replay: graph upload
+            for g in g_fam.values():
+                g.replay()
             barrier()
             t0.record(stream)
             for k in range(args.steps):
                 g_step.replay()
             t1.record(stream)
             barrier()
-            g_detail.replay()
+            for fam, g in g_fam.items():
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for k in range(args.steps):
+                    g.replay()
+                b.record(stream)
+                b.synchronize()
+                fam_ms[fam] = a.elapsed_time(b)
+            if "l2_flush" in fam_ms:
+                per_flush = fam_ms["l2_flush"] / sum(c[0] == "l2_flush" for c in calls)
+                for fam in fam_ms:
+                    if fam != "l2_flush":
+                        fam_ms[fam] -= per_flush * sum(c[0] == fam for c in calls)
+            if g_detail is not None:
+                g_detail.replay()
             barrier()
         else:
             t0.record(stream)
@@ -494,11 +532,15 @@ def run_gpu(args):
             t1.record(stream)
             barrier()
     total_ms = t0.elapsed_time(t1)
-    for k in range(args.steps):
-        for (fam, _, label), (a, b) in zip(calls, ev[k]):
-            ms = a.elapsed_time(b)
-            fam_ms[fam] = fam_ms.get(fam, 0.0) + ms
-            detail_ms[(fam, label)] = detail_ms.get((fam, label), 0.0) + ms
+    if ev is not None:
+        by_call = {}
+        for k in range(args.steps):
+            for (fam, _, label), (a, b) in zip(calls, ev[k]):
+                ms = a.elapsed_time(b)
+                by_call[fam] = by_call.get(fam, 0.0) + ms
+                detail_ms[(fam, label)] = detail_ms.get((fam, label), 0.0) + ms
+        if graphs is None:
+            fam_ms = by_call
     code, word = jet.device_status()
     if code != 0:
         raise RuntimeError(f"device status {code} ({word:#x}) after timing")

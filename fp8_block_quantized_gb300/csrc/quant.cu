@@ -5,10 +5,10 @@
 // section "为什么FP8适配线性层？": E4M3 codes, FP32 scale per group):
 //   amax = max |v|, s = amax / 448 (IEEE division, s = 1 if amax == 0),
 //   q = cvt.rn.satfinite.e4m3(fl32(v / s)).
-// Every kernel is a single pass over HBM: coalesced 16- or 4-byte loads, the
-// group's amax by warp shuffles or shared memory, a correctly rounded divide
-// by the group scale (Markstein, below) and the saturating E4M3 conversion,
-// 8- or 16-byte stores.
+// Every kernel is a single pass over HBM: TMA tile loads into shared memory,
+// the group's amax by warp shuffles and shared memory, a correctly rounded
+// divide by the group scale (Markstein, below) and the saturating E4M3
+// conversion, 16-byte stores.
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -20,33 +20,45 @@
 namespace {
 
 
-__device__ __forceinline__ uint4 ld_stream16(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+// ---------------------------------------------------------------------------
+// Conversions, written as the PTX cvt instructions they are.
+// ---------------------------------------------------------------------------
+
+// Four E4M3 codes (lowest byte first) -> four exact floats.
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t four, float &a, float &b, float &c,
+                                              float &d) {
+    asm("{\n\t.reg .b16 lo, hi, h0, h1, h2, h3;\n\t.reg .b32 p, q;\n\t"
+        "mov.b32 {lo, hi}, %4;\n\t"
+        "cvt.rn.f16x2.e4m3x2 p, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 q, hi;\n\t"
+        "mov.b32 {h0, h1}, p;\n\t"
+        "mov.b32 {h2, h3}, q;\n\t"
+        "cvt.f32.f16 %0, h0;\n\t"
+        "cvt.f32.f16 %1, h1;\n\t"
+        "cvt.f32.f16 %2, h2;\n\t"
+        "cvt.f32.f16 %3, h3;\n\t}"
+        : "=f"(a), "=f"(b), "=f"(c), "=f"(d)
+        : "r"(four));
 }
 
-__device__ __forceinline__ uint32_t ld_stream4(const void *p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
+// Four floats -> four E4M3 codes (a in the lowest byte): round to nearest
+// even, saturating at +-448.
+__device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float a, float b, float c, float d) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
-
-// Two E4M3 codes, `lo` in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
-
-// Two E4M3 codes (low byte first) -> two exact floats.
-__device__ __forceinline__ void e4m3x2_to_f32(uint32_t two, float &lo, float &hi) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
-    lo = __half2float(__half(__half_raw{h.x}));
-    hi = __half2float(__half(__half_raw{h.y}));
+// max(a, |b|, |c|) in one three-input max.
+__device__ __forceinline__ float max_abs2(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(fabsf(b)), "f"(fabsf(c)));
+    return r;
 }
 
 __device__ __forceinline__ float group_scale(float amax) {
@@ -67,81 +79,79 @@ __device__ __forceinline__ float group_scale(float amax) {
 // The theorem needs s, 1/s and the residual free of underflow.  s >= 2^-90
 // (amax >= 448 * 2^-90) keeps them so for every quotient >= 2^-11; smaller
 // quotients can differ from RN(x/s) only far below 2^-10, the smallest E4M3
-// rounding boundary, so their codes are the same.  copysign restores the sign
-// of zero quotients.  Groups with s < 2^-90 divide with __fdiv_rn.
+// rounding boundary, so their codes are the same.  Groups with s < 2^-90
+// divide with __fdiv_rn.
+//
+// The steps run on the negated operands nx = -x and ny = -y:
+//   q0 = RN(nx*ny), r' = q0*s + nx = -r (exact), q1 = RN(q0 + r'*ny), ...
+// which are the same values with the same roundings, but an exactly zero
+// residual now enters the sum as r'*ny with the sign that keeps q's sign of
+// zero (x = -0 gives q = -0), so no per-element sign fix-up is needed.
+// Callers produce -x directly (a negated scale in a product, or the sign bit
+// flipped while widening BF16).
 // ---------------------------------------------------------------------------
 struct Divisor {
-    float s, ns, y;
+    float s, ny;
     bool fast;
 };
 
 __device__ __forceinline__ Divisor make_divisor(float s) {
     Divisor d;
     d.s = s;
-    d.ns = -s;
     d.fast = s >= 0x1p-90f;
-    d.y = d.fast ? __frcp_rn(s) : 0.0f;
+    d.ny = d.fast ? -__frcp_rn(s) : 0.0f;
     return d;
 }
 
-__device__ __forceinline__ float qdiv(float x, const Divisor &d) {
-    if (!d.fast) return __fdiv_rn(x, d.s);
-    float q = __fmul_rn(x, d.y);
-    float r = __fmaf_rn(q, d.ns, x);
-    q = __fmaf_rn(r, d.y, q);
-    r = __fmaf_rn(q, d.ns, x);
-    q = __fmaf_rn(r, d.y, q);
-    return copysignf(q, x);
+// RN(x / s) from nx = -x.
+__device__ __forceinline__ float qdiv_neg(float nx, const Divisor &d) {
+    if (!d.fast) return __fdiv_rn(-nx, d.s);
+    float q = __fmul_rn(nx, d.ny);
+    float r = __fmaf_rn(q, d.s, nx);
+    q = __fmaf_rn(r, d.ny, q);
+    r = __fmaf_rn(q, d.s, nx);
+    q = __fmaf_rn(r, d.ny, q);
+    return q;
 }
 
-// Two quotients with packed f32x2 arithmetic (same steps as qdiv).
-__device__ __forceinline__ void qdiv2(float x0, float x1, const Divisor &d, float &q0, float &q1) {
-    if (!d.fast) {
-        q0 = __fdiv_rn(x0, d.s);
-        q1 = __fdiv_rn(x1, d.s);
-        return;
+// Two quotients with packed f32x2 arithmetic (same steps as qdiv_neg), for a
+// divisor known to take the fast path.
+__device__ __forceinline__ float2 qdiv2_neg_fast(float2 nx, const Divisor &d) {
+    const float2 ny = make_float2(d.ny, d.ny), s = make_float2(d.s, d.s);
+    float2 q = __fmul2_rn(nx, ny);
+    float2 r = __ffma2_rn(q, s, nx);
+    q = __ffma2_rn(r, ny, q);
+    r = __ffma2_rn(q, s, nx);
+    return __ffma2_rn(r, ny, q);
+}
+
+// Four negated values -> four codes of x / s.
+__device__ __forceinline__ uint32_t encode4_fast(const float *nf, const Divisor &d) {
+    const float2 a = qdiv2_neg_fast(make_float2(nf[0], nf[1]), d);
+    const float2 b = qdiv2_neg_fast(make_float2(nf[2], nf[3]), d);
+    return f32x4_to_e4m3x4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ uint32_t encode4(const float *nf, const Divisor &d) {
+    if (d.fast) return encode4_fast(nf, d);
+    return f32x4_to_e4m3x4(qdiv_neg(nf[0], d), qdiv_neg(nf[1], d), qdiv_neg(nf[2], d),
+                           qdiv_neg(nf[3], d));
+}
+
+// Eight BF16 values (one 16-byte load) -> eight negated floats (BF16 is the
+// upper half of a binary32; the sign bit is flipped on the way).
+__device__ __forceinline__ void unpack8_neg(const uint4 &v, float f[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float((w[i] << 16) + 0x80000000u);
+        f[2 * i + 1] = __uint_as_float((w[i] & 0xFFFF0000u) ^ 0x80000000u);
     }
-    const float2 x = make_float2(x0, x1), y = make_float2(d.y, d.y);
-    const float2 ns = make_float2(d.ns, d.ns);
-    float2 q = __fmul2_rn(x, y);
-    float2 r = __ffma2_rn(q, ns, x);
-    q = __ffma2_rn(r, y, q);
-    r = __ffma2_rn(q, ns, x);
-    q = __ffma2_rn(r, y, q);
-    q0 = copysignf(q.x, x0);
-    q1 = copysignf(q.y, x1);
 }
 
-// Eight BF16 values (one 16-byte load) -> eight floats.
-__device__ __forceinline__ void unpack8(const uint4 &v, float f[8]) {
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-}
-
-__device__ __forceinline__ float absmax8(const float f[8]) {
-    float a = fabsf(f[0]);
-#pragma unroll
-    for (int i = 1; i < 8; ++i) a = fmaxf(a, fabsf(f[i]));
-    return a;
-}
-
-// Eight quotients f[i] / s -> eight codes packed little-endian in a uint2.
-__device__ __forceinline__ uint2 encode8(const float f[8], const Divisor &d) {
-    float q[8];
-#pragma unroll
-    for (int i = 0; i < 8; i += 2) qdiv2(f[i], f[i + 1], d, q[i], q[i + 1]);
-    uint2 r;
-    r.x = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
-    r.y = e4m3x2(q[4], q[5]) | (e4m3x2(q[6], q[7]) << 16);
-    return r;
-}
-
-// All three kernels stage their input tile in shared memory with one 2D TMA
-// load (box = the whole tile, no swizzle; rows past the end of the tensor are
-// zero-filled) completing on one mbarrier, then compute from shared memory.
-// Loads in flight cost no registers, so several tiles are in flight per SM.
+// All three kernels stage their input tiles in shared memory by TMA (rows
+// past the end of the tensor are zero-filled) completing on an mbarrier, then
+// compute from shared memory.  Loads in flight cost no registers.
 using jet::ptx::bulk_g2s;
 using jet::ptx::tma_load_2d;
 using jet::ptx::mbar_arrive_expect_tx;
@@ -149,224 +159,389 @@ using jet::ptx::mbar_init;
 using jet::ptx::mbar_wait;
 using jet::ptx::smem_u32;
 
-// Inputs are read once: a plain (evict-normal) policy value for the hinted
-// TMA load.  createpolicy with fraction 0 yields the default policy.
+// Inputs are read once: they are loaded with the evict-first L2 policy.
 #define kStreamPolicy jet::ptx::policy_evict_first()
 
-__device__ __forceinline__ void stage_init(uint64_t *bar) {
+// 16-byte shared-memory load at a shared-window address.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// Address of 16-byte chunk `c` (0 .. 7) of row `r` in a box of 128-byte rows
+// loaded by TMA with the 128-byte swizzle (the box starts 1024-byte aligned):
+// the chunk sits at position c XOR (r mod 8) of its row.
+__device__ __forceinline__ uint32_t swz128(uint32_t box, int r, int c) {
+    return box + (uint32_t)r * 128u + ((uint32_t)(c ^ (r & 7)) << 4);
+}
+
+// The quantizers below are persistent: CTAs walk their tiles with a
+// two-stage ring; each tile arrives by TMA loads on the stage's mbarrier and
+// the load of the tile after next is issued as soon as the current tile has
+// been read into registers, so one load is always in flight per CTA while
+// another tile is computed.
+using jet::ptx::fence_proxy_async;
+
+// ------------------------------------------------------------------ 1x128 --
+// Tile = 64 rows x one K-block (128 BF16 = two 64-column boxes of 128-byte
+// rows with the 128-byte swizzle, 16 KB).  Four lanes per 1x128 group, 32
+// values each: lane tl of team r holds columns 16tl .. 16tl+15 of each box
+// (chunks 2tl and 2tl+1), read one chunk per box and step, so that the eight
+// lanes of every quarter-warp touch eight different bank groups (the
+// granularity at which 16-byte shared loads are served); the group's amax by
+// two shuffles, one scale and reciprocal per group, two 16-byte code stores.
+// Tiles are ordered K-block fastest so that CTAs running together read whole
+// rows.
+constexpr int kActRowsPerCta = 64;
+constexpr int kActBoxBytes = kActRowsPerCta * 128;
+constexpr int kActTileBytes = 2 * kActBoxBytes;
+constexpr int kActCtasPerSm = 4;
+constexpr int kActSmemBytes = 2 * kActTileBytes + 1024;
+
+__global__ void __launch_bounds__(256, kActCtasPerSm)
+quant_act_1x128_kernel(const __grid_constant__ CUtensorMap tmx, int64_t M, int64_t K,
+                       uint8_t *__restrict__ q, float *__restrict__ s, unsigned *status) {
+    extern __shared__ uint8_t act_smem[];
+    __shared__ uint64_t full[2];
+    const uint32_t base = (smem_u32(act_smem) + 1023u) & ~1023u;
+    const int row = threadIdx.x >> 2, tl = threadIdx.x & 3;
+    const int64_t nkb = K / 128;
+    const int64_t ntiles = (M + kActRowsPerCta - 1) / kActRowsPerCta * nkb;
+    const int64_t step = gridDim.x;
     if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
         jet::ptx::fence_mbar_init();
     }
     __syncthreads();
-}
-
-// ------------------------------------------------------------------ 1x128 --
-// CTA = 256 threads = 16 teams of 16 lanes and one tile of 64 rows x one
-// K-block (16 KB of BF16, up to eight CTAs per SM).  A team owns one 1x128
-// group at a time (16 lanes x 8 BF16 read from shared memory); the group's
-// amax by shuffles within the team.  K-blocks are the fast grid index, so
-// CTAs running together read whole rows.
-constexpr int kActRowsPerCta = 64;
-
-__global__ void __launch_bounds__(256)
-quant_act_1x128_kernel(const __grid_constant__ CUtensorMap tmx, int64_t M, int64_t K,
-                       uint8_t *__restrict__ q, float *__restrict__ s, unsigned *status) {
-    __shared__ __align__(128) uint16_t tile[kActRowsPerCta][128];
-    __shared__ uint64_t bar;
-    const int team = threadIdx.x >> 4, tl = threadIdx.x & 15;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t kb = blockIdx.x;
-    const int64_t mbase = (int64_t)blockIdx.y * kActRowsPerCta;
-    const int rows = (int)(M - mbase < kActRowsPerCta ? M - mbase : kActRowsPerCta);
-    stage_init(&bar);
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&bar, (uint32_t)sizeof(tile));
-        tma_load_2d(smem_u32(&tile[0][0]), &tmx, &bar, (int32_t)(kb * 128), (int32_t)mbase,
+    auto issue = [&](int st, int64_t t) {
+        const int64_t mb = t / nkb, kb = t - mb * nkb;
+        const uint32_t dst = base + st * kActTileBytes;
+        mbar_arrive_expect_tx(&full[st], kActTileBytes);
+        tma_load_2d(dst, &tmx, &full[st], (int32_t)(kb * 128), (int32_t)(mb * kActRowsPerCta),
                     kStreamPolicy);
-    }
-    (void)warp;
-    (void)lane;
-    if (!mbar_wait(&bar, 0, nullptr, status, jet::SITE_QUANT_STAGE)) return;
+        tma_load_2d(dst + kActBoxBytes, &tmx, &full[st], (int32_t)(kb * 128 + 64),
+                    (int32_t)(mb * kActRowsPerCta), kStreamPolicy);
+    };
+    int64_t issued = 0;
+    if (threadIdx.x == 0)
+        for (int j = 0; j < 2 && blockIdx.x + j * step < ntiles; ++j, ++issued)
+            issue(j, blockIdx.x + j * step);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles; t += step, ++it) {
+        const int st = it & 1;
+        // A wait that gave up is agreed on at the barrier below, before any
+        // global write; until then the (possibly incomplete) stage is only read.
+        ok = mbar_wait(&full[st], (it >> 1) & 1u, nullptr, status, jet::SITE_QUANT_STAGE);
+        const uint32_t tile = base + st * kActTileBytes;
+        float f[32];  // -x: columns 16tl .. 16tl+15, then 64+16tl .. 64+16tl+15
 #pragma unroll
-    for (int j = 0; j < kActRowsPerCta / 16; ++j) {
-        const int r = team + 16 * j;
-        const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r][tl * 8]);
-        float f[8];
-        unpack8(v, f);
-        float a = absmax8(f);
+        for (int k = 0; k < 4; ++k)
+            unpack8_neg(lds128(swz128(tile + (k >> 1) * kActBoxBytes, row, 2 * tl + (k & 1))),
+                        f + 8 * k);
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
+        if (threadIdx.x == 0 && t + 2 * step < ntiles) {
+            fence_proxy_async();
+            issue(st, t + 2 * step);
+            ++issued;
+        }
+        float a = 0.0f;
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-        if (r < rows) {
+        for (int i = 0; i < 32; i += 2) a = max_abs2(a, f[i], f[i + 1]);
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        const int64_t mb = t / nkb, kb = t - mb * nkb;
+        const int64_t m = mb * kActRowsPerCta + row;
+        if (m < M) {
             const float sc = group_scale(a);
             const Divisor d = make_divisor(sc);
-            const int64_t m = mbase + r;
-            *reinterpret_cast<uint2 *>(q + m * K + kb * 128 + tl * 8) = encode8(f, d);
+            uint32_t w[8];
+            if (d.fast) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = encode4_fast(f + 4 * i, d);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = encode4(f + 4 * i, d);
+            }
+            uint8_t *dst = q + m * K + kb * 128 + tl * 16;
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(dst + 64) = make_uint4(w[4], w[5], w[6], w[7]);
             if (tl == 0) s[kb * M + m] = sc;
         }
     }
+    // After a time-out, loads still in flight must land before the CTA exits.
+    if (!ok && threadIdx.x == 0)
+        for (int64_t j = it; j < issued; ++j)
+            mbar_wait(&full[j & 1], (uint32_t)(j >> 1) & 1u, nullptr, status,
+                      jet::SITE_QUANT_STAGE);
 }
 
 // ---------------------------------------------------------------- 128x128 --
-// One CTA per 128x128 block (32 KB of BF16 in shared memory, six CTAs per
-// SM).  Pass 1: each thread's 64 values -> block amax (shuffles, then
-// shared memory).  Pass 2: the same values re-read, quantized, stored.
-__global__ void __launch_bounds__(256)
+// Tile = one 128x128 block (two 64-column boxes, 128-byte swizzle, 32 KB).
+// Thread i holds row i/2, columns 64h .. 64h+63 (h = i%2, one box row) in
+// registers, reading chunk k XOR 4h at step k so that the two halves of a
+// quarter-warp fall on different bank groups; the block amax by shuffles and
+// a shared-memory exchange between the 8 warps, one scale and reciprocal per
+// block, 64 contiguous codes per thread.
+constexpr int kWBoxBytes = 128 * 128;
+constexpr int kWTileBytes = 2 * kWBoxBytes;
+constexpr int kWCtasPerSm = 2;
+constexpr int kWSmemBytes = 2 * kWTileBytes + 1024;
+
+__global__ void __launch_bounds__(256, kWCtasPerSm)
 quant_w_128x128_kernel(const __grid_constant__ CUtensorMap tmw, int64_t N, int64_t K,
                        uint8_t *__restrict__ q, float *__restrict__ s, unsigned *status) {
-    extern __shared__ __align__(128) uint8_t wsm[];
-    uint16_t(*tile)[128] = reinterpret_cast<uint16_t(*)[128]>(wsm);
-    __shared__ uint64_t bar;
-    __shared__ float warp_max[8];
-    const int64_t kb = blockIdx.x, nb = blockIdx.y;
+    extern __shared__ uint8_t w_smem[];
+    __shared__ uint64_t full[2];
+    __shared__ float warp_max[2][8];
+    const uint32_t base = (smem_u32(w_smem) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r0 = threadIdx.x >> 4, tl = threadIdx.x & 15;
-    stage_init(&bar);
+    const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int64_t nkb = K / 128;
+    const int64_t ntiles = (N / 128) * nkb;
+    const int64_t step = gridDim.x;
     if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&bar, 128u * 256u);
-        tma_load_2d(smem_u32(&tile[0][0]), &tmw, &bar, (int32_t)(kb * 128), (int32_t)(nb * 128),
-                    kStreamPolicy);
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        jet::ptx::fence_mbar_init();
     }
-    if (!mbar_wait(&bar, 0, nullptr, status, jet::SITE_QUANT_STAGE)) return;
-    float a = 0.0f;
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4 *>(&tile[r0 + 16 * p][tl * 8]), f);
-        a = fmaxf(a, absmax8(f));
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-    if (lane == 0) warp_max[warp] = a;
     __syncthreads();
-    a = warp_max[0];
+    auto issue = [&](int st, int64_t t) {
+        const int64_t nb = t / nkb, kb = t - nb * nkb;
+        const uint32_t dst = base + st * kWTileBytes;
+        mbar_arrive_expect_tx(&full[st], kWTileBytes);
+        tma_load_2d(dst, &tmw, &full[st], (int32_t)(kb * 128), (int32_t)(nb * 128),
+                    kStreamPolicy);
+        tma_load_2d(dst + kWBoxBytes, &tmw, &full[st], (int32_t)(kb * 128 + 64),
+                    (int32_t)(nb * 128), kStreamPolicy);
+    };
+    int64_t issued = 0;
+    if (threadIdx.x == 0)
+        for (int j = 0; j < 2 && blockIdx.x + j * step < ntiles; ++j, ++issued)
+            issue(j, blockIdx.x + j * step);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles; t += step, ++it) {
+        const int st = it & 1;
+        // A wait that gave up is agreed on at the barrier below, before any
+        // global write; until then the (possibly incomplete) stage is only read.
+        ok = mbar_wait(&full[st], (it >> 1) & 1u, nullptr, status, jet::SITE_QUANT_STAGE);
+        const uint32_t box = base + st * kWTileBytes + half * kWBoxBytes;
+        float f[64];  // -w; f[8k ..] holds chunk k ^ 4h of the row
 #pragma unroll
-    for (int i = 1; i < 8; ++i) a = fmaxf(a, warp_max[i]);
-    const float sc = group_scale(a);
-    const Divisor d = make_divisor(sc);
+        for (int k = 0; k < 8; ++k) unpack8_neg(lds128(swz128(box, row, k ^ (4 * half))), f + 8 * k);
+        float a = 0.0f;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4 *>(&tile[r0 + 16 * p][tl * 8]), f);
-        *reinterpret_cast<uint2 *>(q + (nb * 128 + r0 + 16 * p) * K + kb * 128 + tl * 8) =
-            encode8(f, d);
+        for (int i = 0; i < 64; i += 2) a = max_abs2(a, f[i], f[i + 1]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+        if (lane == 0) warp_max[it & 1][warp] = a;
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
+        if (threadIdx.x == 0 && t + 2 * step < ntiles) {
+            fence_proxy_async();
+            issue(st, t + 2 * step);
+            ++issued;
+        }
+        a = warp_max[it & 1][0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) a = fmaxf(a, warp_max[it & 1][i]);
+        const float sc = group_scale(a);
+        const Divisor d = make_divisor(sc);
+        const int64_t nb = t / nkb, kb = t - nb * nkb;
+        // f[16j ..] holds chunks 2(j ^ 2h) and 2(j ^ 2h) + 1: 16 bytes of codes
+        uint4 *dst = reinterpret_cast<uint4 *>(q + (nb * 128 + row) * K + kb * 128 + half * 64);
+        if (d.fast) {  // uniform over the block
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j ^ (2 * half)] =
+                    make_uint4(encode4_fast(f + 16 * j, d), encode4_fast(f + 16 * j + 4, d),
+                               encode4_fast(f + 16 * j + 8, d), encode4_fast(f + 16 * j + 12, d));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j ^ (2 * half)] =
+                    make_uint4(encode4(f + 16 * j, d), encode4(f + 16 * j + 4, d),
+                               encode4(f + 16 * j + 8, d), encode4(f + 16 * j + 12, d));
+        }
+        if (threadIdx.x == 0) s[nb * nkb + kb] = sc;
     }
-    if (threadIdx.x == 0) s[nb * (K / 128) + kb] = sc;
+    if (!ok && threadIdx.x == 0)
+        for (int64_t j = it; j < issued; ++j)
+            mbar_wait(&full[j & 1], (uint32_t)(j >> 1) & 1u, nullptr, status,
+                      jet::SITE_QUANT_STAGE);
     (void)N;
 }
 
 // ------------------------------------------------------------------ 128x1 --
-// One CTA (8 warps) per (128 tokens x 128 columns) tile: 16 KB of codes and
-// the 128 row scales in shared memory (four CTAs per SM at 64 registers).  Lane l of
-// warp w owns columns 4l .. 4l+3 and tokens 16w .. 16w+15.  Pass 1 reads its
-// 16 words, dequantizes v = fl32(D4(q) * s_row) and reduces the column maxima
-// over its tokens; the 8 warps meet in shared memory for the 128-token
-// column amax.  Pass 2 re-reads, dequantizes two columns x 8 tokens at a
-// time, re-quantizes and writes each column's 8 codes as one 8-byte store
-// into the transposed output.
-__global__ void __launch_bounds__(256, 4)
+// Persistent CTAs (two per SM, 256 threads) walk the (128 tokens x 128
+// columns) tiles with a two-stage ring: each tile's 16 KB of codes arrive by
+// one 2D TMA load and its 128 row scales by one bulk copy, both on the
+// stage's mbarrier, and the load of the tile after next is issued as soon as
+// the current tile has been read, so one tile is always in flight while
+// another is computed.  Lane l of warp w owns columns 4l .. 4l+3 and tokens
+// 16w .. 16w+15 (a warp reads one 128-byte token row per shared load, free
+// of bank conflicts).  Pass 1 dequantizes -v = fl32(D4(q) * -s_row) (the
+// negated product, exactly -v) into 64 registers and reduces the column
+// maxima over its tokens; the 8 warps meet in shared memory, where 128
+// threads turn the column maxima into the scales and their negated
+// reciprocals (one column each).  Pass 2 divides the register-held values,
+// converts, and writes each column's 16 codes as one 16-byte store into the
+// transposed output.
+constexpr int kRqThreads = 256;
+constexpr int kRqCtasPerSm = 2;
+
+__global__ void __launch_bounds__(kRqThreads, kRqCtasPerSm)
 requant_128x1_kernel(const __grid_constant__ CUtensorMap tmq, const float *__restrict__ s,
                      int64_t M, int64_t K, uint8_t *__restrict__ qT,
                      float *__restrict__ sT, unsigned *status) {
-    __shared__ __align__(128) uint32_t tile[128][32];  // [token][4 codes]
-    __shared__ __align__(16) float srow[128];
+    __shared__ __align__(128) uint32_t tile[2][128][32];  // [stage][token][4 codes]
+    __shared__ __align__(16) float srow[2][128];
     __shared__ __align__(16) float col_max[8][128];
-    __shared__ uint64_t bar;
-    const int64_t kb = blockIdx.x, mb = blockIdx.y;
+    __shared__ __align__(16) float col_s[128];
+    __shared__ __align__(16) float col_y[128];
+    __shared__ uint64_t full[2];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    stage_init(&bar);
+    const int64_t nkb = K / 128;
+    const int64_t ntiles = (M / 128) * nkb;
+    const int64_t step = gridDim.x;
     if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&bar, 128u * 128u + 512u);
-        tma_load_2d(smem_u32(&tile[0][0]), &tmq, &bar, (int32_t)(kb * 128), (int32_t)(mb * 128),
-                    kStreamPolicy);
-        bulk_g2s(smem_u32(srow), s + kb * M + mb * 128, 512u, &bar);
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        jet::ptx::fence_mbar_init();
     }
-    if (!mbar_wait(&bar, 0, nullptr, status, jet::SITE_QUANT_STAGE)) return;
-    const int t0 = w * 16;
-
-    // pass 1: column maxima of v = fl32(D4(q) * s_row)
-    float amax[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t code = tile[t0 + i][lane];
-        float d0, d1, d2, d3;
-        e4m3x2_to_f32(code, d0, d1);
-        e4m3x2_to_f32(code >> 16, d2, d3);
-        const float2 sr = make_float2(srow[t0 + i], srow[t0 + i]);
-        const float2 v01 = __fmul2_rn(make_float2(d0, d1), sr);
-        const float2 v23 = __fmul2_rn(make_float2(d2, d3), sr);
-        amax[0] = fmaxf(amax[0], fabsf(v01.x));
-        amax[1] = fmaxf(amax[1], fabsf(v01.y));
-        amax[2] = fmaxf(amax[2], fabsf(v23.x));
-        amax[3] = fmaxf(amax[3], fabsf(v23.y));
-    }
-    *reinterpret_cast<float4 *>(&col_max[w][lane * 4]) =
-        make_float4(amax[0], amax[1], amax[2], amax[3]);
     __syncthreads();
+    // Tile t = mb * nkb + kb: CTAs running together take neighbouring column
+    // blocks of the same 128 tokens.
+    auto issue = [&](int st, int64_t t) {
+        const int64_t mb = t / nkb, kb = t - mb * nkb;
+        mbar_arrive_expect_tx(&full[st], 128u * 128u + 512u);
+        tma_load_2d(smem_u32(&tile[st][0][0]), &tmq, &full[st], (int32_t)(kb * 128),
+                    (int32_t)(mb * 128), kStreamPolicy);
+        bulk_g2s(smem_u32(&srow[st][0]), s + kb * M + mb * 128, 512u, &full[st]);
+    };
+    int64_t issued = 0;  // loads issued (thread 0's count)
+    if (threadIdx.x == 0)
+        for (int j = 0; j < 2 && blockIdx.x + j * step < ntiles; ++j, ++issued)
+            issue(j, blockIdx.x + j * step);
+    const int t0 = w * 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles; t += step, ++it) {
+        const int st = it & 1;
+        // A wait that gave up is agreed on at the barrier below, before any
+        // global write; until then the (possibly incomplete) stage is only read.
+        ok = mbar_wait(&full[st], (it >> 1) & 1u, nullptr, status, jet::SITE_QUANT_STAGE);
+        // pass 1: v = fl32(D4(q) * s_row) into registers, column maxima
+        float v[4][16];
+        float amax[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float4 t = *reinterpret_cast<const float4 *>(&col_max[j][lane * 4]);
-        amax[0] = fmaxf(amax[0], t.x); amax[1] = fmaxf(amax[1], t.y);
-        amax[2] = fmaxf(amax[2], t.z); amax[3] = fmaxf(amax[3], t.w);
-    }
-    float sc[4];
+        for (int i = 0; i < 16; i += 4) {
+            const float4 sr4 = *reinterpret_cast<const float4 *>(&srow[st][t0 + i]);
+            const float sr[4] = {sr4.x, sr4.y, sr4.z, sr4.w};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) sc[c] = group_scale(amax[c]);
-
-    // pass 2: two columns x 8 tokens at a time
-    const int64_t col = kb * 128 + lane * 4;
-    const int64_t m0 = mb * 128 + t0;
-#pragma unroll
-    for (int cp = 0; cp < 2; ++cp) {
-        const Divisor d0 = make_divisor(sc[2 * cp]), d1 = make_divisor(sc[2 * cp + 1]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float va[8], vb[8];  // column 2cp and 2cp+1, tokens 8h .. 8h+7
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = t0 + 8 * h + i;
-                float x0, x1;
-                e4m3x2_to_f32(tile[t][lane] >> (16 * cp), x0, x1);
-                const float2 v = __fmul2_rn(make_float2(x0, x1), make_float2(srow[t], srow[t]));
-                va[i] = v.x;
-                vb[i] = v.y;
+            for (int u = 0; u < 4; ++u) {
+                float d0, d1, d2, d3;
+                e4m3x4_to_f32(tile[st][t0 + i + u][lane], d0, d1, d2, d3);
+                const float2 s2 = make_float2(-sr[u], -sr[u]);
+                const float2 a = __fmul2_rn(make_float2(d0, d1), s2);
+                const float2 b = __fmul2_rn(make_float2(d2, d3), s2);
+                v[0][i + u] = a.x;
+                v[1][i + u] = a.y;
+                v[2][i + u] = b.x;
+                v[3][i + u] = b.y;
             }
-            uint32_t oa[2], ob[2];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float q0, q1, q2, q3;
-                qdiv2(va[4 * j + 0], va[4 * j + 1], d0, q0, q1);
-                qdiv2(va[4 * j + 2], va[4 * j + 3], d0, q2, q3);
-                oa[j] = e4m3x2(q0, q1) | (e4m3x2(q2, q3) << 16);
-                qdiv2(vb[4 * j + 0], vb[4 * j + 1], d1, q0, q1);
-                qdiv2(vb[4 * j + 2], vb[4 * j + 3], d1, q2, q3);
-                ob[j] = e4m3x2(q0, q1) | (e4m3x2(q2, q3) << 16);
+            for (int j = 0; j < 4; ++j) {
+                amax[j] = max_abs2(amax[j], v[j][i], v[j][i + 1]);
+                amax[j] = max_abs2(amax[j], v[j][i + 2], v[j][i + 3]);
             }
-            *reinterpret_cast<uint2 *>(qT + (col + 2 * cp) * M + m0 + 8 * h) =
-                make_uint2(oa[0], oa[1]);
-            *reinterpret_cast<uint2 *>(qT + (col + 2 * cp + 1) * M + m0 + 8 * h) =
-                make_uint2(ob[0], ob[1]);
         }
+        *reinterpret_cast<float4 *>(&col_max[w][lane * 4]) =
+            make_float4(amax[0], amax[1], amax[2], amax[3]);
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
+        // The stage has been read: refill it with the tile after next.
+        if (threadIdx.x == 0 && t + 2 * step < ntiles) {
+            jet::ptx::fence_proxy_async();
+            issue(st, t + 2 * step);
+            ++issued;
+        }
+        bool fast = true;
+        if (threadIdx.x < 128) {
+            float a = col_max[0][threadIdx.x];
+#pragma unroll
+            for (int j = 1; j < 8; ++j) a = fmaxf(a, col_max[j][threadIdx.x]);
+            const float sc = group_scale(a);
+            const Divisor d = make_divisor(sc);
+            col_s[threadIdx.x] = sc;
+            col_y[threadIdx.x] = d.ny;
+            fast = d.fast;
+        }
+        // Tiles whose every column takes the fast division (all but the
+        // tiniest data) run pass 2 without a per-column test.
+        fast = __syncthreads_and(fast);
+        // pass 2: quotients, codes, one 16-byte store per column
+        const float4 s4 = *reinterpret_cast<const float4 *>(&col_s[lane * 4]);
+        const float4 y4 = *reinterpret_cast<const float4 *>(&col_y[lane * 4]);
+        const float scs[4] = {s4.x, s4.y, s4.z, s4.w};
+        const float ys[4] = {y4.x, y4.y, y4.z, y4.w};
+        const int64_t mb = t / nkb, kb = t - mb * nkb;
+        const int64_t col = kb * 128 + lane * 4;
+        uint8_t *dst = qT + col * M + mb * 128 + t0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            Divisor d;
+            d.s = scs[j];
+            d.ny = ys[j];
+            d.fast = scs[j] >= 0x1p-90f;
+            uint32_t o[4];
+            if (fast) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) o[g] = encode4_fast(&v[j][4 * g], d);
+            } else {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) o[g] = encode4(&v[j][4 * g], d);
+            }
+            *reinterpret_cast<uint4 *>(dst + (int64_t)j * M) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (w == 0) *reinterpret_cast<float4 *>(sT + mb * K + col) = s4;
     }
-    if (w == 0)
-        *reinterpret_cast<float4 *>(sT + mb * K + col) = make_float4(sc[0], sc[1], sc[2], sc[3]);
+    // After a time-out, loads still in flight must land before the CTA exits.
+    if (!ok && threadIdx.x == 0)
+        for (int64_t j = it; j < issued; ++j)
+            mbar_wait(&full[j & 1], (uint32_t)(j >> 1) & 1u, nullptr, status,
+                      jet::SITE_QUANT_STAGE);
 }
 
 // Self-test of the division used above: q[i] = x[i] / s[i] through
-// make_divisor + qdiv, the same path the quantizers take for a group scale.
+// make_divisor + qdiv_neg, the same steps the quantizers take for a group
+// scale.
 __global__ void selftest_quotient_kernel(const float *__restrict__ x, const float *__restrict__ s,
                                          int64_t n, float *__restrict__ q) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
-        q[i] = qdiv(x[i], make_divisor(s[i]));
+        q[i] = qdiv_neg(-x[i], make_divisor(s[i]));
 }
-
-constexpr int kWTileBytes = 128 * 128 * 2;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// TMA coordinates are 32-bit: every tensor extent stays below 2^31.
+constexpr int64_t kMaxRows = (int64_t)1 << 31;
 
 EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = nullptr;
@@ -384,9 +559,10 @@ EncodeTiledFn encode_fn() {
 }
 
 // Row-major [outer][inner] tensor of 1- or 2-byte elements, box box_outer x
-// box_inner, no swizzle, zero fill outside.
+// box_inner, zero fill outside (no swizzle unless asked).
 bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, uint32_t esize,
-              uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+              uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -394,8 +570,8 @@ bool make_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, uint32
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, type, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -407,19 +583,20 @@ jet_status jet_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, uint8_t 
     JET_REQUIRE(M >= 0 && K >= 0, JET_ERR_SHAPE);
     const bool empty = (M == 0 || K == 0);
     JET_REQUIRE(empty || (x && q && s), JET_ERR_NULL);
-    JET_REQUIRE(K % 128 == 0 && (M + kActRowsPerCta - 1) / kActRowsPerCta <= 65535, JET_ERR_SHAPE);
+    JET_REQUIRE(K % 128 == 0 && M < kMaxRows && K < kMaxRows, JET_ERR_SHAPE);
     JET_REQUIRE(jet::aligned16(x) && jet::aligned16(q) && jet::aligned16(s), JET_ERR_ALIGN);
     jet::DeviceInfo dev;
     jet_status st = jet::current_device(&dev);
     if (st != JET_OK) return st;
     if (empty) return JET_OK;
     CUtensorMap tm;
-    if (!make_map(&tm, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)M, 128,
-                  kActRowsPerCta))
+    if (!make_map(&tm, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)M, 64,
+                  kActRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B))
         return JET_ERR_CUDA;
-    dim3 grid((unsigned)(K / 128), (unsigned)((M + kActRowsPerCta - 1) / kActRowsPerCta));
-    quant_act_1x128_kernel<<<grid, 256, 0, jet::as_stream(stream)>>>(tm, M, K, q, s,
-                                                                     dev.status_word);
+    const int64_t tiles = (M + kActRowsPerCta - 1) / kActRowsPerCta * (K / 128);
+    const int64_t cap = (int64_t)dev.num_sms * kActCtasPerSm;
+    quant_act_1x128_kernel<<<(unsigned)(tiles < cap ? tiles : cap), 256, kActSmemBytes,
+                             jet::as_stream(stream)>>>(tm, M, K, q, s, dev.status_word);
     return jet::launch_status();
 }
 
@@ -428,7 +605,7 @@ jet_status jet_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K, uint8_t 
     JET_REQUIRE(N >= 0 && K >= 0, JET_ERR_SHAPE);
     const bool empty = (N == 0 || K == 0);
     JET_REQUIRE(empty || (w && q && s), JET_ERR_NULL);
-    JET_REQUIRE(N % 128 == 0 && K % 128 == 0 && N / 128 <= 65535, JET_ERR_SHAPE);
+    JET_REQUIRE(N % 128 == 0 && K % 128 == 0 && N < kMaxRows && K < kMaxRows, JET_ERR_SHAPE);
     JET_REQUIRE(jet::aligned16(w) && jet::aligned16(q) && jet::aligned16(s), JET_ERR_ALIGN);
     jet::DeviceInfo dev;
     jet_status st = jet::current_device(&dev);
@@ -438,18 +615,20 @@ jet_status jet_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K, uint8_t 
     if (!attr_set[dev.ordinal]) {
         if (cudaFuncSetAttribute(quant_w_128x128_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kWTileBytes) != cudaSuccess) {
+                                 kWSmemBytes) != cudaSuccess) {
             cudaGetLastError();
             return JET_ERR_CUDA;
         }
         attr_set[dev.ordinal] = true;
     }
     CUtensorMap tm;
-    if (!make_map(&tm, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)N, 128, 128))
+    if (!make_map(&tm, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)N, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return JET_ERR_CUDA;
-    dim3 grid((unsigned)(K / 128), (unsigned)(N / 128));
-    quant_w_128x128_kernel<<<grid, 256, kWTileBytes, jet::as_stream(stream)>>>(tm, N, K, q, s,
-                                                                               dev.status_word);
+    const int64_t tiles = (N / 128) * (K / 128);
+    const int64_t cap = (int64_t)dev.num_sms * kWCtasPerSm;
+    quant_w_128x128_kernel<<<(unsigned)(tiles < cap ? tiles : cap), 256, kWSmemBytes,
+                             jet::as_stream(stream)>>>(tm, N, K, q, s, dev.status_word);
     return jet::launch_status();
 }
 
@@ -458,7 +637,7 @@ jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M, int64_
     JET_REQUIRE(M >= 0 && K >= 0, JET_ERR_SHAPE);
     const bool empty = (M == 0 || K == 0);
     JET_REQUIRE(empty || (q && s && qT && sT), JET_ERR_NULL);
-    JET_REQUIRE(M % 128 == 0 && K % 128 == 0 && M / 128 <= 65535, JET_ERR_SHAPE);
+    JET_REQUIRE(M % 128 == 0 && K % 128 == 0 && M < kMaxRows && K < kMaxRows, JET_ERR_SHAPE);
     JET_REQUIRE(jet::aligned16(q) && jet::aligned16(s) && jet::aligned16(qT) &&
                     jet::aligned16(sT),
                 JET_ERR_ALIGN);
@@ -469,9 +648,10 @@ jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M, int64_
     CUtensorMap tm;
     if (!make_map(&tm, q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K, (uint64_t)M, 128, 128))
         return JET_ERR_CUDA;
-    dim3 grid((unsigned)(K / 128), (unsigned)(M / 128));
-    requant_128x1_kernel<<<grid, 256, 0, jet::as_stream(stream)>>>(tm, s, M, K, qT, sT,
-                                                                   dev.status_word);
+    const int64_t tiles = (M / 128) * (K / 128);
+    const int64_t cap = (int64_t)dev.num_sms * kRqCtasPerSm;
+    requant_128x1_kernel<<<(unsigned)(tiles < cap ? tiles : cap), kRqThreads, 0,
+                           jet::as_stream(stream)>>>(tm, s, M, K, qT, sT, dev.status_word);
     return jet::launch_status();
 }
 
