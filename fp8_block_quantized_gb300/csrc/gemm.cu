@@ -531,8 +531,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&tmY, wbuf, col0, m0 + quad * 32);
-                    tma_store_2d(&tmY, wbuf + 4096, col0 + 64, m0 + quad * 32);
+                    tma_store_2d_hint(&tmY, wbuf, col0, m0 + quad * 32, pol_out);
+                    tma_store_2d_hint(&tmY, wbuf + 4096, col0 + 64, m0 + quad * 32, pol_out);
                     bulk_commit_group();
                 }
             } else if (splits > 1) {

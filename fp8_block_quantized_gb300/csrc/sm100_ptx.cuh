@@ -140,6 +140,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t smem
         : "memory");
 }
 
+// Same store with an L2 eviction-policy hint for the written lines.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *m, uint32_t smem_src,
+                                                  int32_t x, int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+        " [%0, {%1, %2}], [%3], %4;" ::"l"(m),
+        "r"(x), "r"(y), "r"(smem_src), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
