@@ -50,6 +50,8 @@ BYTES_PER_ELEM = {
     "quant_act_1x128": 2 + 1 + 4 / 128,          # BF16 in, code out, one scale per 128
     "quant_w_128x128": 2 + 1 + 4 / (128 * 128),
     "requant_128x1": 1 + 1 + 4 / 128 + 4 / 128,  # code in/out, row scales in, col scales out
+    # BF16 in, 1x128 codes + scales out, 128x1 codes + scales out
+    "quant_dual_1x128_128x1": 2 + 1 + 1 + 4 / 128 + 4 / 128,
     "token_mult_prob_error": 8,                  # two FP32 per token
 }
 
@@ -187,14 +189,17 @@ class LayerStep:
                      "gemm_fp8_dgrad": sum(2 * M * c.N * c.K for c in self.cases),
                      "gemm_fp8_wgrad": sum(2 * M * c.N * c.K for c in self.cases),
                      "quant_w_128x128": sum(c.N * c.K for c in self.cases) * BYTES_PER_ELEM["quant_w_128x128"],
-                     "quant_act_1x128": (sum(M * v["K"] for v in self.inputs.values())
-                                         + sum(M * c.N for c in self.cases)) * BYTES_PER_ELEM["quant_act_1x128"],
-                     "requant_128x1": (sum(M * v["K"] for v in self.inputs.values())
-                                       + sum(M * c.N for c in self.cases)) * BYTES_PER_ELEM["requant_128x1"],
+                     "quant_act_1x128": sum(M * v["K"] for v in self.inputs.values())
+                                        * BYTES_PER_ELEM["quant_act_1x128"],
+                     "requant_128x1": sum(M * v["K"] for v in self.inputs.values())
+                                      * BYTES_PER_ELEM["requant_128x1"],
+                     "quant_dual_1x128_128x1": sum(M * c.N for c in self.cases)
+                                               * BYTES_PER_ELEM["quant_dual_1x128_128x1"],
                      "token_mult_prob_error": M * BYTES_PER_ELEM["token_mult_prob_error"]}
-        # per linear: weight quant, fwd, dY quant, dgrad, dY requant, wgrad;
-        # per distinct input: quant, requant; the metric: two passes
-        self.launches_per_step = len(self.lin) * 6 + len(self.inputs) * 2 + 2
+        # per linear: weight quant, fwd, dY's fused 1x128 + 128x1 quantization,
+        # dgrad, wgrad; per distinct input: quant (forward), requant (backward,
+        # from the saved FP8 form); the metric: two passes
+        self.launches_per_step = len(self.lin) * 5 + len(self.inputs) * 2 + 2
         self.primary = ("TFLOP/s", self.flops)
         self.config = {"workload": f"{kind}_layer_M{M}", "tokens": M,
                        "linears": [(c.name, c.N, c.K) for c in self.cases],
@@ -216,12 +221,10 @@ class LayerStep:
             out.append(("gemm_fp8_fwd", lambda L=L, v=v: j.jet_gemm_fp8_fwd(v["q"], v["s"], L["qw"], L["sw"], L["y"]),
                         L["case"].name))
         for L in self.lin:
-            out.append(("quant_act_1x128", lambda L=L: j.jet_quant_act_1x128(L["dy"], L["qdy"], L["sdy"]),
-                        "dy_" + L["case"].name))
+            out.append(("quant_dual_1x128_128x1", lambda L=L: j.jet_quant_dual_1x128_128x1(
+                L["dy"], L["qdy"], L["sdy"], L["qdyT"], L["sdyT"]), "dy_" + L["case"].name))
             out.append(("gemm_fp8_dgrad", lambda L=L: j.jet_gemm_fp8_dgrad(L["qdy"], L["sdy"], L["qw"], L["sw"], L["dx"]),
                         L["case"].name))
-            out.append(("requant_128x1", lambda L=L: j.jet_requant_128x1(L["qdy"], L["sdy"], L["qdyT"], L["sdyT"]),
-                        "dy_" + L["case"].name))
         for v in self.inputs.values():
             out.append(("requant_128x1", lambda v=v: j.jet_requant_128x1(v["q"], v["s"], v["qT"], v["sT"]),
                         "x%d" % v["K"]))

@@ -14,11 +14,13 @@ from .binding import (  # noqa: F401
     jet_gemm_fp8_fwd,
     jet_gemm_fp8_wgrad,
     jet_quant_act_1x128,
+    jet_quant_dual_1x128_128x1,
     jet_quant_w_128x128,
     jet_requant_128x1,
     jet_token_mult_prob_error,
     load,
     quant_act_1x128,
+    quant_dual_1x128_128x1,
     quant_w_128x128,
     requant_128x1,
     selftest_bounded_wait,

@@ -22,7 +22,7 @@ STATUS = {0: "JET_OK", 1: "JET_ERR_NULL", 2: "JET_ERR_SHAPE", 3: "JET_ERR_ALIGN"
           7: "JET_ERR_TIMEOUT"}
 OP = {"quant_act_1x128": 0, "quant_w_128x128": 1, "requant_128x1": 2,
       "gemm_fp8_fwd": 3, "gemm_fp8_dgrad": 4, "gemm_fp8_wgrad": 5,
-      "token_mult_prob_error": 6}
+      "token_mult_prob_error": 6, "quant_dual_1x128_128x1": 7}
 
 # name -> argtypes (restype is int status unless listed in _RESTYPE)
 P, I, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
@@ -32,6 +32,7 @@ SIGNATURES = {
     "jet_quant_act_1x128": [P, I, I, P, P, P],
     "jet_quant_w_128x128": [P, I, I, P, P, P],
     "jet_requant_128x1": [P, P, I, I, P, P, P],
+    "jet_quant_dual_1x128_128x1": [P, I, I, P, P, P, P, P],
     "jet_gemm_fp8_fwd": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_gemm_fp8_dgrad": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_gemm_fp8_wgrad": [P, P, P, P, I, I, I, P, P, Z, P],
@@ -166,6 +167,18 @@ def jet_requant_128x1(q, s, qT, sT, stream=None):
         _ptr(q), _ptr(s), M, K, _ptr(qT), _ptr(sT), _stream(stream)))
 
 
+def jet_quant_dual_1x128_128x1(x, q, s, qT, sT, stream=None):
+    import torch
+    M, K = x.shape
+    _need(x, torch.bfloat16, (M, K), "x")
+    _need(q, torch.uint8, (M, K), "q")
+    _need(s, torch.float32, (K // 128, M), "s")
+    _need(qT, torch.uint8, (K, M), "qT")
+    _need(sT, torch.float32, (M // 128, K), "sT")
+    _check("jet_quant_dual_1x128_128x1", load().jet_quant_dual_1x128_128x1(
+        _ptr(x), M, K, _ptr(q), _ptr(s), _ptr(qT), _ptr(sT), _stream(stream)))
+
+
 def _gemm(name, a, sa, b, sb, M, N, K, out, ws, stream):
     if ws is None:  # the split-contraction partials of small-M products
         ws = _ws(name[4:], M, N, K, out.device)
@@ -261,6 +274,18 @@ def requant_128x1(q, s, stream=None):
     sT = torch.empty((M // 128, K), dtype=torch.float32, device=q.device)
     jet_requant_128x1(q, s, qT, sT, stream)
     return qT, sT
+
+
+def quant_dual_1x128_128x1(x, stream=None):
+    """(q, s, qT, sT): the 1x128 and the transposed 128x1 forms of x."""
+    import torch
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    qT = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    sT = torch.empty((M // 128, K), dtype=torch.float32, device=x.device)
+    jet_quant_dual_1x128_128x1(x, q, s, qT, sT, stream)
+    return q, s, qT, sT
 
 
 def _ws(op, M, N, K, device):

@@ -400,6 +400,95 @@ quant_w_128x128_kernel(const __grid_constant__ CUtensorMap tmw, int64_t N, int64
 constexpr int kRqThreads = 256;
 constexpr int kRqCtasPerSm = 2;
 
+// Pass 1 of a 128x1 tile: this thread's 4 columns x 16 tokens of a [128
+// tokens][128 codes] shared-memory tile, dequantized and negated,
+// -v = fl32(D4(q) * -s_row), into registers, and the column maxima over its
+// tokens into col_max[w].  kSwz: the tile's 16-byte chunks are stored at
+// chunk XOR (token % 8) (the fused quantizer writes it so; a TMA-loaded tile
+// is plain).
+template <bool kSwz>
+__device__ __forceinline__ void rq_pass1(const uint32_t (*codes)[32], const float *srow,
+                                         float (&v)[4][16], float (*col_max)[128], int lane,
+                                         int w) {
+    const int t0 = w * 16;
+    float amax[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
+        const float4 sr4 = *reinterpret_cast<const float4 *>(&srow[t0 + i]);
+        const float sr[4] = {sr4.x, sr4.y, sr4.z, sr4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = t0 + i + u;
+            const int word = kSwz ? ((((lane >> 2) ^ (t & 7)) << 2) | (lane & 3)) : lane;
+            float d0, d1, d2, d3;
+            e4m3x4_to_f32(codes[t][word], d0, d1, d2, d3);
+            const float2 s2 = make_float2(-sr[u], -sr[u]);
+            const float2 a = __fmul2_rn(make_float2(d0, d1), s2);
+            const float2 b = __fmul2_rn(make_float2(d2, d3), s2);
+            v[0][i + u] = a.x;
+            v[1][i + u] = a.y;
+            v[2][i + u] = b.x;
+            v[3][i + u] = b.y;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            amax[j] = max_abs2(amax[j], v[j][i], v[j][i + 1]);
+            amax[j] = max_abs2(amax[j], v[j][i + 2], v[j][i + 3]);
+        }
+    }
+    *reinterpret_cast<float4 *>(&col_max[w][lane * 4]) =
+        make_float4(amax[0], amax[1], amax[2], amax[3]);
+}
+
+// Between the passes, once col_max is complete: threads 0..127 turn the
+// column maxima into the scales and negated reciprocals (one column each).
+// Returns whether this thread's column takes the fast division (true for the
+// other threads).
+__device__ __forceinline__ bool rq_scales(const float (*col_max)[128], float *col_s,
+                                          float *col_y) {
+    if (threadIdx.x >= 128) return true;
+    float a = col_max[0][threadIdx.x];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) a = fmaxf(a, col_max[j][threadIdx.x]);
+    const float sc = group_scale(a);
+    const Divisor d = make_divisor(sc);
+    col_s[threadIdx.x] = sc;
+    col_y[threadIdx.x] = d.ny;
+    return d.fast;
+}
+
+// Pass 2: quotients of the register-held values, each column's 16 codes as
+// one 16-byte store into qT [K][M], the column scales into sT [M/128][K].
+// `fast`: every column of the tile takes the fast division.
+__device__ __forceinline__ void rq_pass2(const float (&v)[4][16], const float *col_s,
+                                         const float *col_y, bool fast, int64_t M, int64_t K,
+                                         int64_t mb, int64_t kb, uint8_t *__restrict__ qT,
+                                         float *__restrict__ sT, int lane, int w) {
+    const float4 s4 = *reinterpret_cast<const float4 *>(&col_s[lane * 4]);
+    const float4 y4 = *reinterpret_cast<const float4 *>(&col_y[lane * 4]);
+    const float scs[4] = {s4.x, s4.y, s4.z, s4.w};
+    const float ys[4] = {y4.x, y4.y, y4.z, y4.w};
+    const int64_t col = kb * 128 + lane * 4;
+    uint8_t *dst = qT + col * M + mb * 128 + w * 16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        Divisor d;
+        d.s = scs[j];
+        d.ny = ys[j];
+        d.fast = scs[j] >= 0x1p-90f;
+        uint32_t o[4];
+        if (fast) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) o[g] = encode4_fast(&v[j][4 * g], d);
+        } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) o[g] = encode4(&v[j][4 * g], d);
+        }
+        *reinterpret_cast<uint4 *>(dst + (int64_t)j * M) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (w == 0) *reinterpret_cast<float4 *>(sT + mb * K + col) = s4;
+}
+
 __global__ void __launch_bounds__(kRqThreads, kRqCtasPerSm)
 requant_128x1_kernel(const __grid_constant__ CUtensorMap tmq, const float *__restrict__ s,
                      int64_t M, int64_t K, uint8_t *__restrict__ qT,
@@ -433,7 +522,6 @@ requant_128x1_kernel(const __grid_constant__ CUtensorMap tmq, const float *__res
     if (threadIdx.x == 0)
         for (int j = 0; j < 2 && blockIdx.x + j * step < ntiles; ++j, ++issued)
             issue(j, blockIdx.x + j * step);
-    const int t0 = w * 16;
     uint32_t it = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < ntiles; t += step, ++it) {
@@ -441,33 +529,8 @@ requant_128x1_kernel(const __grid_constant__ CUtensorMap tmq, const float *__res
         // A wait that gave up is agreed on at the barrier below, before any
         // global write; until then the (possibly incomplete) stage is only read.
         ok = mbar_wait(&full[st], (it >> 1) & 1u, nullptr, status, jet::SITE_QUANT_STAGE);
-        // pass 1: v = fl32(D4(q) * s_row) into registers, column maxima
         float v[4][16];
-        float amax[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-            const float4 sr4 = *reinterpret_cast<const float4 *>(&srow[st][t0 + i]);
-            const float sr[4] = {sr4.x, sr4.y, sr4.z, sr4.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float d0, d1, d2, d3;
-                e4m3x4_to_f32(tile[st][t0 + i + u][lane], d0, d1, d2, d3);
-                const float2 s2 = make_float2(-sr[u], -sr[u]);
-                const float2 a = __fmul2_rn(make_float2(d0, d1), s2);
-                const float2 b = __fmul2_rn(make_float2(d2, d3), s2);
-                v[0][i + u] = a.x;
-                v[1][i + u] = a.y;
-                v[2][i + u] = b.x;
-                v[3][i + u] = b.y;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                amax[j] = max_abs2(amax[j], v[j][i], v[j][i + 1]);
-                amax[j] = max_abs2(amax[j], v[j][i + 2], v[j][i + 3]);
-            }
-        }
-        *reinterpret_cast<float4 *>(&col_max[w][lane * 4]) =
-            make_float4(amax[0], amax[1], amax[2], amax[3]);
+        rq_pass1<false>(tile[st], srow[st], v, col_max, lane, w);
         if (__syncthreads_or(!ok)) {
             ok = false;
             break;
@@ -478,47 +541,125 @@ requant_128x1_kernel(const __grid_constant__ CUtensorMap tmq, const float *__res
             issue(st, t + 2 * step);
             ++issued;
         }
-        bool fast = true;
-        if (threadIdx.x < 128) {
-            float a = col_max[0][threadIdx.x];
-#pragma unroll
-            for (int j = 1; j < 8; ++j) a = fmaxf(a, col_max[j][threadIdx.x]);
-            const float sc = group_scale(a);
-            const Divisor d = make_divisor(sc);
-            col_s[threadIdx.x] = sc;
-            col_y[threadIdx.x] = d.ny;
-            fast = d.fast;
-        }
         // Tiles whose every column takes the fast division (all but the
         // tiniest data) run pass 2 without a per-column test.
-        fast = __syncthreads_and(fast);
-        // pass 2: quotients, codes, one 16-byte store per column
-        const float4 s4 = *reinterpret_cast<const float4 *>(&col_s[lane * 4]);
-        const float4 y4 = *reinterpret_cast<const float4 *>(&col_y[lane * 4]);
-        const float scs[4] = {s4.x, s4.y, s4.z, s4.w};
-        const float ys[4] = {y4.x, y4.y, y4.z, y4.w};
+        const bool fast = __syncthreads_and(rq_scales(col_max, col_s, col_y));
         const int64_t mb = t / nkb, kb = t - mb * nkb;
-        const int64_t col = kb * 128 + lane * 4;
-        uint8_t *dst = qT + col * M + mb * 128 + t0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            Divisor d;
-            d.s = scs[j];
-            d.ny = ys[j];
-            d.fast = scs[j] >= 0x1p-90f;
-            uint32_t o[4];
-            if (fast) {
-#pragma unroll
-                for (int g = 0; g < 4; ++g) o[g] = encode4_fast(&v[j][4 * g], d);
-            } else {
-#pragma unroll
-                for (int g = 0; g < 4; ++g) o[g] = encode4(&v[j][4 * g], d);
-            }
-            *reinterpret_cast<uint4 *>(dst + (int64_t)j * M) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (w == 0) *reinterpret_cast<float4 *>(sT + mb * K + col) = s4;
+        rq_pass2(v, col_s, col_y, fast, M, K, mb, kb, qT, sT, lane, w);
     }
     // After a time-out, loads still in flight must land before the CTA exits.
+    if (!ok && threadIdx.x == 0)
+        for (int64_t j = it; j < issued; ++j)
+            mbar_wait(&full[j & 1], (uint32_t)(j >> 1) & 1u, nullptr, status,
+                      jet::SITE_QUANT_STAGE);
+}
+
+// --------------------------------------------------- 1x128 and 128x1 fused --
+// Both quantizations of one BF16 tensor (the output gradient) from a single
+// read: per tile of 128 tokens x one K-block (two 64-column boxes with the
+// 128-byte swizzle, 32 KB, two-stage TMA ring as above), phase A quantizes
+// each token row as a 1x128 group (two threads per row, 64 values each, the
+// row amax by one shuffle) and writes its codes and scale to global memory and
+// to a shared-memory code tile (16-byte chunks at chunk XOR (row % 8): the
+// stores are conflict-free per quarter-warp and the row reads of phase B still
+// touch every bank once); phase B is the 128x1 re-quantization of that tile
+// (rq_pass1/rq_scales/rq_pass2), i.e. from the FP8 values just written.  The
+// results equal jet_quant_act_1x128 followed by jet_requant_128x1 bit for bit.
+constexpr int kDualBoxBytes = 128 * 128;  // 128 rows x 64 BF16
+constexpr int kDualTileBytes = 2 * kDualBoxBytes;
+constexpr int kDualCtasPerSm = 2;
+constexpr int kDualSmemBytes = 2 * kDualTileBytes + 1024;
+
+__global__ void __launch_bounds__(256, kDualCtasPerSm)
+quant_dual_kernel(const __grid_constant__ CUtensorMap tmx, int64_t M, int64_t K,
+                  uint8_t *__restrict__ q, float *__restrict__ s, uint8_t *__restrict__ qT,
+                  float *__restrict__ sT, unsigned *status) {
+    extern __shared__ uint8_t dual_smem[];
+    __shared__ __align__(128) uint32_t codes[128][32];
+    __shared__ __align__(16) float srow[128];
+    __shared__ __align__(16) float col_max[8][128];
+    __shared__ __align__(16) float col_s[128];
+    __shared__ __align__(16) float col_y[128];
+    __shared__ uint64_t full[2];
+    const uint32_t base = (smem_u32(dual_smem) + 1023u) & ~1023u;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int64_t nkb = K / 128;
+    const int64_t ntiles = (M / 128) * nkb;
+    const int64_t step = gridDim.x;
+    if (threadIdx.x == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        jet::ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int st, int64_t t) {
+        const int64_t mb = t / nkb, kb = t - mb * nkb;
+        const uint32_t dst = base + st * kDualTileBytes;
+        mbar_arrive_expect_tx(&full[st], kDualTileBytes);
+        tma_load_2d(dst, &tmx, &full[st], (int32_t)(kb * 128), (int32_t)(mb * 128),
+                    kStreamPolicy);
+        tma_load_2d(dst + kDualBoxBytes, &tmx, &full[st], (int32_t)(kb * 128 + 64),
+                    (int32_t)(mb * 128), kStreamPolicy);
+    };
+    int64_t issued = 0;
+    if (threadIdx.x == 0)
+        for (int j = 0; j < 2 && blockIdx.x + j * step < ntiles; ++j, ++issued)
+            issue(j, blockIdx.x + j * step);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < ntiles; t += step, ++it) {
+        const int st = it & 1;
+        ok = mbar_wait(&full[st], (it >> 1) & 1u, nullptr, status, jet::SITE_QUANT_STAGE);
+        // phase A: the 1x128 group of token `row`, columns 64h .. 64h+63 here
+        const uint32_t box = base + st * kDualTileBytes + half * kDualBoxBytes;
+        float f[64];  // -x; f[8k ..] holds chunk k ^ 4h of the box row
+#pragma unroll
+        for (int k = 0; k < 8; ++k) unpack8_neg(lds128(swz128(box, row, k ^ (4 * half))), f + 8 * k);
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) a = max_abs2(a, f[i], f[i + 1]);
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
+        if (threadIdx.x == 0 && t + 2 * step < ntiles) {
+            fence_proxy_async();
+            issue(st, t + 2 * step);
+            ++issued;
+        }
+        const int64_t mb = t / nkb, kb = t - mb * nkb;
+        const int64_t m = mb * 128 + row;
+        const float sc = group_scale(a);
+        const Divisor d = make_divisor(sc);
+        // f[16j ..] holds code chunk (16 codes) 4h + (j ^ 2h) of the row
+        uint4 *gq = reinterpret_cast<uint4 *>(q + m * K + kb * 128 + half * 64);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 c;
+            if (d.fast)
+                c = make_uint4(encode4_fast(f + 16 * j, d), encode4_fast(f + 16 * j + 4, d),
+                               encode4_fast(f + 16 * j + 8, d), encode4_fast(f + 16 * j + 12, d));
+            else
+                c = make_uint4(encode4(f + 16 * j, d), encode4(f + 16 * j + 4, d),
+                               encode4(f + 16 * j + 8, d), encode4(f + 16 * j + 12, d));
+            const int chunk = 4 * half + (j ^ (2 * half));
+            gq[j ^ (2 * half)] = c;
+            *reinterpret_cast<uint4 *>(&codes[row][(chunk ^ (row & 7)) * 4]) = c;
+        }
+        if (half == 0) {
+            s[kb * M + m] = sc;
+            srow[row] = sc;
+        }
+        __syncthreads();
+        // phase B: 128x1 groups of the codes just written
+        float v[4][16];
+        rq_pass1<true>(codes, srow, v, col_max, lane, w);
+        __syncthreads();
+        const bool fast = __syncthreads_and(rq_scales(col_max, col_s, col_y));
+        rq_pass2(v, col_s, col_y, fast, M, K, mb, kb, qT, sT, lane, w);
+    }
     if (!ok && threadIdx.x == 0)
         for (int64_t j = it; j < issued; ++j)
             mbar_wait(&full[j & 1], (uint32_t)(j >> 1) & 1u, nullptr, status,
@@ -652,6 +793,39 @@ jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M, int64_
     const int64_t cap = (int64_t)dev.num_sms * kRqCtasPerSm;
     requant_128x1_kernel<<<(unsigned)(tiles < cap ? tiles : cap), kRqThreads, 0,
                            jet::as_stream(stream)>>>(tm, s, M, K, qT, sT, dev.status_word);
+    return jet::launch_status();
+}
+
+jet_status jet_quant_dual_1x128_128x1(const uint16_t *x, int64_t M, int64_t K, uint8_t *q,
+                                      float *s, uint8_t *qT, float *sT, jet_stream_t stream) {
+    JET_REQUIRE(M >= 0 && K >= 0, JET_ERR_SHAPE);
+    const bool empty = (M == 0 || K == 0);
+    JET_REQUIRE(empty || (x && q && s && qT && sT), JET_ERR_NULL);
+    JET_REQUIRE(M % 128 == 0 && K % 128 == 0 && M < kMaxRows && K < kMaxRows, JET_ERR_SHAPE);
+    JET_REQUIRE(jet::aligned16(x) && jet::aligned16(q) && jet::aligned16(s) &&
+                    jet::aligned16(qT) && jet::aligned16(sT),
+                JET_ERR_ALIGN);
+    jet::DeviceInfo dev;
+    jet_status st = jet::current_device(&dev);
+    if (st != JET_OK) return st;
+    if (empty) return JET_OK;
+    static bool attr_set[64] = {};
+    if (!attr_set[dev.ordinal]) {
+        if (cudaFuncSetAttribute(quant_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kDualSmemBytes) != cudaSuccess) {
+            cudaGetLastError();
+            return JET_ERR_CUDA;
+        }
+        attr_set[dev.ordinal] = true;
+    }
+    CUtensorMap tm;
+    if (!make_map(&tm, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K, (uint64_t)M, 64, 128,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return JET_ERR_CUDA;
+    const int64_t tiles = (M / 128) * (K / 128);
+    const int64_t cap = (int64_t)dev.num_sms * kDualCtasPerSm;
+    quant_dual_kernel<<<(unsigned)(tiles < cap ? tiles : cap), 256, kDualSmemBytes,
+                        jet::as_stream(stream)>>>(tm, M, K, q, s, qT, sT, dev.status_word);
     return jet::launch_status();
 }
 

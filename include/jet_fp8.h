@@ -70,7 +70,8 @@ typedef enum {
     JET_OP_GEMM_FWD = 3,
     JET_OP_GEMM_DGRAD = 4,
     JET_OP_GEMM_WGRAD = 5,
-    JET_OP_TOKEN_MULT_PROB_ERROR = 6
+    JET_OP_TOKEN_MULT_PROB_ERROR = 6,
+    JET_OP_QUANT_DUAL_1X128_128X1 = 7
 } jet_op;
 
 /* A cudaStream_t handle passed as an opaque pointer. */
@@ -122,6 +123,24 @@ JET_API jet_status jet_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K,
 JET_API jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M,
                              int64_t K, uint8_t *qT, float *sT,
                              jet_stream_t stream);
+
+/*
+ * Both quantizations of one tensor from a single read: the 1x128 form of
+ * jet_quant_act_1x128 and the transposed 128x1 form that jet_requant_128x1
+ * derives from it (re-quantized from the FP8 1x128 values).  Used for the
+ * output gradient dY, whose two forms feed DGrad and WGrad in the same
+ * backward step.  Source: 163.com article, section 五 (1x128 groups
+ * re-quantized as 128x1 for backward; quantization fused into the operator
+ * that produces the tensor); gist.science summary, "Quantisierungsschema"
+ * (DGrad with 1x128, WGrad with 1x128 and 128x1).  Codes and scales equal
+ * those of jet_quant_act_1x128 followed by jet_requant_128x1, bit for bit.
+ *   x   [M][K] BF16 bits (in).      M, K >= 0, both multiples of 128.
+ *   q   [M][K] E4M3 codes, s [Kb][M] FP32 scales (out; the 1x128 form).
+ *   qT  [K][M] E4M3 codes, sT [Mb][K] FP32 scales (out; the 128x1 form).
+ */
+JET_API jet_status jet_quant_dual_1x128_128x1(const uint16_t *x, int64_t M, int64_t K,
+                                              uint8_t *q, float *s, uint8_t *qT, float *sT,
+                                              jet_stream_t stream);
 
 /*
  * Forward GEMM  Y = X W^T  with per-128-K-block scale promotion:

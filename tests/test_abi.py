@@ -91,6 +91,19 @@ def test_quant_act_checks(lib):
     assert f(fake(A), 4, 128, fake(B), fake(MIS), None) == ALIGN
 
 
+def test_quant_dual_checks(lib):
+    f = lib.jet_quant_dual_1x128_128x1
+    ok = [fake(A), 128, 128, fake(B), fake(C), fake(D), fake(A + 0x1000)]
+    assert f(None, *ok[1:], None) == NULL
+    assert f(*ok[:6], None, None) == NULL
+    assert f(ok[0], 100, 128, *ok[3:], None) == SHAPE       # tokens must hold whole 128x1 groups
+    assert f(ok[0], 128, 100, *ok[3:], None) == SHAPE
+    assert f(ok[0], -128, 128, *ok[3:], None) == SHAPE
+    assert f(*ok[:5], fake(MIS), ok[6], None) == ALIGN
+    assert f(None, 0, 128, None, None, None, None, None) in (OK, DEVICE)   # empty: nothing to do
+    assert lib.jet_workspace_bytes(binding.OP["quant_dual_1x128_128x1"], 8192, 4096, 0) == 0
+
+
 def test_quant_w_and_requant_checks(lib):
     w = lib.jet_quant_w_128x128
     assert w(None, 128, 128, fake(B), fake(C), None) == NULL

@@ -157,6 +157,57 @@ def test_requant_empty(jet):
     assert qT.shape == (128, 0) and sT.shape == (0, 128)
 
 
+def check_dual(jet, x_cpu, kblocks=None):
+    """The fused quantizer against the oracle's 1x128 quantization followed by
+    its 128x1 re-quantization of the FP8 values."""
+    q, s, qT, sT = jet.quant_dual_1x128_128x1(x_cpu.cuda())
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quant_act_1x128(bits(x_cpu))
+    assert_codes_equal(q, q_ref)
+    assert_scales_equal(s, s_ref)
+    if kblocks is None:
+        qT_ref, sT_ref = oracle.requant_128x1(q_ref, s_ref)
+        assert_codes_equal(qT, qT_ref)
+        assert_scales_equal(sT, sT_ref)
+    else:
+        for kb in kblocks:
+            sl = slice(kb * 128, (kb + 1) * 128)
+            qT_ref, sT_ref = oracle.requant_128x1(np.ascontiguousarray(q_ref[:, sl]),
+                                                  np.ascontiguousarray(s_ref[kb:kb + 1]))
+            assert_codes_equal(qT[sl], qT_ref)
+            assert_scales_equal(sT[:, sl], sT_ref)
+
+
+def test_dual_single_linear(jet):
+    c = wl.single_linear()
+    check_dual(jet, c.dy)
+    check_dual(jet, c.x)      # outlier channels and an all-zero 1x128 group
+
+
+@pytest.mark.parametrize("M,K", [(128, 128), (384, 256), (1024, 1024), (256, 14336)])
+def test_dual_shapes(jet, M, K):
+    check_dual(jet, wl.grad_output(M, K, seed=M * 3 + K, config=3))
+
+
+def test_dual_edge_values(jet):
+    M, K = 256, 384
+    x = torch.randn((M, K), generator=torch.Generator().manual_seed(3)) * 1e-3
+    x[:, 5] = 0.0                                   # an all-zero 128x1 group per token block
+    x[7, :] = -0.0                                   # signed zeros
+    x[9, 128:256] = 3.3895e38                        # BF16 max in one group
+    x[200:, 300] = 1e-38                             # subnormal column
+    check_dual(jet, x.to(torch.bfloat16))
+
+
+def test_dual_train8b_gradients_sampled(jet):
+    check_dual(jet, wl.grad_output(8192, 4096, seed=0, config=3, tensor_id=200), kblocks=[0, 17, 31])
+
+
+def test_dual_empty(jet):
+    q, s, qT, sT = jet.quant_dual_1x128_128x1(torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"))
+    assert q.shape == (0, 256) and qT.shape == (256, 0) and sT.shape == (0, 256)
+
+
 def _ieee_quotients(x, s):
     with np.errstate(all="ignore"):
         return (x.astype(np.float32) / s.astype(np.float32)).astype(np.float32)
