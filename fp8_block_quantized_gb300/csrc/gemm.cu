@@ -247,6 +247,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    griddep_launch_dependents();
+    griddep_wait();
 
     // Each role is nested inside its own setmaxnreg branch so that the
     // register limit of one branch never applies to the other.
@@ -584,6 +586,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float4 *__restrict__ partial, int splits, int64_t n4,
                      uint2 *__restrict__ out) {
+    griddep_launch_dependents();
+    griddep_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
          i += (int64_t)gridDim.x * blockDim.x) {
         float4 a = partial[i];
@@ -684,7 +688,7 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     static std::mutex mu;
     static int max_units[64] = {};  // co-resident CTAs (CL = 1) or clusters (CL = 2)
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = CF::kSmemBytes;
     cfg.stream = stream;
@@ -692,6 +696,10 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch (see launch_pdl); the occupancy query
+    // below sees only the cluster attribute
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     {
@@ -725,6 +733,7 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     const int64_t grid_units = units < max_units[dev.ordinal] ? units : max_units[dev.ordinal];
     cfg.gridDim = dim3((unsigned)(grid_units * CL));
     const Raster raster = choose_raster(R, C, D);
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kernel, tmA_arg(ta), tmA_arg(tb), tmA_arg(ty), sa, sb, out,
                            (int)R, (int)C, (int)D, raster, splits, partial,
                            dev.status_word) != cudaSuccess) {
@@ -734,8 +743,9 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     if (splits > 1) {
         const int64_t n4 = R * C / 4;
         const int64_t want = (n4 + 255) / 256, cap = (int64_t)dev.num_sms * 8;
-        splitk_reduce_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, stream>>>(
-            reinterpret_cast<const float4 *>(partial), splits, n4, reinterpret_cast<uint2 *>(out));
+        return launch_pdl(splitk_reduce_kernel, dim3((unsigned)(want < cap ? want : cap)),
+                          dim3(256), 0, stream, reinterpret_cast<const float4 *>(partial),
+                          splits, n4, reinterpret_cast<uint2 *>(out));
     }
     return launch_status();
 }

@@ -31,6 +31,32 @@ inline jet_status launch_status() {
     return e == cudaSuccess ? JET_OK : JET_ERR_CUDA;
 }
 
+// Launches a kernel of this library with programmatic dependent launch
+// allowed: its blocks may start (barrier set-up, TMEM allocation) while the
+// previous work on the stream is finishing.  Every such kernel calls
+// griddep_wait() before it touches global memory, which waits until that
+// previous work has completed and its writes are visible, so stream order is
+// kept; the overlap hides the launch gap between short kernels.
+template <typename... KArgs, typename... Args>
+inline jet_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) {
+        cudaGetLastError();
+        return JET_ERR_CUDA;
+    }
+    return launch_status();
+}
+
 }  // namespace jet
 
 // Early-return helpers for argument validation.
@@ -59,6 +85,17 @@ enum WaitSite : unsigned {
 __device__ __forceinline__ void report_timeout(unsigned *status_word, unsigned site) {
     // First error wins; later ones are dropped.
     atomicCAS(status_word, 0u, (site << 8) | (unsigned)JET_ERR_TIMEOUT);
+}
+
+// Programmatic dependent launch (see launch_pdl): allow the next kernel on
+// the stream to start its blocks, and wait for the previous kernel's
+// completion before touching global memory.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

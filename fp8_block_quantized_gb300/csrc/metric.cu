@@ -38,6 +38,8 @@ __device__ __forceinline__ double block_sum(double v) {
 __global__ void __launch_bounds__(kThreads)
 tmpe_partial_kernel(const float *__restrict__ a, const float *__restrict__ b, int64_t n,
                     double *__restrict__ partial) {
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
     float acc = 0.0f;
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -57,6 +59,8 @@ tmpe_partial_kernel(const float *__restrict__ a, const float *__restrict__ b, in
 
 __global__ void __launch_bounds__(kThreads)
 tmpe_final_kernel(const double *__restrict__ partial, int nblocks, int64_t n, float *out) {
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
     double v = 0.0;
     for (int i = threadIdx.x; i < nblocks; i += kThreads) v += partial[i];
     const double t = block_sum(v);
@@ -77,9 +81,11 @@ int jet_metric_blocks(int64_t n) {
 jet_status jet_metric_launch(const float *a, const float *b, int64_t n, float *out,
                              double *partial, cudaStream_t stream) {
     const int g = jet_metric_blocks(n);
-    tmpe_partial_kernel<<<g, kThreads, 0, stream>>>(a, b, n, partial);
-    tmpe_final_kernel<<<1, kThreads, 0, stream>>>(partial, g, n, out);
-    return jet::launch_status();
+    jet_status st = jet::launch_pdl(tmpe_partial_kernel, dim3(g), dim3(kThreads), 0, stream, a, b,
+                                    n, partial);
+    if (st != JET_OK) return st;
+    return jet::launch_pdl(tmpe_final_kernel, dim3(1), dim3(kThreads), 0, stream,
+                           static_cast<const double *>(partial), g, n, out);
 }
 
 extern "C" jet_status jet_token_mult_prob_error(const float *logp_train,

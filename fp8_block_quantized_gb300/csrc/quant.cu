@@ -217,6 +217,8 @@ quant_act_1x128_kernel(const __grid_constant__ CUtensorMap tmx, int64_t M, int64
         jet::ptx::fence_mbar_init();
     }
     __syncthreads();
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
     auto issue = [&](int st, int64_t t) {
         const int64_t mb = t / nkb, kb = t - mb * nkb;
         const uint32_t dst = base + st * kActTileBytes;
@@ -313,6 +315,8 @@ quant_w_128x128_kernel(const __grid_constant__ CUtensorMap tmw, int64_t N, int64
         jet::ptx::fence_mbar_init();
     }
     __syncthreads();
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
     auto issue = [&](int st, int64_t t) {
         const int64_t nb = t / nkb, kb = t - nb * nkb;
         const uint32_t dst = base + st * kWTileBytes;
@@ -509,6 +513,8 @@ requant_128x1_kernel(const __grid_constant__ CUtensorMap tmq, const float *__res
         jet::ptx::fence_mbar_init();
     }
     __syncthreads();
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
     // Tile t = mb * nkb + kb: CTAs running together take neighbouring column
     // blocks of the same 128 tokens.
     auto issue = [&](int st, int64_t t) {
@@ -593,6 +599,8 @@ quant_dual_kernel(const __grid_constant__ CUtensorMap tmx, int64_t M, int64_t K,
         jet::ptx::fence_mbar_init();
     }
     __syncthreads();
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
     auto issue = [&](int st, int64_t t) {
         const int64_t mb = t / nkb, kb = t - mb * nkb;
         const uint32_t dst = base + st * kDualTileBytes;
@@ -736,9 +744,9 @@ jet_status jet_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, uint8_t 
         return JET_ERR_CUDA;
     const int64_t tiles = (M + kActRowsPerCta - 1) / kActRowsPerCta * (K / 128);
     const int64_t cap = (int64_t)dev.num_sms * kActCtasPerSm;
-    quant_act_1x128_kernel<<<(unsigned)(tiles < cap ? tiles : cap), 256, kActSmemBytes,
-                             jet::as_stream(stream)>>>(tm, M, K, q, s, dev.status_word);
-    return jet::launch_status();
+    return jet::launch_pdl(quant_act_1x128_kernel, dim3((unsigned)(tiles < cap ? tiles : cap)),
+                           dim3(256), kActSmemBytes, jet::as_stream(stream), tm, M, K, q, s,
+                           dev.status_word);
 }
 
 jet_status jet_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K, uint8_t *q,
@@ -768,9 +776,9 @@ jet_status jet_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K, uint8_t 
         return JET_ERR_CUDA;
     const int64_t tiles = (N / 128) * (K / 128);
     const int64_t cap = (int64_t)dev.num_sms * kWCtasPerSm;
-    quant_w_128x128_kernel<<<(unsigned)(tiles < cap ? tiles : cap), 256, kWSmemBytes,
-                             jet::as_stream(stream)>>>(tm, N, K, q, s, dev.status_word);
-    return jet::launch_status();
+    return jet::launch_pdl(quant_w_128x128_kernel, dim3((unsigned)(tiles < cap ? tiles : cap)),
+                           dim3(256), kWSmemBytes, jet::as_stream(stream), tm, N, K, q, s,
+                           dev.status_word);
 }
 
 jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M, int64_t K,
@@ -791,9 +799,9 @@ jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M, int64_
         return JET_ERR_CUDA;
     const int64_t tiles = (M / 128) * (K / 128);
     const int64_t cap = (int64_t)dev.num_sms * kRqCtasPerSm;
-    requant_128x1_kernel<<<(unsigned)(tiles < cap ? tiles : cap), kRqThreads, 0,
-                           jet::as_stream(stream)>>>(tm, s, M, K, qT, sT, dev.status_word);
-    return jet::launch_status();
+    return jet::launch_pdl(requant_128x1_kernel, dim3((unsigned)(tiles < cap ? tiles : cap)),
+                           dim3(kRqThreads), 0, jet::as_stream(stream), tm, s, M, K, qT, sT,
+                           dev.status_word);
 }
 
 jet_status jet_quant_dual_1x128_128x1(const uint16_t *x, int64_t M, int64_t K, uint8_t *q,
@@ -824,9 +832,9 @@ jet_status jet_quant_dual_1x128_128x1(const uint16_t *x, int64_t M, int64_t K, u
         return JET_ERR_CUDA;
     const int64_t tiles = (M / 128) * (K / 128);
     const int64_t cap = (int64_t)dev.num_sms * kDualCtasPerSm;
-    quant_dual_kernel<<<(unsigned)(tiles < cap ? tiles : cap), 256, kDualSmemBytes,
-                        jet::as_stream(stream)>>>(tm, M, K, q, s, qT, sT, dev.status_word);
-    return jet::launch_status();
+    return jet::launch_pdl(quant_dual_kernel, dim3((unsigned)(tiles < cap ? tiles : cap)),
+                           dim3(256), kDualSmemBytes, jet::as_stream(stream), tm, M, K, q, s, qT,
+                           sT, dev.status_word);
 }
 
 }  // extern "C"
