@@ -36,10 +36,10 @@
 // K-major for forward and wgrad; for dgrad the weight codes qw[N][K] are read
 // as they are, MN-major (the output column contiguous), so no transposed copy
 // of the weights is needed.
-// Split contraction (one row tile only, i.e. at most 128 output rows, as in
-// rollout decode): a 128-row problem has only C/BN tiles, far fewer than the
-// 152 SMs, so the contraction is cut into `splits` contiguous ranges of
-// 128-slices, one work unit per (tile, range).  Each unit writes its FP32
+// Split contraction (at most 512 output rows, as in rollout decode): such a
+// problem has only a few C/BN-wide tiles, far fewer than the 152 SMs, so the
+// contraction is cut into `splits` contiguous ranges of 128-slices, one work
+// unit per (tile, range).  Each unit writes its FP32
 // partial tile to a caller-provided workspace [splits][R][C]; a second kernel
 // adds the partials in split order (deterministic) and rounds once to BF16.
 // Every mbarrier wait is bounded (see jet_common.cuh); a role that gives up
@@ -750,17 +750,22 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     return launch_status();
 }
 
-// Number of contraction ranges for an R x C x D product (1 = no split).  Only
-// a single row tile (R <= 128) is split, into at most as many ranges as fill
-// 152 SMs with one unit each, at most one range per 128-slice, and at most
-// D / (8 R) ranges so that the FP32 partials (written and read back:
-// 8 * splits * R * C bytes) cost no more traffic than the C x D codes.  It
-// depends only on the sizes, never on the device, so the workspace size and
-// the summation order (hence the result) are the same on every GPU.
+// Number of contraction ranges for an R x C x D product (1 = no split).
+// Products of at most 512 rows (decode and short prefill) have too few
+// output tiles for 152 SMs; they run on the single-CTA kernel, split into
+// at most as many ranges as fill 152 SMs with one unit each, at most one
+// range per 128-slice, and at most D / (8 R) ranges so that the FP32 partials
+// (written and read back: 8 * splits * R * C bytes) cost no more traffic than
+// the C x D codes.  Fewer than two ranges means no split (and rows above 128
+// then take the CTA-pair kernel).  It depends only on the sizes, never on the
+// device, so the workspace size and the summation order (hence the result)
+// are the same on every GPU.
+constexpr int64_t kSplitMaxRows = 512;
+
 int splitk_splits(int64_t R, int64_t C, int64_t D) {
     constexpr int64_t kUnits = 152;
-    if (R <= 0 || R > BM || C <= 0 || D <= 0 || C % 128 != 0 || D % BK != 0) return 1;
-    const int64_t tiles = C / (C % 256 == 0 ? 256 : 128);
+    if (R <= 0 || R > kSplitMaxRows || C <= 0 || D <= 0 || C % 128 != 0 || D % BK != 0) return 1;
+    const int64_t tiles = (R + BM - 1) / BM * (C / (C % 256 == 0 ? 256 : 128));
     int64_t s = kUnits / tiles;
     const int64_t nkb = D / BK, by_bytes = D / (8 * R);
     if (s > nkb) s = nkb;
@@ -785,12 +790,14 @@ jet_status run_gemm(const uint8_t *a, const float *sa, const uint8_t *b, const f
         return cudaMemsetAsync(out, 0, (size_t)R * C * 2, stream) == cudaSuccess ? JET_OK
                                                                                : JET_ERR_CUDA;
     }
-    // The pair MMA (256 x 256 per CTA pair) whenever there are at least two
-    // row tiles and the output is a multiple of 256 wide.
+    // A split contraction runs on the single-CTA kernel; otherwise the pair
+    // MMA (256 x 256 per CTA pair) whenever there are at least two row tiles
+    // and the output is a multiple of 256 wide.
     const int splits = MODE == kWgrad ? 1 : splitk_splits(R, C, D);
     float *partial = splits > 1 ? static_cast<float *>(ws) : nullptr;
     if (C % 256 == 0) {
-        if (R > BM) return launch<256, MODE, 2>(dev, a, sa, b, sb, out, R, C, D, 1, nullptr, stream);
+        if (R > BM && splits == 1)
+            return launch<256, MODE, 2>(dev, a, sa, b, sb, out, R, C, D, 1, nullptr, stream);
         return launch<256, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, splits, partial, stream);
     }
     return launch<128, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, splits, partial, stream);

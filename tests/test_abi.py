@@ -58,7 +58,10 @@ def test_workspace_bytes(lib):
     assert lib.jet_workspace_bytes(fwd, 64, 14336, 4096) == 2 * 64 * 14336 * 4  # 56 tiles
     assert lib.jet_workspace_bytes(fwd, 1, 1024, 4096) == 32 * 1024 * 4         # one per slice
     assert lib.jet_workspace_bytes(fwd, 128, 128, 128) == 0                     # one slice
-    assert lib.jet_workspace_bytes(fwd, 129, 4096, 4096) == 0                   # two row tiles
+    assert lib.jet_workspace_bytes(fwd, 129, 4096, 4096) == 3 * 129 * 4096 * 4  # two row tiles
+    assert lib.jet_workspace_bytes(fwd, 256, 4096, 14336) == 4 * 256 * 4096 * 4
+    assert lib.jet_workspace_bytes(fwd, 513, 4096, 14336) == 0                  # pair kernel
+    assert lib.jet_workspace_bytes(fwd, 256, 14336, 4096) == 0                  # 112 tiles
     assert lib.jet_workspace_bytes(fwd, 128, 4096, 1024) == 0                   # K/(8M) = 1
     assert lib.jet_workspace_bytes(dgrad, 16, 4096, 1024) == 32 * 16 * 1024 * 4  # C = K = 1024
     assert lib.jet_workspace_bytes(dgrad, 16, 1024, 4096) == 8 * 16 * 4096 * 4   # K/(8M) = 8

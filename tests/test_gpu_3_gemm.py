@@ -115,9 +115,9 @@ def test_wgrad_shapes(jet, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 512, 1024), (1, 4096, 1024), (100, 2048, 384),
-                                   (128, 4096, 1024)])
+                                   (128, 4096, 1024), (256, 4096, 1024), (300, 8192, 512)])
 def test_dgrad_small_rows_split_contraction(jet, M, N, K):
-    # at most 128 rows: the contraction (N) is split into ranges of 128-slices
+    # at most 512 rows: the contraction (N) is split into ranges of 128-slices
     assert jet.workspace_bytes("gemm_fp8_dgrad", M, N, K) > 0
     run_dgrad(jet, wl.grad_output(M, N, seed=M + N, config=3), wl.weights(N, K, seed=K, config=3))
 
@@ -177,7 +177,7 @@ def test_fwd_persistent_many_tiles(jet):
 
 
 @pytest.mark.parametrize("name,N,K", [("kv", 1024, 4096), ("down", 4096, 14336)])
-@pytest.mark.parametrize("M", [1, 64, 2048])
+@pytest.mark.parametrize("M", [1, 64, 256, 385, 2048])
 def test_fwd_rollout_shapes(jet, name, N, K, M):
     run_fwd(jet, wl.activations(M, K, seed=M, config=2), wl.weights(N, K, seed=N, config=2),
             nrows=24)
