@@ -20,7 +20,11 @@ Sources followed (page title and section):
     Training and Rollout Precision Flow" (gist.science), "Quantisierungsschema";
   * 1x128 forward groups re-quantized as 128x1 in backward: "英伟达破解AI训练
     效率难题" (163.com), section 五;
-  * token-mult-prob-error: nmedialink page, section "FP8面临的关键挑战：数值分歧".
+  * token-mult-prob-error: nmedialink page, section "FP8面临的关键挑战：数值分歧";
+  * importance weights (ratio of the original to the compressed model's token
+    probability): FP8-RL article (m.66260.cn), paragraph on error correction;
+    importance sampling combined with FP8: nmedialink page, section
+    "重要抽样技术：提升RL精度的尖兵".
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against facts the
 pages or mathematics fix (no function is "parity unpinned").
@@ -83,6 +87,9 @@ def _load():
             f.restype = None
         lib.jo_token_mult_prob_error.restype = ctypes.c_double
         lib.jo_token_mult_prob_error.argtypes = [P, P, I]
+        lib.jo_token_mismatch_masked.restype = ctypes.c_double
+        lib.jo_token_mismatch_masked.argtypes = [P, P, P, I, ctypes.c_double, P,
+                                                 ctypes.POINTER(ctypes.c_int64)]
         lib.jo_init()
         _lib = lib
         return lib
@@ -262,3 +269,22 @@ def token_mult_prob_error(logp_train, logp_infer) -> float:
     if a.size != b.size or a.size == 0:
         raise ValueError("need two non-empty vectors of equal length")
     return float(_load().jo_token_mult_prob_error(_ptr(a), _ptr(b), a.size))
+
+
+def token_mismatch_masked(logp_train, logp_rollout, mask=None, cap: float = 0.0):
+    """(metric, count, w): the token-mult-prob-error over the masked tokens,
+    their number, and the per-token importance weights
+    w_i = min(exp(logp_train_i - logp_rollout_i), cap) (cap <= 0: no cap),
+    0 outside the mask; binary64.  mask=None counts every token."""
+    a = np.ascontiguousarray(logp_train, np.float32).reshape(-1)
+    b = np.ascontiguousarray(logp_rollout, np.float32).reshape(-1)
+    if a.size != b.size:
+        raise ValueError("need two vectors of equal length")
+    m = None if mask is None else np.ascontiguousarray(mask, np.uint8).reshape(-1)
+    if m is not None and m.size != a.size:
+        raise ValueError("mask length differs")
+    w = np.empty(a.size, np.float64)
+    count = ctypes.c_int64(0)
+    metric = _load().jo_token_mismatch_masked(_ptr(a), _ptr(b), None if m is None else _ptr(m),
+                                              a.size, float(cap), _ptr(w), ctypes.byref(count))
+    return float(metric), int(count.value), w

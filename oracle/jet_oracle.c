@@ -309,3 +309,36 @@ double jo_token_mult_prob_error(const float *a, const float *b, int64_t n)
         sum += exp(fabs((double)a[i] - (double)b[i]));
     return sum / (double)n;
 }
+
+/* Masked mismatch metric with per-token importance weights.
+ * The importance weight of a token is the ratio of the training model's
+ * probability of it to the rollout model's ("FP8-RL" article: the ratio of
+ * the original to the compressed model's token probability), here
+ * w_i = exp(a_i - b_i) with a = logp_train and b = logp_rollout, optionally
+ * capped at `cap` (cap <= 0: no cap; the pages give no constant), and 0 for a
+ * token outside the mask.  The metric is the token-mult-prob-error of the
+ * nmedialink page over the masked tokens only:
+ *   (sum over masked i of exp|a_i - b_i|) / count.
+ * mask == NULL counts every token.  *count receives the number of masked
+ * tokens; with none the metric is NaN.  All arithmetic in binary64. */
+double jo_token_mismatch_masked(const float *a, const float *b, const uint8_t *mask,
+                                int64_t n, double cap, double *w, int64_t *count)
+{
+    double sum = 0.0;
+    int64_t c = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int on = mask == NULL || mask[i] != 0;
+        const double d = (double)a[i] - (double)b[i];
+        if (on) {
+            double wi = exp(d);
+            if (cap > 0.0 && wi > cap) wi = cap;
+            w[i] = wi;
+            sum += exp(fabs(d));
+            ++c;
+        } else {
+            w[i] = 0.0;
+        }
+    }
+    *count = c;
+    return c > 0 ? sum / (double)c : NAN;
+}

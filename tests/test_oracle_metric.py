@@ -52,3 +52,64 @@ def test_closed_form_gaussian_gap():
     assert abs(r - expect) < 3e-5                           # ~5 standard errors
     lo, hi = load_metric_band()
     assert r < lo < hi                                      # sigma = 0.02 sits below the band
+
+
+# ---------------------------------------------- masked metric + IS weights --
+
+def test_masked_metric_all_tokens_equals_plain_metric():
+    rng = np.random.default_rng(11)
+    a = rng.normal(-2, 1, 5000).astype(np.float32)
+    b = (a + rng.normal(0, 0.05, 5000)).astype(np.float32)
+    m, c, _ = oracle.token_mismatch_masked(a, b)
+    assert c == 5000
+    assert abs(m - oracle.token_mult_prob_error(a, b)) <= 1e-15 * m
+    m1, c1, _ = oracle.token_mismatch_masked(a, b, np.ones(5000, np.uint8))
+    assert (m1, c1) == (m, c)
+
+
+def test_masked_metric_closed_form_on_masked_tokens():
+    """Masked tokens differ by exactly d, the others by anything: metric = e^|d|."""
+    rng = np.random.default_rng(12)
+    n = 4096
+    mask = (rng.random(n) < 0.37).astype(np.uint8)
+    # multiples of 2^-10 in (-8, 0]: b + d is exact in binary32
+    b = (np.round(rng.uniform(-8, 0, n) * 1024) / 1024).astype(np.float32)
+    d = np.float32(-0.375)
+    a = np.where(mask == 1, b + d, rng.normal(0, 3, n)).astype(np.float32)
+    assert (a[mask == 1] - b[mask == 1] == d).all()
+    m, c, w = oracle.token_mismatch_masked(a, b, mask)
+    assert c == int(mask.sum())
+    assert abs(m - math.exp(0.375)) <= 1e-12          # summation of equal terms only
+    assert np.allclose(w[mask == 1], math.exp(-0.375), rtol=1e-15, atol=0)
+    assert (w[mask == 0] == 0).all()
+
+
+def test_importance_weights_direction_and_cap():
+    """w = p_train / p_rollout: a token the rollout model found less likely
+    than the trained model gets weight > 1 (the pages' correction raises it)."""
+    b = np.log(np.array([0.5, 0.01, 0.2, 0.9], np.float32))        # rollout
+    a = np.log(np.array([0.5, 0.05, 0.1, 0.9], np.float32))        # train
+    _, _, w = oracle.token_mismatch_masked(a, b)
+    ratio = np.exp(a.astype(np.float64) - b.astype(np.float64))
+    assert np.allclose(w, ratio, rtol=1e-15)
+    assert w[0] == 1.0 and w[3] == 1.0
+    assert w[1] > 1.0 and w[2] < 1.0
+    assert abs(w[1] - 5.0) < 1e-5 and abs(w[2] - 0.5) < 1e-6
+    _, _, wc = oracle.token_mismatch_masked(a, b, cap=2.0)
+    assert wc[1] == 2.0 and np.array_equal(wc[[0, 2, 3]], w[[0, 2, 3]])
+    _, _, wz = oracle.token_mismatch_masked(a, b, cap=0.0)        # no cap
+    assert np.array_equal(wz, w)
+
+
+def test_masked_metric_subset_and_empty():
+    rng = np.random.default_rng(13)
+    a = rng.normal(-3, 1, 1000).astype(np.float32)
+    b = (a + rng.normal(0, 0.1, 1000)).astype(np.float32)
+    mask = np.zeros(1000, np.uint8)
+    mask[::3] = 1
+    m, c, _ = oracle.token_mismatch_masked(a, b, mask)
+    assert c == 334
+    direct = np.mean(np.exp(np.abs(a[::3].astype(np.float64) - b[::3].astype(np.float64))))
+    assert abs(m - direct) <= 1e-14 * direct
+    m0, c0, w0 = oracle.token_mismatch_masked(a, b, np.zeros(1000, np.uint8))
+    assert c0 == 0 and math.isnan(m0) and (w0 == 0).all()
