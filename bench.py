@@ -53,6 +53,7 @@ BYTES_PER_ELEM = {
     # BF16 in, 1x128 codes + scales out, 128x1 codes + scales out
     "quant_dual_1x128_128x1": 2 + 1 + 1 + 4 / 128 + 4 / 128,
     "token_mult_prob_error": 8,                  # two FP32 per token
+    "token_mismatch_masked": 4 + 4 + 1 + 4,      # two FP32 and the mask in, the weight out
 }
 
 
@@ -359,7 +360,8 @@ class SyncStep:
 
 
 class MetricStep:
-    """token-mult-prob-error over n = 4,194,304 tokens."""
+    """token-mult-prob-error over n = 4,194,304 tokens, and the masked variant
+    with per-token importance weights (75% of the tokens in the mask)."""
 
     def __init__(self, device, seed: int = 0, n: int = 4_194_304):
         import torch
@@ -371,22 +373,33 @@ class MetricStep:
         self.out = torch.empty((1,), dtype=torch.float32, device=device)
         self.ws = torch.empty((max(jet.workspace_bytes("token_mult_prob_error", n), 16),),
                               dtype=torch.uint8, device=device)
-        # an L2-sized scratch written between steps so the 33.5 MB inputs are
+        g = torch.Generator().manual_seed(seed + 5000)
+        self.mask = (torch.rand(n, generator=g) < 0.75).to(torch.uint8).to(device)
+        self.w = torch.empty((n,), dtype=torch.float32, device=device)
+        self.mout = torch.empty((1,), dtype=torch.float32, device=device)
+        self.mcount = torch.empty((1,), dtype=torch.int64, device=device)
+        self.mws = torch.empty((max(jet.workspace_bytes("token_mismatch_masked", n), 16),),
+                               dtype=torch.uint8, device=device)
+        # an L2-sized scratch written before each call so that its inputs are
         # read from HBM every step
         self.flush = torch.empty((256 << 20,), dtype=torch.uint8, device=device)
-        self.work = {"token_mult_prob_error": n * BYTES_PER_ELEM["token_mult_prob_error"]}
-        self.bytes = self.work["token_mult_prob_error"]
+        self.work = {"token_mult_prob_error": n * BYTES_PER_ELEM["token_mult_prob_error"],
+                     "token_mismatch_masked": n * BYTES_PER_ELEM["token_mismatch_masked"]}
+        self.bytes = sum(self.work.values())
         self.flops = 0
-        self.launches_per_step = 2
+        self.launches_per_step = 4
         self.primary = ("GB/s", self.bytes)
-        self.config = {"workload": f"metric_n{n}", "tokens": n,
-                       "l2": "flushed: 256 MB written between steps, outside the kernel's events"}
+        self.config = {"workload": f"metric_n{n}", "tokens": n, "masked_fraction": 0.75,
+                       "l2": "flushed: 256 MB written before each call, outside the kernels' events"}
 
     def calls(self):
         j = self.jet
         return [("l2_flush", lambda: self.flush.fill_(1), "flush"),
                 ("token_mult_prob_error", lambda: j.jet_token_mult_prob_error(
-                    self.a, self.b, self.out, self.ws), "n")]
+                    self.a, self.b, self.out, self.ws), "n"),
+                ("l2_flush", lambda: self.flush.fill_(1), "flush"),
+                ("token_mismatch_masked", lambda: j.jet_token_mismatch_masked(
+                    self.a, self.b, self.mask, 0.0, self.w, self.mout, self.mcount, self.mws), "n")]
 
 
 def make_step(args, device, rank):

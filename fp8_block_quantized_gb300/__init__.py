@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     jet_quant_dual_1x128_128x1,
     jet_quant_w_128x128,
     jet_requant_128x1,
+    jet_token_mismatch_masked,
     jet_token_mult_prob_error,
     load,
     quant_act_1x128,
@@ -25,6 +26,7 @@ from .binding import (  # noqa: F401
     requant_128x1,
     selftest_bounded_wait,
     selftest_quotient,
+    token_mismatch_masked,
     token_mult_prob_error,
     workspace_bytes,
 )

@@ -22,7 +22,7 @@ STATUS = {0: "JET_OK", 1: "JET_ERR_NULL", 2: "JET_ERR_SHAPE", 3: "JET_ERR_ALIGN"
           7: "JET_ERR_TIMEOUT"}
 OP = {"quant_act_1x128": 0, "quant_w_128x128": 1, "requant_128x1": 2,
       "gemm_fp8_fwd": 3, "gemm_fp8_dgrad": 4, "gemm_fp8_wgrad": 5,
-      "token_mult_prob_error": 6, "quant_dual_1x128_128x1": 7}
+      "token_mult_prob_error": 6, "quant_dual_1x128_128x1": 7, "token_mismatch_masked": 8}
 
 # name -> argtypes (restype is int status unless listed in _RESTYPE)
 P, I, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
@@ -38,6 +38,7 @@ SIGNATURES = {
     "jet_gemm_fp8_wgrad": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_token_mult_prob_error": [P, P, I, P, P, Z, P],
     "jet_token_mult_prob_error_noalloc": [P, P, I, P, P],
+    "jet_token_mismatch_masked": [P, P, P, I, ctypes.c_float, P, P, P, P, Z, P],
     "jet_workspace_bytes": [ctypes.c_int, I, I, I],
     "jet_device_status": [P, ctypes.POINTER(ctypes.c_uint32)],
     "jet_selftest_bounded_wait": [ctypes.c_uint32, P],
@@ -245,6 +246,24 @@ def jet_token_mult_prob_error_noalloc(logp_train, logp_rollout, out, stream=None
         _ptr(logp_train), _ptr(logp_rollout), n, _ptr(out), _stream(stream)))
 
 
+def jet_token_mismatch_masked(logp_train, logp_rollout, mask, cap, w, out, count, ws,
+                              stream=None):
+    import torch
+    n = logp_train.numel()
+    _need(logp_train, torch.float32, (n,), "logp_train")
+    _need(logp_rollout, torch.float32, (n,), "logp_rollout")
+    if mask is not None:
+        _need(mask, torch.uint8, (n,), "mask")
+    if w is not None:
+        _need(w, torch.float32, (n,), "w")
+    _need(out, torch.float32, (1,), "out")
+    if count is not None:
+        _need(count, torch.int64, (1,), "count")
+    _check("jet_token_mismatch_masked", load().jet_token_mismatch_masked(
+        _ptr(logp_train), _ptr(logp_rollout), _ptr(mask), n, float(cap), _ptr(w), _ptr(out),
+        _ptr(count), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
 # --------------------------------------------------------------------------
 # Allocation helpers (torch owns the memory; the library never allocates).
 # --------------------------------------------------------------------------
@@ -329,3 +348,17 @@ def token_mult_prob_error(logp_train, logp_rollout, stream=None):
                      dtype=torch.uint8, device=logp_train.device)
     jet_token_mult_prob_error(logp_train, logp_rollout, out, ws, stream)
     return out
+
+
+def token_mismatch_masked(logp_train, logp_rollout, mask=None, cap: float = 0.0, stream=None):
+    """(metric [1], count [1], w [n]) for the masked tokens; see the C header."""
+    import torch
+    n = logp_train.numel()
+    dev = logp_train.device
+    out = torch.empty((1,), dtype=torch.float32, device=dev)
+    count = torch.empty((1,), dtype=torch.int64, device=dev)
+    w = torch.empty((n,), dtype=torch.float32, device=dev)
+    ws = torch.empty((max(workspace_bytes("token_mismatch_masked", n), 16),), dtype=torch.uint8,
+                     device=dev)
+    jet_token_mismatch_masked(logp_train, logp_rollout, mask, cap, w, out, count, ws, stream)
+    return out, count, w

@@ -62,6 +62,8 @@ jet_status current_device(DeviceInfo *info) {
 int jet_metric_blocks(int64_t n);
 // FP32 partial tiles of a split-contraction GEMM (0 when it is not split).
 size_t jet_gemm_workspace(int op, int64_t M, int64_t N, int64_t K);
+// Per-block sums and counts of the masked metric's first pass.
+size_t jet_mismatch_masked_workspace(int64_t n);
 
 extern "C" {
 
@@ -89,6 +91,8 @@ size_t jet_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
     case JET_OP_GEMM_FWD:
     case JET_OP_GEMM_DGRAD:
         return jet_gemm_workspace(op, M, N, K);
+    case JET_OP_TOKEN_MISMATCH_MASKED:
+        return jet_mismatch_masked_workspace(M);
     default:
         return 0;
     }

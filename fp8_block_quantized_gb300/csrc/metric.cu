@@ -165,3 +165,114 @@ extern "C" jet_status jet_token_mult_prob_error_noalloc(const float *logp_train,
     // call, so the array needs no clearing between calls.
     return jet_metric_launch(logp_train, logp_rollout, n, out, partial, jet::as_stream(stream));
 }
+
+// ---------------------------------------------------------------------------
+// Masked metric with per-token importance weights, one pass over the tokens.
+// The importance weight of a token is the ratio of the training model's
+// probability of it to the rollout model's ("FP8-RL" article: the ratio of
+// the original to the compressed model's token probability; nmedialink page,
+// section "重要抽样技术：提升RL精度的尖兵"): w_i = exp(a_i - b_i) with
+// a = logp_train, b = logp_rollout, capped at `cap` when cap > 0 (the pages
+// give no constant), 0 outside the mask.  The metric is token-mult-prob-error
+// over the masked tokens.  Pass 1: four tokens per thread and step (16-byte
+// loads of a and b, one 4-byte load of the mask, a 16-byte store of w), FP32
+// sums per thread, FP64 per block; pass 2 adds the block partials in order.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+__device__ __forceinline__ float is_weight(float d, float cap) {
+    const float w = expf(d);
+    return cap > 0.0f ? fminf(w, cap) : w;
+}
+
+__global__ void __launch_bounds__(kThreads)
+tmm_partial_kernel(const float *__restrict__ a, const float *__restrict__ b,
+                   const uint8_t *__restrict__ mask, int64_t n, float cap,
+                   float *__restrict__ w, double *__restrict__ partial) {
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
+    float acc = 0.0f;
+    int cnt = 0;
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    const int64_t n4 = n >> 2;
+    for (int64_t i = tid; i < n4; i += stride) {
+        const float4 x = ld_stream_f4(a + 4 * i);
+        const float4 y = ld_stream_f4(b + 4 * i);
+        const uint32_t m4 = mask ? *reinterpret_cast<const uint32_t *>(mask + 4 * i) : 0x01010101u;
+        const float d[4] = {x.x - y.x, x.y - y.y, x.z - y.z, x.w - y.w};
+        float wv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool on = ((m4 >> (8 * j)) & 0xFFu) != 0u;
+            wv[j] = on ? is_weight(d[j], cap) : 0.0f;
+            acc += on ? expf(fabsf(d[j])) : 0.0f;
+            cnt += on ? 1 : 0;
+        }
+        if (w) *reinterpret_cast<float4 *>(w + 4 * i) = make_float4(wv[0], wv[1], wv[2], wv[3]);
+    }
+    for (int64_t i = 4 * n4 + tid; i < n; i += stride) {
+        const bool on = mask == nullptr || mask[i] != 0;
+        const float d = a[i] - b[i];
+        if (w) w[i] = on ? is_weight(d, cap) : 0.0f;
+        acc += on ? expf(fabsf(d)) : 0.0f;
+        cnt += on ? 1 : 0;
+    }
+    const double t = block_sum((double)acc);
+    __syncthreads();  // block_sum's shared scratch is reused below
+    const double c = block_sum((double)cnt);
+    if (threadIdx.x == 0) {
+        partial[2 * blockIdx.x] = t;
+        partial[2 * blockIdx.x + 1] = c;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+tmm_final_kernel(const double *__restrict__ partial, int nblocks, float *out, int64_t *count) {
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
+    double v = 0.0, c = 0.0;
+    for (int i = threadIdx.x; i < nblocks; i += kThreads) {
+        v += partial[2 * i];
+        c += partial[2 * i + 1];
+    }
+    const double t = block_sum(v);
+    __syncthreads();
+    const double tc = block_sum(c);
+    if (threadIdx.x == 0) {
+        *out = tc > 0.0 ? (float)(t / tc) : __int_as_float(0x7fc00000);  // NaN: no masked token
+        if (count) *count = (int64_t)tc;
+    }
+}
+
+}  // namespace
+
+// Workspace of jet_token_mismatch_masked: a sum and a count per first-pass block.
+size_t jet_mismatch_masked_workspace(int64_t n) {
+    return n > 0 ? (size_t)jet_metric_blocks(n) * 2 * sizeof(double) : 0;
+}
+
+extern "C" jet_status jet_token_mismatch_masked(const float *logp_train, const float *logp_rollout,
+                                                const uint8_t *mask, int64_t n, float cap,
+                                                float *w, float *out, int64_t *count, void *ws,
+                                                size_t ws_bytes, jet_stream_t stream) {
+    JET_REQUIRE(logp_train && logp_rollout && out, JET_ERR_NULL);
+    JET_REQUIRE(n >= 1, JET_ERR_SHAPE);
+    JET_REQUIRE(jet::aligned16(logp_train) && jet::aligned16(logp_rollout) &&
+                    jet::aligned16(mask) && jet::aligned16(w) && jet::aligned16(out) &&
+                    jet::aligned16(count) && jet::aligned16(ws),
+                JET_ERR_ALIGN);
+    JET_REQUIRE(ws != nullptr && ws_bytes >= jet_mismatch_masked_workspace(n), JET_ERR_WORKSPACE);
+    jet::DeviceInfo dev;
+    jet_status st = jet::current_device(&dev);
+    if (st != JET_OK) return st;
+    const int g = jet_metric_blocks(n);
+    double *partial = static_cast<double *>(ws);
+    cudaStream_t s = jet::as_stream(stream);
+    st = jet::launch_pdl(tmm_partial_kernel, dim3(g), dim3(kThreads), 0, s, logp_train,
+                         logp_rollout, mask, n, cap, w, partial);
+    if (st != JET_OK) return st;
+    return jet::launch_pdl(tmm_final_kernel, dim3(1), dim3(kThreads), 0, s,
+                           static_cast<const double *>(partial), g, out, count);
+}

@@ -71,7 +71,8 @@ typedef enum {
     JET_OP_GEMM_DGRAD = 4,
     JET_OP_GEMM_WGRAD = 5,
     JET_OP_TOKEN_MULT_PROB_ERROR = 6,
-    JET_OP_QUANT_DUAL_1X128_128X1 = 7
+    JET_OP_QUANT_DUAL_1X128_128X1 = 7,
+    JET_OP_TOKEN_MISMATCH_MASKED = 8
 } jet_op;
 
 /* A cudaStream_t handle passed as an opaque pointer. */
@@ -240,8 +241,33 @@ JET_API jet_status jet_token_mult_prob_error_noalloc(const float *logp_train,
                                                      jet_stream_t stream);
 
 /*
+ * The mismatch metric over a subset of the tokens, fused with the per-token
+ * importance weights of the training loss, in one pass over the tokens.
+ * Source: nmedialink.com page, sections "FP8面临的关键挑战：数值分歧" (the
+ * metric) and "重要抽样技术：提升RL精度的尖兵" (importance sampling with FP8);
+ * m.66260.cn FP8-RL article (the weight is the ratio of the original to the
+ * compressed model's token probability).  With a = logp_train, b =
+ * logp_rollout and mask m (the tokens that count, e.g. a response mask):
+ *   w_i = m_i ? min(exp(a_i - b_i), cap) : 0        (no cap when cap <= 0;
+ *                                                    the pages give none)
+ *   out = sum_{m_i} exp(|a_i - b_i|) / count,  count = #{i : m_i != 0}
+ * exp in FP32 per token, sums in FP32 per thread and FP64 across threads and
+ * blocks in a fixed order; out is NaN when no token counts.
+ *   logp_train, logp_rollout [n] FP32 (in), n >= 1.
+ *   mask [n] uint8 (in; nonzero = the token counts), or NULL: every token.
+ *   w [n] FP32 (out), or NULL: the weights are not written.
+ *   out: one FP32 (out); count: one int64 (out), or NULL.  Device pointers.
+ *   ws / ws_bytes: at least jet_workspace_bytes(JET_OP_TOKEN_MISMATCH_MASKED,
+ *   n, 0, 0) bytes of device memory.
+ */
+JET_API jet_status jet_token_mismatch_masked(const float *logp_train, const float *logp_rollout,
+                                             const uint8_t *mask, int64_t n, float cap, float *w,
+                                             float *out, int64_t *count, void *ws,
+                                             size_t ws_bytes, jet_stream_t stream);
+
+/*
  * Workspace bytes an operation needs for the given sizes (0 if none).
- * For JET_OP_TOKEN_MULT_PROB_ERROR pass n as M.  Returns 0 for negative sizes
+ * For JET_OP_TOKEN_MULT_PROB_ERROR and JET_OP_TOKEN_MISMATCH_MASKED pass n as M.  Returns 0 for negative sizes
  * or an unknown op.  Pure host function; needs no device.
  */
 JET_API size_t jet_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);

@@ -150,6 +150,19 @@ def test_metric_checks(lib):
     assert f(fake(A), fake(B), 4096, fake(C), fake(D), 8, None) == WORKSPACE  # needs 16
 
 
+def test_masked_metric_checks(lib):
+    f = lib.jet_token_mismatch_masked
+    op = binding.OP["token_mismatch_masked"]
+    need = lib.jet_workspace_bytes(op, 4096, 0, 0)
+    assert need == 2 * 8 * 2                               # two blocks: a sum and a count each
+    assert f(None, fake(B), None, 16, 0.0, None, fake(C), None, fake(D), 64, None) == NULL
+    assert f(fake(A), fake(B), None, 16, 0.0, None, None, None, fake(D), 64, None) == NULL
+    assert f(fake(A), fake(B), None, 0, 0.0, None, fake(C), None, fake(D), 64, None) == SHAPE
+    assert f(fake(A), fake(B), fake(MIS), 16, 0.0, None, fake(C), None, fake(D), 64, None) == ALIGN
+    assert f(fake(A), fake(B), None, 16, 0.0, None, fake(C), None, None, 0, None) == WORKSPACE
+    assert f(fake(A), fake(B), None, 4096, 0.0, None, fake(C), None, fake(D), need - 8, None) == WORKSPACE
+
+
 def test_selftest_limit_checks(lib):
     assert lib.jet_selftest_bounded_wait(0, None) == SHAPE
     assert lib.jet_selftest_bounded_wait(2_000_000, None) == SHAPE

@@ -65,3 +65,67 @@ def test_bounded_wait_times_out_and_context_survives(jet):
     assert code == 0 and word == 0
     a, b = wl.logprobs(4096)
     check(jet, a, b)                              # the context is still usable
+
+
+
+# ---------------------------------------------- masked metric + IS weights --
+
+def check_masked(jet, a, b, mask=None, cap=0.0, rtol=1e-5, wtol=2e-6):
+    """Metric within 1e-5 relative of the oracle; weights within a few FP32
+    ulps (expf of the FP32 difference against binary64); count exact."""
+    dev_mask = None if mask is None else torch.from_numpy(mask).cuda()
+    out, count, w = jet.token_mismatch_masked(a.cuda(), b.cuda(), dev_mask, cap)
+    ref, ref_count, ref_w = oracle.token_mismatch_masked(a.numpy(), b.numpy(), mask, cap)
+    got = float(out.cpu()[0])
+    assert int(count.cpu()[0]) == ref_count
+    if ref_count == 0:
+        assert math.isnan(got)
+    else:
+        assert abs(got - ref) <= rtol * ref, (got, ref)
+    gw = w.cpu().numpy().astype(np.float64)
+    on = ref_w != 0
+    assert (gw[~on] == 0).all()
+    assert np.allclose(gw[on], ref_w[on], rtol=wtol, atol=0), np.max(np.abs(gw[on] / ref_w[on] - 1))
+    if cap > 0:
+        assert (gw <= np.float32(cap)).all()
+    return got, ref
+
+
+@pytest.mark.parametrize("n", [1, 3, 4, 5, 2047, 2049, 100_003])
+def test_masked_sizes(jet, n):
+    a, b = wl.logprobs(n, seed=n)
+    mask = (np.random.default_rng(n).random(n) < 0.8).astype(np.uint8)
+    mask[0] = 1
+    check_masked(jet, a, b, mask)
+
+
+def test_masked_4m_tokens_with_cap(jet):
+    a, b = wl.logprobs(4_194_304, seed=7)
+    rng = np.random.default_rng(7)
+    mask = np.ones(4_194_304, np.uint8)
+    mask[rng.random(4_194_304) < 0.25] = 0          # prompt / padding tokens
+    check_masked(jet, a, b, mask, cap=1.01)
+
+
+def test_masked_without_mask_equals_plain_metric(jet):
+    a, b = wl.logprobs(100_000, seed=3)
+    got, _ = check_masked(jet, a, b, None)
+    plain = float(jet.token_mult_prob_error(a.cuda(), b.cuda()).cpu()[0])
+    assert abs(got - plain) <= 1e-6 * plain
+
+
+def test_masked_no_token_counts(jet):
+    a, b = wl.logprobs(1000, seed=4)
+    check_masked(jet, a, b, np.zeros(1000, np.uint8))
+
+
+def test_masked_optional_outputs(jet):
+    """w and count may be NULL; the metric is unchanged."""
+    a, b = wl.logprobs(5000, seed=5)
+    mask = torch.from_numpy((np.arange(5000) % 2).astype(np.uint8)).cuda()
+    out = torch.empty((1,), dtype=torch.float32, device="cuda")
+    ws = torch.empty((max(jet.workspace_bytes("token_mismatch_masked", 5000), 16),),
+                     dtype=torch.uint8, device="cuda")
+    jet.jet_token_mismatch_masked(a.cuda(), b.cuda(), mask, 0.0, None, out, None, ws)
+    ref, _, _ = oracle.token_mismatch_masked(a.numpy(), b.numpy(), mask.cpu().numpy())
+    assert abs(float(out.cpu()[0]) - ref) <= 1e-5 * ref
