@@ -807,10 +807,26 @@ constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
 }  // namespace
 
+// Forward products of one token, and of 2-4 tokens with M * N * K <= 2^25
+// (e.g. two tokens on a 4096 x 4096 weight, four on 1024 x 4096), run on the
+// CUDA-core kernel of gemv.cu (no workspace): its fixed cost per call is a
+// fraction of the split tensor-core path's, and at one token it also streams
+// the largest 8B weights faster; with more tokens its multiply-adds grow
+// with M and the tensor path wins (measured on the 8B projections).
+constexpr int64_t kGemvMaxRows = 4;
+constexpr int64_t kGemvMaxMacs = (int64_t)1 << 25;
+jet_status jet_gemv_fp8_fwd(const uint8_t *qx, const float *sx, const uint8_t *qw,
+                            const float *sw, int64_t M, int64_t N, int64_t K, uint16_t *y,
+                            int num_sms, cudaStream_t stream);
+inline bool use_gemv(int64_t M, int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0 || M < 1 || M > kGemvMaxRows) return false;
+    return M == 1 || M * N * K <= kGemvMaxMacs;
+}
+
 // Workspace bytes of a GEMM (JET_OP_GEMM_*), for jet_workspace_bytes().
 size_t jet_gemm_workspace(int op, int64_t M, int64_t N, int64_t K) {
     if (M < 0 || N < 0 || K < 0) return 0;
-    if (op == JET_OP_GEMM_FWD) return splitk_workspace(M, N, K);
+    if (op == JET_OP_GEMM_FWD) return use_gemv(M, N, K) ? 0 : splitk_workspace(M, N, K);
     if (op == JET_OP_GEMM_DGRAD) return splitk_workspace(M, K, N);
     return 0;
 }
@@ -830,8 +846,14 @@ jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx, const uint8_t *q
                     aligned16(y),
                 JET_ERR_ALIGN);
     JET_REQUIRE(aligned16(ws), JET_ERR_ALIGN);
-    const size_t need = splitk_workspace(M, N, K);
+    const size_t need = jet_gemm_workspace(JET_OP_GEMM_FWD, M, N, K);
     JET_REQUIRE(need == 0 || (ws && ws_bytes >= need), JET_ERR_WORKSPACE);
+    if (use_gemv(M, N, K)) {  // decode: weight streaming
+        DeviceInfo dev;
+        jet_status st = current_device(&dev);
+        if (st != JET_OK) return st;
+        return jet_gemv_fp8_fwd(qx, sx, qw, sw, M, N, K, y, dev.num_sms, as_stream(stream));
+    }
     return run_gemm<kFwd>(qx, sx, qw, sw, y, M, N, K, ws, stream);
 }
 

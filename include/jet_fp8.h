@@ -154,12 +154,16 @@ JET_API jet_status jet_quant_dual_1x128_128x1(const uint16_t *x, int64_t M, int6
  *   y  [M][N] BF16 bits (out).  K == 0 writes zeros.
  *   ws / ws_bytes: device workspace of at least
  *   jet_workspace_bytes(JET_OP_GEMM_FWD, M, N, K) bytes, else JET_ERR_WORKSPACE
- *   (NULL/0 allowed when that is 0).  It is non-zero only for M <= 128, where
- *   the contraction is split into ranges whose FP32 partial tiles
+ *   (NULL/0 allowed when that is 0).  It can be non-zero only for M <= 512,
+ *   where the contraction may be split into ranges whose FP32 partial tiles
  *   [splits][M][N] go to ws and are then summed in a fixed order and rounded
  *   once to BF16; the split depends only on (M, N, K), so results are the same
  *   on every call and every device.  Its contents need no initialisation and
  *   are scratch after the call; concurrent calls need separate workspaces.
+ *   M == 1, and 2 <= M <= 4 with M * N * K <= 2^25 (decode), run a weight-streaming kernel
+ *   on CUDA cores with the same arithmetic (exact code products, FP32 sums
+ *   per scale group, scaled and summed in a fixed order) and needs no
+ *   workspace.
  */
 JET_API jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx,
                             const uint8_t *qw, const float *sw, int64_t M,

@@ -53,10 +53,16 @@ def test_workspace_bytes(lib):
         assert lib.jet_workspace_bytes(op[name], 8192, 4096, 4096) == 0
     # split contraction for at most 128 output rows: FP32 partials [splits][R][C]
     fwd, dgrad, wgrad = op["gemm_fp8_fwd"], op["gemm_fp8_dgrad"], op["gemm_fp8_wgrad"]
-    assert lib.jet_workspace_bytes(fwd, 1, 4096, 4096) == 9 * 1 * 4096 * 4      # 16 tiles
+    assert lib.jet_workspace_bytes(fwd, 1, 4096, 4096) == 0                     # decode kernel
+    assert lib.jet_workspace_bytes(fwd, 1, 14336, 4096) == 0                    # one token: always
+    assert lib.jet_workspace_bytes(fwd, 2, 4096, 4096) == 0                     # M N K = 2^25
+    assert lib.jet_workspace_bytes(fwd, 4, 1024, 4096) == 0
+    assert lib.jet_workspace_bytes(fwd, 4, 4096, 4096) == 9 * 4 * 4096 * 4      # M N K > 2^25: split
+    assert lib.jet_workspace_bytes(fwd, 2, 14336, 4096) == 2 * 2 * 14336 * 4
+    assert lib.jet_workspace_bytes(fwd, 5, 4096, 4096) == 9 * 5 * 4096 * 4      # 16 tiles
     assert lib.jet_workspace_bytes(fwd, 64, 4096, 4096) == 8 * 64 * 4096 * 4    # K/(8M) = 8
     assert lib.jet_workspace_bytes(fwd, 64, 14336, 4096) == 2 * 64 * 14336 * 4  # 56 tiles
-    assert lib.jet_workspace_bytes(fwd, 1, 1024, 4096) == 32 * 1024 * 4         # one per slice
+    assert lib.jet_workspace_bytes(fwd, 16, 1024, 4096) == 32 * 16 * 1024 * 4   # one per slice
     assert lib.jet_workspace_bytes(fwd, 128, 128, 128) == 0                     # one slice
     assert lib.jet_workspace_bytes(fwd, 129, 4096, 4096) == 3 * 129 * 4096 * 4  # two row tiles
     assert lib.jet_workspace_bytes(fwd, 256, 4096, 14336) == 4 * 256 * 4096 * 4

@@ -100,6 +100,22 @@ def test_fwd_ragged_rows_and_widths(jet, M, N):
     run_fwd(jet, wl.activations(M, 512, seed=M, config=2), wl.weights(N, 512, seed=N, config=2))
 
 
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (1024, 640), (384, 1152), (4096, 14336)])
+def test_fwd_decode_rows(jet, M, N, K):
+    # at most 4 tokens: the weight-streaming kernel (K tails of 128 / 384 codes included)
+    run_fwd(jet, wl.activations(M, K, seed=M * 7 + K, config=2), wl.weights(N, K, seed=N + K, config=2),
+            nrows=None)
+
+
+def test_fwd_decode_deterministic(jet):
+    x, w = wl.activations(3, 4096, seed=21, config=2), wl.weights(4096, 4096, seed=21, config=2)
+    qx, sx, qw, sw = (to_dev(a) for a in quant_pair(x, w))
+    y1 = jet.gemm_fp8_fwd(qx, sx, qw, sw)
+    y2 = jet.gemm_fp8_fwd(qx, sx, qw, sw)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
 @pytest.mark.parametrize("M,N,K", [(200, 256, 384), (128, 128, 256), (256, 512, 128),
                                    (384, 512, 512), (300, 256, 512)])
 def test_dgrad_shapes(jet, M, N, K):
