@@ -32,6 +32,10 @@
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream).  Launch failures return JET_ERR_CUDA.  Device-side
  *    bounded waits that give up are reported by jet_device_status().
+ *  - Kernels are launched with programmatic dependent launch allowed: their
+ *    blocks may start while earlier work on the stream finishes, but each
+ *    waits for that work to complete before it reads or writes memory, so
+ *    stream order holds (also inside captured CUDA graphs).
  *  - Non-finite inputs are outside the contract (their codes are unspecified).
  *  - Calls are reentrant; concurrent calls must not share output buffers.
  */
