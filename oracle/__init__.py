@@ -240,6 +240,31 @@ def gemm_fwd(qx, sx, qw, sw, rows=None, nthreads=None):
     return _gemm(_load().jo_gemm_fwd, qx, sx, qw, sw, M, N, K, M, N, rows, nthreads)
 
 
+def gemm_fwd_grouped(qx, sx, qw, sw, offsets, nthreads=None):
+    """Grouped forward product of expert linears: for every expert e,
+    Y[o_e:o_{e+1}] = dq(X[o_e:o_{e+1}]) . dq(W_e)^T in binary64.
+
+    X [Mtot,K] holds the tokens of all experts in expert order (sx [K/128,
+    Mtot]); W [E,N,K] the experts' weights (sw [E,N/128,K/128]); offsets
+    [E+1] the experts' first rows (offsets[0] = 0, non-decreasing,
+    offsets[E] = Mtot).  Each expert's rows are the plain forward product of
+    its own tokens and weights (its definition and pins are gemm_fwd's)."""
+    qw = np.asarray(qw)
+    sw = np.asarray(sw)
+    E, N, K = qw.shape
+    off = np.asarray(offsets, np.int64)
+    assert off.shape == (E + 1,) and off[0] == 0 and (np.diff(off) >= 0).all()
+    assert np.shape(qx) == (off[-1], K) and np.shape(sx) == (K // 128, off[-1])
+    assert sw.shape == (E, N // 128, K // 128)
+    out = np.zeros((int(off[-1]), N), np.float64)
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            out[a:b] = gemm_fwd(np.ascontiguousarray(qx[a:b]), np.ascontiguousarray(sx[:, a:b]),
+                                qw[e], sw[e], nthreads=nthreads)
+    return out
+
+
 def gemm_dgrad(qdy, sdy, qw, sw, rows=None, nthreads=None):
     """dX = dq(dY) . dq(W) in binary64; dY [M,N] (sdy [N/128,M]), W [N,K]."""
     M, N = np.shape(qdy)

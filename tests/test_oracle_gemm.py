@@ -109,3 +109,32 @@ def test_transposition_relations():
     dYf = c.dy.double().numpy()
     exact = dYf.T @ Xf
     assert rel_err(dW, exact) < 0.1
+
+
+def test_grouped_forward_is_per_expert_forward():
+    """Expert e's rows use only expert e's tokens and weights; an expert with
+    no tokens contributes nothing; a single expert is the plain forward."""
+    rng = np.random.default_rng(5)
+    E, N, K = 4, 256, 384
+    counts = np.array([3, 0, 130, 7])
+    off = np.concatenate([[0], np.cumsum(counts)])
+    Mt = int(off[-1])
+    qx = rand_q(rng, (Mt, K))
+    sx = rng.uniform(0.01, 1, (K // 128, Mt)).astype(np.float32)
+    qw = rand_q(rng, (E, N, K))
+    sw = rng.uniform(0.01, 1, (E, N // 128, K // 128)).astype(np.float32)
+    y = oracle.gemm_fwd_grouped(qx, sx, qw, sw, off)
+    assert y.shape == (Mt, N)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b > a:
+            ref = dq_rows(qx[a:b], sx[:, a:b]) @ dq_blocks(qw[e], sw[e]).T
+            assert rel_err(y[a:b], ref) < 1e-12
+    # swapping two experts' weights changes exactly their rows
+    qw2, sw2 = qw.copy(), sw.copy()
+    qw2[[0, 3]], sw2[[0, 3]] = qw[[3, 0]], sw[[3, 0]]
+    y2 = oracle.gemm_fwd_grouped(qx, sx, qw2, sw2, off)
+    assert np.array_equal(y2[off[1]:off[3]], y[off[1]:off[3]])
+    assert not np.allclose(y2[:off[1]], y[:off[1]])
+    one = oracle.gemm_fwd_grouped(qx[:3], sx[:, :3].copy(), qw[:1], sw[:1], np.array([0, 3]))
+    assert np.array_equal(one, oracle.gemm_fwd(qx[:3], sx[:, :3].copy(), qw[0], sw[0]))
