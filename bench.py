@@ -359,6 +359,75 @@ class SyncStep:
         return out
 
 
+class MoeStep:
+    """Forward of the expert linears of one Qwen3-30B-A3B-shaped MoE layer
+    (4096 tokens, top-8 of 128 experts, 32768 routed rows): 1x128
+    quantization of the routed gate_up input, the grouped gate_up product
+    (N = 1536, K = 2048 per expert), 1x128 quantization of the routed down
+    input, the grouped down product (N = 2048, K = 768).  The routing (row
+    offsets per expert) and the experts' FP8 weights are prepared beforehand
+    and not timed."""
+
+    def __init__(self, device, seed: int = 0):
+        import torch
+        from fp8_block_quantized_gb300 import workloads as wl
+        import fp8_block_quantized_gb300 as jet
+
+        self.jet = jet
+        off, lins = wl.moe_layer(seed=seed, device=device)
+        self.off = off
+        self.M = M = int(off[-1].item())
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        self.lin = []
+        flops = nbytes = 0
+        counts = (off[1:] - off[:-1]).cpu()
+        for name, x, w in lins:
+            E, N, K = w.shape
+            qw = e((E, N, K), torch.uint8)
+            sw = e((E, N // 128, K // 128), torch.float32)
+            for i in range(E):
+                jet.jet_quant_w_128x128(w[i], qw[i], sw[i])
+            self.lin.append({"name": name, "x": x, "K": K, "N": N, "qw": qw, "sw": sw,
+                             "q": e((M, K), torch.uint8), "s": e((K // 128, M), torch.float32),
+                             "y": e((M, N), torch.bfloat16)})
+            flops += 2 * M * N * K
+            used = int((counts > 0).sum())
+            nbytes += M * K + 4 * M * K // 128 + used * (N * K + 4 * N * K // 16384) + 2 * M * N
+        torch.cuda.synchronize()
+        self.flops = flops
+        self.work = {"gemm_fp8_fwd_grouped": flops, "gemm_fp8_fwd_grouped_bytes": nbytes,
+                     "quant_act_1x128": sum(M * L["K"] for L in self.lin)
+                     * BYTES_PER_ELEM["quant_act_1x128"]}
+        self.launches_per_step = 2 * len(self.lin)
+        self.primary = ("TFLOP/s", flops)
+        tiles = int(((counts + 127) // 128).sum())
+        self.config = {"workload": f"moe_qwen3_30b_a3b_T{wl.MOE_TOKENS}",
+                       "tokens": wl.MOE_TOKENS, "experts": wl.MOE_EXPERTS, "topk": wl.MOE_TOPK,
+                       "routed_rows": M, "linears": [(L["name"], L["N"], L["K"]) for L in self.lin],
+                       "rows_per_expert": [int(counts.min()), int(counts.max())],
+                       "row_tiles": tiles, "dense_row_tiles": (M + 127) // 128,
+                       "gemm_tflop_per_step": round(flops / 1e12, 4),
+                       "l2": "no flush: per-step working set (~0.9 GB) > 129 MB L2"}
+
+    def calls(self):
+        j, out = self.jet, []
+        for L in self.lin:
+            out.append(("quant_act_1x128", lambda L=L: j.jet_quant_act_1x128(L["x"], L["q"], L["s"]),
+                        "x_" + L["name"]))
+            out.append(("gemm_fp8_fwd_grouped", lambda L=L: j.jet_gemm_fp8_fwd_grouped(
+                L["q"], L["s"], L["qw"], L["sw"], self.off, L["y"]), L["name"]))
+        return out
+
+    def host_io(self):
+        import torch
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        self.h_in = [(pin(L["x"]), L["x"]) for L in self.lin] + [(pin(self.off), self.off)]
+        self.h_out = [(torch.empty(L["y"].shape, dtype=L["y"].dtype, pin_memory=True), L["y"])
+                      for L in self.lin]
+        nbytes = lambda pairs: sum(h.numel() * h.element_size() for h, _ in pairs)
+        return nbytes(self.h_in), nbytes(self.h_out)
+
+
 class MetricStep:
     """token-mult-prob-error over n = 4,194,304 tokens, and the masked variant
     with per-token importance weights (75% of the tokens in the mask)."""
@@ -409,6 +478,8 @@ def make_step(args, device, rank):
         return RolloutStep(args.tokens, device, seed=args.seed + rank)
     if args.workload == "sync":
         return SyncStep(device, seed=args.seed + rank)
+    if args.workload == "moe":
+        return MoeStep(device, seed=args.seed + rank)
     return MetricStep(device, seed=args.seed + rank)
 
 
@@ -831,10 +902,10 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("jet", "reference"), default="jet")
-    ap.add_argument("--workload", choices=("train8b", "train32b", "rollout", "sync", "metric"),
+    ap.add_argument("--workload", choices=("train8b", "train32b", "rollout", "sync", "metric", "moe"),
                     default="train8b",
                     help="train8b (default, the benchmark's workload), train32b, or the "
-                         "rollout / weight-sync / metric configurations")
+                         "rollout / weight-sync / metric / MoE expert-forward configurations")
     ap.add_argument("--tokens", type=int, default=2048, help="M for --workload rollout")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")

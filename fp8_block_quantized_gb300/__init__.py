@@ -9,9 +9,11 @@ from .binding import (  # noqa: F401
     device_status,
     gemm_fp8_dgrad,
     gemm_fp8_fwd,
+    gemm_fp8_fwd_grouped,
     gemm_fp8_wgrad,
     jet_gemm_fp8_dgrad,
     jet_gemm_fp8_fwd,
+    jet_gemm_fp8_fwd_grouped,
     jet_gemm_fp8_wgrad,
     jet_quant_act_1x128,
     jet_quant_dual_1x128_128x1,

@@ -34,6 +34,7 @@ SIGNATURES = {
     "jet_requant_128x1": [P, P, I, I, P, P, P],
     "jet_quant_dual_1x128_128x1": [P, I, I, P, P, P, P, P],
     "jet_gemm_fp8_fwd": [P, P, P, P, I, I, I, P, P, Z, P],
+    "jet_gemm_fp8_fwd_grouped": [P, P, P, P, P, I, I, I, I, P, P],
     "jet_gemm_fp8_dgrad": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_gemm_fp8_wgrad": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_token_mult_prob_error": [P, P, I, P, P, Z, P],
@@ -200,6 +201,23 @@ def jet_gemm_fp8_fwd(qx, sx, qw, sw, y, ws=None, stream=None):
     _gemm("jet_gemm_fp8_fwd", qx, sx, qw, sw, M, N, K, y, ws, stream)
 
 
+def jet_gemm_fp8_fwd_grouped(qx, sx, qw, sw, offsets, y, stream=None):
+    """Expert-grouped forward product; ``offsets`` is the int64 device tensor
+    of the E+1 row offsets of the experts' tokens in ``qx``."""
+    import torch
+    M, K = qx.shape
+    E, N = qw.shape[0], qw.shape[1]
+    _need(qx, torch.uint8, (M, K), "qx")
+    _need(sx, torch.float32, (K // 128, M), "sx")
+    _need(qw, torch.uint8, (E, N, K), "qw")
+    _need(sw, torch.float32, (E, N // 128, K // 128), "sw")
+    _need(offsets, torch.int64, (E + 1,), "offsets")
+    _need(y, torch.bfloat16, (M, N), "y")
+    _check("jet_gemm_fp8_fwd_grouped", load().jet_gemm_fp8_fwd_grouped(
+        _ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(offsets), E, M, N, K, _ptr(y),
+        _stream(stream)))
+
+
 def jet_gemm_fp8_dgrad(qdy, sdy, qw, sw, dx, ws=None, stream=None):
     import torch
     M, N = qdy.shape
@@ -319,6 +337,15 @@ def gemm_fp8_fwd(qx, sx, qw, sw, stream=None):
     N = qw.shape[0]
     y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device)
     jet_gemm_fp8_fwd(qx, sx, qw, sw, y, _ws("gemm_fp8_fwd", M, N, K, qx.device), stream)
+    return y
+
+
+def gemm_fp8_fwd_grouped(qx, sx, qw, sw, offsets, stream=None):
+    """Y [M][N] BF16: every expert's tokens times that expert's weights."""
+    import torch
+    M, N = qx.shape[0], qw.shape[1]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device)
+    jet_gemm_fp8_fwd_grouped(qx, sx, qw, sw, offsets, y, stream)
     return y
 
 

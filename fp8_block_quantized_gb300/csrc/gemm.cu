@@ -58,9 +58,13 @@ namespace {
 using namespace jet;
 using namespace jet::ptx;
 
-enum Mode { kFwd = 0, kDgrad = 1, kWgrad = 2 };
+// kFwdGrouped: the forward product of several expert linears in one launch
+// (tokens concatenated in expert order, weights stacked [E][N][K]).
+enum Mode { kFwd = 0, kDgrad = 1, kWgrad = 2, kFwdGrouped = 3 };
+constexpr int kMaxGroups = 384;  // one expert per thread of the unit-count scan
 
 constexpr int kThreads = 384;
+static_assert(kMaxGroups <= kThreads, "the unit-count scan takes one expert per thread");
 constexpr uint32_t kRegsControl = 72;    // warpgroup 0 after setmaxnreg
 constexpr uint32_t kRegsEpilogue = 200;  // warpgroups 1-2 after setmaxnreg
 static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168,
@@ -184,7 +188,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const __grid_constant__ CUtensorMap tmY, const float *__restrict__ sa,
                 const float *__restrict__ sb,
                 uint16_t *__restrict__ out, int R, int C, int D, Raster raster, int splits,
-                float *__restrict__ partial, unsigned *status) {
+                float *__restrict__ partial, const int64_t *__restrict__ goff, int gE,
+                unsigned *status) {
     using CF = Cfg<BN, CL>;
     constexpr int S = CF::kStages;
     constexpr int SS = CF::kScaleSlots;
@@ -195,6 +200,12 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     __shared__ uint64_t sfull_bar[SS], sempty_bar[SS];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
+    // grouped forward: per expert, its first row and the prefix of its units
+    constexpr bool kGrp = MODE == kFwdGrouped;
+    constexpr bool kFwdLike = MODE == kFwd || kGrp;
+    constexpr int kGT = kGrp ? kMaxGroups + 1 : 1;
+    __shared__ int g_off[kGT], g_pre[kGT];
+    __shared__ int g_warp[kThreads / 32];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t smem_base = (smem_u32(dyn_smem) + 1023u) & ~1023u;
@@ -203,7 +214,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int tiles_m = (R + BM - 1) / BM;
     const int tiles_n = C / BN;
     const int units_m = (tiles_m + CL - 1) / CL;  // row tiles per cluster step
-    const int total = units_m * tiles_n * splits;  // work units: (tile, contraction range)
+    int total = units_m * tiles_n * splits;  // work units: (tile, contraction range)
     const int nkb = D / BK;
     const uint32_t rank = kPair ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
@@ -249,6 +260,59 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const uint32_t tmem = tmem_base_sh;
     griddep_launch_dependents();
     griddep_wait();
+    if (kGrp) {
+        // Expert e owns rows off[e] .. off[e+1] (clamped to [0, R], so that
+        // nothing outside the output is ever written) and
+        // ceil(rows / 128) * tiles_n units; one expert per thread, then a
+        // block-wide inclusive scan of the unit counts.
+        const int i = threadIdx.x;
+        auto clampr = [&](int64_t v) { return (int)(v < 0 ? 0 : (v > R ? R : v)); };
+        int cnt = 0;
+        for (int j = i; j <= gE; j += kThreads) g_off[j] = clampr(goff[j]);  // gE + 1 entries
+        if (i < gE) {
+            const int rows = clampr(goff[i + 1]) - clampr(goff[i]);
+            cnt = rows > 0 ? (rows + BM - 1) / BM * tiles_n : 0;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        if (lane == 31) g_warp[warp] = incl;
+        __syncthreads();
+        int before = 0;
+        for (int j = 0; j < warp; ++j) before += g_warp[j];
+        if (i < gE) g_pre[i + 1] = before + incl;
+        if (i == 0) g_pre[0] = 0;
+        __syncthreads();
+        total = g_pre[gE];
+    }
+    // Work unit t -> row tile origin m0 (absolute row), column origin n0, its
+    // slice range, its row limit and the expert whose weights it uses.
+    auto coords = [&](int t, int &m0, int &n0, int &kb0, int &kb1, int &rlim, int &grp) {
+        if (kGrp) {
+            int lo = 0, hi = gE - 1;  // the expert e with g_pre[e] <= t < g_pre[e+1]
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (g_pre[mid] <= t) lo = mid; else hi = mid - 1;
+            }
+            const int u = t - g_pre[lo], mt = u / tiles_n;
+            grp = lo;
+            m0 = g_off[lo] + mt * BM;
+            n0 = (u - mt * tiles_n) * BN;
+            rlim = g_off[lo + 1] > g_off[lo] ? g_off[lo + 1] : g_off[lo];
+            kb0 = 0;
+            kb1 = nkb;
+        } else {
+            int mu, nt;
+            unit_coords(t, splits, nkb, units_m, tiles_n, raster, mu, nt, kb0, kb1);
+            m0 = (mu * CL + (int)rank) * BM;
+            n0 = nt * BN;
+            rlim = R;
+            grp = 0;
+        }
+    };
 
     // Each role is nested inside its own setmaxnreg branch so that the
     // register limit of one branch never applies to the other.
@@ -264,9 +328,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t it = 0;
             bool ok = true;
             for (int t = unit0; ok && t < total; t += unit_step) {
-                int mu, nt, kb0, kb1;
-                unit_coords(t, splits, nkb, units_m, tiles_n, raster, mu, nt, kb0, kb1);
-                const int m0 = (mu * CL + (int)rank) * BM, n0 = nt * BN;
+                int m0, n0, kb0, kb1, rlim, grp;
+                coords(t, m0, n0, kb0, kb1, rlim, grp);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
@@ -295,9 +358,9 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         for (int j = 0; j < BN / 128; ++j)
                             cp_async16(scol + (lane + 32 * j) * 16, src + 4 * (lane + 32 * j));
                     } else if (lane < BN / 128) {
-                        const float *src = MODE == kFwd
-                                               ? sb + (size_t)(n0 / 128 + lane) * nkb + kb
-                                               : sb + (size_t)kb * (C / 128) + n0 / 128 + lane;
+                        const float *src =
+                            kFwdLike ? sb + ((size_t)grp * (C / 128) + n0 / 128 + lane) * nkb + kb
+                                     : sb + (size_t)kb * (C / 128) + n0 / 128 + lane;
                         cp_async4(scol + lane * 4, src, 4u);
                     }
                     cp_async_arrive_noinc(&sfull_bar[ss]);
@@ -325,7 +388,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                     tma_load_2d(b_s + h * 128 * BK, &tmB, &full_bar[s],
                                                 n0 + 128 * h, kb * BK, pol_b);
                             } else {
-                                tma_load_2d(b_s, &tmB, &full_bar[s], kb * BK, n0, pol_b);
+                                tma_load_2d(b_s, &tmB, &full_bar[s], kb * BK, grp * C + n0,
+                                            pol_b);
                             }
                         }
                     }
@@ -348,8 +412,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t it = 0;
             bool ok = true;
             for (int t = unit0; ok && t < total; t += unit_step) {
-                int mu, nt, kb0, kb1;
-                unit_coords(t, splits, nkb, units_m, tiles_n, raster, mu, nt, kb0, kb1);
+                int m0, n0, kb0, kb1, rlim, grp;
+                coords(t, m0, n0, kb0, kb1, rlim, grp);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
@@ -430,11 +494,10 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         uint32_t it = 0;
         bool ok = true;
         for (int t = unit0; ok && t < total; t += unit_step) {
-            int mu, nt, kb0, kb1;
-            unit_coords(t, splits, nkb, units_m, tiles_n, raster, mu, nt, kb0, kb1);
-            const int m0 = (mu * CL + (int)rank) * BM, n0 = nt * BN;
+            int m0, n0, kb0, kb1, rlim, grp;
+            coords(t, m0, n0, kb0, kb1, rlim, grp);
             const int row = m0 + quad * 32 + lane;
-            const bool row_ok = row < R;
+            const bool row_ok = row < rlim;
             const int col0 = n0 + ch * H;
             float2 acc[H / 2];
 #pragma unroll
@@ -682,7 +745,8 @@ inline const CUtensorMap &tmA_arg(const CUtensorMap &m) { return m; }
 template <int BN, int MODE, int CL>
 jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, const uint8_t *b,
                   const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D, int splits,
-                  float *partial, cudaStream_t stream) {
+                  float *partial, cudaStream_t stream, const int64_t *goff = nullptr,
+                  int gE = 0) {
     using CF = Cfg<BN, CL>;
     auto kernel = gemm_fp8_kernel<BN, MODE, CL>;
     static std::mutex mu;
@@ -726,16 +790,19 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     if (!make_map_u8(&ta, a, (uint64_t)D, (uint64_t)R, BK, BM)) return JET_ERR_CUDA;
     if (CL == 2 && !make_map_out(&ty, out, (uint64_t)C, (uint64_t)R)) return JET_ERR_CUDA;
     if (CL == 1) ty = ta;  // unused by the single-CTA kernel
+    // grouped forward: B is the experts' weights stacked, [gE * C][D]
+    const uint64_t b_rows = MODE == kFwdGrouped ? (uint64_t)gE * (uint64_t)C : (uint64_t)C;
     bool okb = MODE == kDgrad ? make_map_u8(&tb, b, (uint64_t)C, (uint64_t)D, 128, BK)
-                              : make_map_u8(&tb, b, (uint64_t)D, (uint64_t)C, BK, CF::kBRows);
+                              : make_map_u8(&tb, b, (uint64_t)D, b_rows, BK, CF::kBRows);
     if (!okb) return JET_ERR_CUDA;
-    const int64_t units = ((R + BM * CL - 1) / (BM * CL)) * (C / BN) * splits;
+    // (grouped: at most one unit per expert more than the dense count)
+    const int64_t units = ((R + BM * CL - 1) / (BM * CL) + gE) * (C / BN) * splits;
     const int64_t grid_units = units < max_units[dev.ordinal] ? units : max_units[dev.ordinal];
     cfg.gridDim = dim3((unsigned)(grid_units * CL));
     const Raster raster = choose_raster(R, C, D);
     cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kernel, tmA_arg(ta), tmA_arg(tb), tmA_arg(ty), sa, sb, out,
-                           (int)R, (int)C, (int)D, raster, splits, partial,
+                           (int)R, (int)C, (int)D, raster, splits, partial, goff, gE,
                            dev.status_word) != cudaSuccess) {
         cudaGetLastError();
         return JET_ERR_CUDA;
@@ -855,6 +922,34 @@ jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx, const uint8_t *q
         return jet_gemv_fp8_fwd(qx, sx, qw, sw, M, N, K, y, dev.num_sms, as_stream(stream));
     }
     return run_gemm<kFwd>(qx, sx, qw, sw, y, M, N, K, ws, stream);
+}
+
+jet_status jet_gemm_fp8_fwd_grouped(const uint8_t *qx, const float *sx, const uint8_t *qw,
+                                    const float *sw, const int64_t *offsets, int64_t E,
+                                    int64_t M, int64_t N, int64_t K, uint16_t *y,
+                                    jet_stream_t stream) {
+    JET_REQUIRE(M >= 0 && N >= 0 && K >= 0 && E >= 1 && E <= kMaxGroups, JET_ERR_SHAPE);
+    const bool out_empty = (M == 0 || N == 0), in_empty = out_empty || K == 0;
+    JET_REQUIRE(out_empty || (y && offsets), JET_ERR_NULL);
+    JET_REQUIRE(in_empty || (qx && sx && qw && sw), JET_ERR_NULL);
+    JET_REQUIRE(N % 128 == 0 && K % 128 == 0 && M < kMaxDim && N < kMaxDim && K < kMaxDim &&
+                    E * N < kMaxDim,
+                JET_ERR_SHAPE);
+    JET_REQUIRE(aligned16(qx) && aligned16(sx) && aligned16(qw) && aligned16(sw) &&
+                    aligned16(offsets) && aligned16(y),
+                JET_ERR_ALIGN);
+    DeviceInfo dev;
+    jet_status st = current_device(&dev);
+    if (st != JET_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    if (out_empty) return JET_OK;
+    if (K == 0)  // empty contraction: the product is zero
+        return cudaMemsetAsync(y, 0, (size_t)M * N * 2, s) == cudaSuccess ? JET_OK : JET_ERR_CUDA;
+    if (N % 256 == 0)
+        return launch<256, kFwdGrouped, 1>(dev, qx, sx, qw, sw, y, M, N, K, 1, nullptr, s, offsets,
+                                           (int)E);
+    return launch<128, kFwdGrouped, 1>(dev, qx, sx, qw, sw, y, M, N, K, 1, nullptr, s, offsets,
+                                       (int)E);
 }
 
 jet_status jet_gemm_fp8_dgrad(const uint8_t *qdy, const float *sdy, const uint8_t *qw,

@@ -20,6 +20,13 @@ Ergebnisse", and the 163.com article, section 四):
   and 1x128 quantization of a 16384 x 14336 t(3) activation matrix.
 * ``metric``  - n = 4,194,304 tokens, logp_rollout = log U(1e-4, 1),
   logp_train = logp_rollout + N(0, 0.02), float32.
+* ``moe``     - the expert linears of one mixture-of-experts layer shaped like
+  Qwen3-30B-A3B (hidden 2048, 128 experts, expert FFN width 768, top-8
+  routing): 4096 tokens routed to 8 distinct experts each, drawn with
+  probabilities softmax(N(0,1)) over the experts (a skewed load with ragged,
+  sometimes empty, experts); X as ``rollout``, W ~ N(0, 0.02) per expert.
+  The FP8 MoE experiment is on the 163.com / nmedialink pages ("在专家混合
+  模型中的突破"); the layer shape is the public model configuration.
 
 "N(0, s)": s is the standard deviation.  Student-t(3) is drawn as
 Z / sqrt((Z1^2 + Z2^2 + Z3^2) / 3) with independent standard normals.
@@ -54,7 +61,11 @@ SHARED_INPUT = {"q": "attn_in", "k": "attn_in", "v": "attn_in", "o": "attn_out",
                 "gate": "mlp_in", "up": "mlp_in", "down": "mlp_act"}
 ROLLOUT_M = (1, 16, 64, 256, 2048)
 CONFIG_ID = {"single": 1, "rollout": 2, "train8b": 3, "train32b": 4, "sync": 5,
-             "metric": 5}
+             "metric": 5, "moe": 6}
+# (name, N, K) of one expert of the Qwen3-30B-A3B-shaped MoE layer; gate and
+# up of an expert are one [2 * 768, 2048] product.
+MOE_EXPERTS, MOE_TOPK, MOE_TOKENS = 128, 8, 4096
+MOE_LINEARS = (("gate_up", 1536, 2048), ("down", 2048, 768))
 
 
 def _gen(seed: int, config: int, tensor_id: int, device) -> torch.Generator:
@@ -170,6 +181,36 @@ def training_layer(kind="train8b", seed=0, device="cpu", M=None, with_grad=True)
                           device=device) if with_grad else None)
         cases.append(LinearCase(name, M, N, K, inputs[key], w, dy))
     return cases
+
+
+def moe_offsets(tokens: int, experts: int, topk: int, *, seed=0, config=6, tensor_id=500,
+                device="cpu") -> torch.Tensor:
+    """int64 [experts + 1]: first row of each expert's tokens once the
+    tokens * topk routed copies are sorted by expert.  Each token picks topk
+    distinct experts with probabilities softmax(N(0,1)) drawn once per layer."""
+    g = _gen(seed, config, tensor_id, "cpu")
+    popularity = torch.softmax(torch.randn((experts,), generator=g, dtype=torch.float64), 0)
+    pick = torch.multinomial(popularity.expand(tokens, experts), topk, replacement=False,
+                             generator=g)
+    counts = torch.bincount(pick.flatten(), minlength=experts)
+    off = torch.zeros((experts + 1,), dtype=torch.int64)
+    off[1:] = torch.cumsum(counts, 0)
+    return off.to(device)
+
+
+def moe_layer(seed=0, device="cpu", tokens=MOE_TOKENS, experts=MOE_EXPERTS, topk=MOE_TOPK,
+              linears=MOE_LINEARS):
+    """(offsets, [(name, x [M, K], w [E, N, K])]) of one MoE layer; M = tokens * topk."""
+    cfg = CONFIG_ID["moe"]
+    off = moe_offsets(tokens, experts, topk, seed=seed, config=cfg, device=device)
+    M = int(off[-1])
+    out = []
+    for i, (name, N, K) in enumerate(linears):
+        x = activations(M, K, seed=seed, config=cfg, tensor_id=i, device=device)
+        w = weights(experts * N, K, seed=seed, config=cfg, tensor_id=100 + i,
+                    device=device).view(experts, N, K)
+        out.append((name, x, w))
+    return off, out
 
 
 def bf16_bits(t: torch.Tensor):

@@ -175,6 +175,31 @@ JET_API jet_status jet_gemm_fp8_fwd(const uint8_t *qx, const float *sx,
                             size_t ws_bytes, jet_stream_t stream);
 
 /*
+ * Grouped forward GEMM of expert linears (mixture-of-experts layers), one
+ * launch for all experts:  for every expert e and its tokens
+ * m in [offsets[e], offsets[e+1]),
+ *   Y[m][n] = sum_kb sx[kb][m] * sw[e][n/128][kb] * sum_{k in kb} qx[m][k] qw[e][n][k]
+ * with the arithmetic of jet_gemm_fp8_fwd (FP32 accumulation, BF16 out).
+ * Source: 163.com article / nmedialink.com page (FP8 for the Qwen3-30B MoE
+ * model, section "在专家混合模型中的突破"); m.66260.cn FP8-RL article (expert
+ * layers in the compressed format).  The pages give no grouped kernel; this
+ * layout is this library's choice.
+ *   qx [M][K], sx [Kb][M]: the tokens of all experts, in expert order (the
+ *     jet_quant_act_1x128 form of the concatenated activations).
+ *   qw [E][N][K], sw [E][Nb][Kb]: the experts' weights and scales, stacked.
+ *   offsets [E+1] int64, DEVICE array: offsets[0] = 0, non-decreasing,
+ *     offsets[E] = M (e.g. written by the routing kernel).  Offsets outside
+ *     [0, M] are clamped and a decreasing pair is an empty expert, so no
+ *     write ever leaves y; results are then unspecified.
+ *   y [M][N] BF16 bits (out).  1 <= E <= 384; N, K multiples of 128.
+ */
+JET_API jet_status jet_gemm_fp8_fwd_grouped(const uint8_t *qx, const float *sx,
+                                            const uint8_t *qw, const float *sw,
+                                            const int64_t *offsets, int64_t E, int64_t M,
+                                            int64_t N, int64_t K, uint16_t *y,
+                                            jet_stream_t stream);
+
+/*
  * DGrad GEMM  dX = dY W :
  *   dX[m][k] = sum_nb sdy[nb][m] * sw[nb][k/128] * sum_{n in nb} qdy[m][n] qw[n][k]
  * FP32 accumulation, BF16 out.  Source: gist.science summary,

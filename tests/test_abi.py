@@ -147,6 +147,24 @@ def test_gemm_checks(lib, name):
         assert f(*args, 16, 1024, 1024, fake(A), fake(MIS), need, None) == ALIGN
 
 
+def test_grouped_gemm_checks(lib):
+    f = lib.jet_gemm_fp8_fwd_grouped
+    args = [fake(A), fake(B), fake(C), fake(D)]
+    assert f(*args, fake(A), 8, 256, 128, 128, None, None) == NULL        # no output
+    assert f(*args, None, 8, 256, 128, 128, fake(A), None) == NULL        # no offsets
+    assert f(None, fake(B), fake(C), fake(D), fake(A), 8, 256, 128, 128, fake(A), None) == NULL
+    assert f(*args, fake(A), 0, 256, 128, 128, fake(A), None) == SHAPE    # no expert
+    assert f(*args, fake(A), 385, 256, 128, 128, fake(A), None) == SHAPE  # over the limit
+    assert f(*args, fake(A), 8, -1, 128, 128, fake(A), None) == SHAPE
+    assert f(*args, fake(A), 8, 256, 100, 128, fake(A), None) == SHAPE
+    assert f(*args, fake(A), 8, 256, 128, 100, fake(A), None) == SHAPE
+    assert f(*args, fake(A), 384, 256, 1 << 22, 128, fake(A), None) == SHAPE  # E*N rows
+    assert f(*args, fake(MIS), 8, 256, 128, 128, fake(A), None) == ALIGN
+    assert f(*args, fake(A), 8, 256, 128, 128, fake(MIS), None) == ALIGN
+    # an empty output needs no pointer at all; empty experts are no error
+    assert f(None, None, None, None, None, 8, 0, 128, 128, None, None) in (OK, DEVICE)
+
+
 def test_metric_checks(lib):
     f = lib.jet_token_mult_prob_error
     assert f(None, fake(B), 16, fake(C), fake(D), 8, None) == NULL
@@ -186,6 +204,8 @@ def test_no_device_is_reported():
     need = lib.jet_workspace_bytes(binding.OP["gemm_fp8_fwd"], 16, 1024, 1024)
     assert lib.jet_gemm_fp8_fwd(fake(A), fake(B), fake(C), fake(D), 16, 1024, 1024,
                                 fake(A), fake(B), need, None) == DEVICE
+    assert lib.jet_gemm_fp8_fwd_grouped(fake(A), fake(B), fake(C), fake(D), fake(A), 4, 256,
+                                        128, 128, fake(A), None) == DEVICE
     assert lib.jet_device_status(None, None) == DEVICE
 
 

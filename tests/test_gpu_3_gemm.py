@@ -212,3 +212,114 @@ def test_train32b_kv_proj_wgrad(jet):
     M, N, K = 16384, 1024, 5120
     run_wgrad(jet, wl.grad_output(M, N, seed=0, config=4, tensor_id=201),
               wl.activations(M, K, seed=0, config=4), nrows=8)
+
+
+# ------------------------------------------ grouped forward (expert linears) --
+
+def quant_experts(x, w):
+    """Oracle quantization of the tokens and of every expert's weights."""
+    qx, sx = oracle.quant_act_1x128(bits(x))
+    E = w.shape[0]
+    pairs = [oracle.quant_w_128x128(bits(w[e])) for e in range(E)]
+    return qx, sx, np.stack([p[0] for p in pairs]), np.stack([p[1] for p in pairs])
+
+
+def run_grouped(jet, x, w, off, rows_per_expert=None, experts=None):
+    qx, sx, qw, sw = quant_experts(x, w)
+    off = np.asarray(off, np.int64)
+    y = jet.gemm_fp8_fwd_grouped(to_dev(qx), to_dev(sx), to_dev(qw), to_dev(sw),
+                                 torch.from_numpy(off).cuda())
+    torch.cuda.synchronize()
+    if rows_per_expert is None:
+        assert_gemm_close(y, oracle.gemm_fwd_grouped(qx, sx, qw, sw, off), "grouped fwd")
+        return y
+    # sampled rows of sampled experts: each expert's rows are the plain forward
+    # product of its own tokens, which the oracle computes row by row
+    for e in experts:
+        a, b = int(off[e]), int(off[e + 1])
+        if b == a:
+            continue
+        r = sample_rows(b - a, rows_per_expert, seed=e)
+        r = np.arange(b - a) if r is None else r
+        ref = oracle.gemm_fwd(np.ascontiguousarray(qx[a:b]), np.ascontiguousarray(sx[:, a:b]),
+                              qw[e], sw[e], rows=r)
+        assert_gemm_close(y[torch.as_tensor(a + r).cuda()], ref, f"grouped fwd, expert {e}")
+    return y
+
+
+@pytest.mark.parametrize("N", [256, 384])      # 256-wide and 128-wide column tiles
+def test_grouped_ragged_and_empty_experts(jet, N):
+    off = [0, 5, 5, 133, 300, 300, 301, 556, 700]   # empty, 1-row and ragged experts
+    E, K = len(off) - 1, 384
+    x = wl.activations(off[-1], K, seed=N, config=6)
+    w = wl.weights(E * N, K, seed=N, config=6).view(E, N, K)
+    run_grouped(jet, x, w, off)
+
+
+def test_grouped_single_expert_is_the_forward_product(jet):
+    x, w = wl.activations(300, 512, seed=3, config=6), wl.weights(256, 512, seed=3, config=6)
+    y = run_grouped(jet, x, w.view(1, 256, 512), [0, 300])
+    qx, sx, qw, sw = quant_pair(x, w)
+    assert_gemm_close(y, oracle.gemm_fwd(qx, sx, qw, sw), "grouped, one expert")
+
+
+def test_grouped_empty_leading_and_trailing_experts(jet):
+    off = [0, 0, 0, 129, 129, 257, 257, 257]
+    E, N, K = len(off) - 1, 256, 256
+    run_grouped(jet, wl.activations(257, K, seed=4, config=6),
+                wl.weights(E * N, K, seed=4, config=6).view(E, N, K), off)
+
+
+def test_grouped_max_experts_one_token_each(jet):
+    # 384 experts (the limit), most with one token, some with none
+    rng = np.random.default_rng(8)
+    counts = rng.integers(0, 3, 384)
+    off = np.concatenate([[0], np.cumsum(counts)])
+    E, N, K = 384, 128, 128
+    run_grouped(jet, wl.activations(int(off[-1]), K, seed=8, config=6),
+                wl.weights(E * N, K, seed=8, config=6).view(E, N, K), off)
+
+
+def test_grouped_deterministic_and_rows_independent(jet):
+    off = np.array([0, 200, 200, 650, 1000], np.int64)
+    E, N, K = 4, 512, 1024
+    x = wl.activations(1000, K, seed=10, config=6)
+    w = wl.weights(E * N, K, seed=10, config=6).view(E, N, K)
+    qx, sx, qw, sw = (to_dev(a) for a in quant_experts(x, w))
+    o = torch.from_numpy(off).cuda()
+    y1 = jet.gemm_fp8_fwd_grouped(qx, sx, qw, sw, o)
+    y2 = jet.gemm_fp8_fwd_grouped(qx, sx, qw, sw, o)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    # expert 2 alone (its own launch) gives the same bits: tiles never mix experts
+    a, b = 200, 650
+    y3 = jet.gemm_fp8_fwd_grouped(qx[a:b].contiguous(), sx[:, a:b].contiguous(), qw[2:3].contiguous(),
+                                  sw[2:3].contiguous(), torch.tensor([0, b - a], device="cuda"))
+    assert torch.equal(y1[a:b].view(torch.int16), y3.view(torch.int16))
+
+
+def test_grouped_empty_contraction_and_no_tokens(jet):
+    off = torch.tensor([0, 3, 64], dtype=torch.int64, device="cuda")
+    y = torch.full((64, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    jet.jet_gemm_fp8_fwd_grouped(torch.empty((64, 0), dtype=torch.uint8, device="cuda"),
+                                 torch.empty((0, 64), dtype=torch.float32, device="cuda"),
+                                 torch.empty((2, 256, 0), dtype=torch.uint8, device="cuda"),
+                                 torch.empty((2, 2, 0), dtype=torch.float32, device="cuda"), off, y)
+    assert (y == 0).all()
+    y0 = jet.gemm_fp8_fwd_grouped(torch.empty((0, 128), dtype=torch.uint8, device="cuda"),
+                                  torch.empty((1, 0), dtype=torch.float32, device="cuda"),
+                                  torch.zeros((2, 256, 128), dtype=torch.uint8, device="cuda"),
+                                  torch.ones((2, 2, 1), dtype=torch.float32, device="cuda"),
+                                  torch.zeros((3,), dtype=torch.int64, device="cuda"))
+    assert y0.shape == (0, 256)
+
+
+@pytest.mark.parametrize("lin", [0, 1])
+def test_grouped_moe_layer_sampled(jet, lin):
+    """The Qwen3-30B-A3B-shaped MoE layer at full size (4096 tokens, top-8 of
+    128 experts): sampled rows of sampled experts, incl. the smallest and the
+    largest expert."""
+    off, lins = wl.moe_layer()
+    name, x, w = lins[lin]
+    counts = (off[1:] - off[:-1]).numpy()
+    experts = sorted({int(counts.argmin()), int(counts.argmax()), 0, 63, 127})
+    run_grouped(jet, x, w, off.numpy(), rows_per_expert=6, experts=experts)
