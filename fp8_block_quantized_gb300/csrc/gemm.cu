@@ -72,23 +72,27 @@ static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168,
 constexpr int BM = 128;  // output rows per tile (TMEM lanes)
 constexpr int BK = 128;  // contraction slice = one scale block
 
-template <int BN, int CL>
+template <int BN, int CL, bool STAGED>
 struct Cfg {
     // Per CTA and stage: A's 128 rows and B's BN (CL = 1) or BN/2 (pair) rows.
     static constexpr int kBRows = BN / CL;
     static constexpr int kABytes = BM * BK;
     static constexpr int kBBytes = kBRows * BK;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = 4;
     // Scale ring: per slice, the tile's 128 row scales and its column scales
     // (BN per-column values for wgrad, BN/128 block values otherwise).
     static constexpr int kScaleSlots = 8;
     static constexpr int kScaleRowBytes = BM * 4;
     static constexpr int kScaleSlotBytes = kScaleRowBytes + BN * 4;
-    // Output staging (pair kernel): each promotion warp's 32 x 128 BF16 block,
-    // 128-byte swizzled, written out by TMA stores.
+    // Output staging (STAGED: the pair kernel and the grouped forward): each
+    // promotion warp's 32 x 128 BF16 block, 128-byte swizzled, written out by
+    // TMA stores, so that the promotion warps go back to the accumulators
+    // while the stores drain.
     static constexpr int kOutWarpBytes = 32 * 128 * 2;
-    static constexpr int kOutBytes = CL == 2 ? 8 * kOutWarpBytes : 0;
+    static constexpr int kOutBytes = STAGED ? 8 * kOutWarpBytes : 0;
+    // four operand stages where they fit beside the staging, else three
+    static constexpr int kStages =
+        4 * kStageBytes + kOutBytes + kScaleSlots * kScaleSlotBytes + 1024 <= 227 * 1024 ? 4 : 3;
     static constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes +
                                       kScaleSlots * kScaleSlotBytes + 1024;  // + alignment slack
     static constexpr int kTmemCols = 2 * BN;                           // two accumulators
@@ -190,7 +194,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 uint16_t *__restrict__ out, int R, int C, int D, Raster raster, int splits,
                 float *__restrict__ partial, const int64_t *__restrict__ goff, int gE,
                 unsigned *status) {
-    using CF = Cfg<BN, CL>;
+    using CF = Cfg<BN, CL, CL == 2 || MODE == kFwdGrouped>;
     constexpr int S = CF::kStages;
     constexpr int SS = CF::kScaleSlots;
     constexpr bool kPair = CL == 2;
@@ -573,10 +577,12 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
             }
             if (!ok) break;
-            if (kPair) {
-                // Stage this warp's 32 rows x 128 columns (two 64-column boxes,
+            if (kPair || (kGrp && m0 + quad * 32 + 31 < rlim)) {
+                // Stage this warp's 32 rows x H columns (64-column boxes,
                 // 128-byte swizzle: 16-byte chunk j of row r goes to j ^ (r % 8))
-                // and hand them to the TMA; rows past R are clipped by it.
+                // and hand them to the TMA; rows past R are clipped by it.  (A
+                // grouped tile's warp whose rows cross its expert's end takes
+                // the plain stores below instead.)
                 const uint32_t wbuf = out_base + ew * CF::kOutWarpBytes;
                 if (lane == 0) bulk_wait_group_read0();  // previous tile's stores have read it
                 __syncwarp();
@@ -596,8 +602,10 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d_hint(&tmY, wbuf, col0, m0 + quad * 32, pol_out);
-                    tma_store_2d_hint(&tmY, wbuf + 4096, col0 + 64, m0 + quad * 32, pol_out);
+#pragma unroll
+                    for (int h = 0; h < H / 64; ++h)
+                        tma_store_2d_hint(&tmY, wbuf + 4096 * h, col0 + 64 * h, m0 + quad * 32,
+                                          pol_out);
                     bulk_commit_group();
                 }
             } else if (splits > 1) {
@@ -627,7 +635,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 
     // Outstanding TMA stores must finish reading shared memory before exit.
-    if (kPair && warp >= 4 && (threadIdx.x & 31) == 0) bulk_wait_group0();
+    if ((kPair || kGrp) && warp >= 4 && (threadIdx.x & 31) == 0) bulk_wait_group0();
     tc_fence_before();
     // Neither CTA of a pair may exit or free TMEM while the other can still
     // use its barriers, shared memory or the pair's TMEM allocation.
@@ -747,7 +755,7 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
                   const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D, int splits,
                   float *partial, cudaStream_t stream, const int64_t *goff = nullptr,
                   int gE = 0) {
-    using CF = Cfg<BN, CL>;
+    using CF = Cfg<BN, CL, CL == 2 || MODE == kFwdGrouped>;
     auto kernel = gemm_fp8_kernel<BN, MODE, CL>;
     static std::mutex mu;
     static int max_units[64] = {};  // co-resident CTAs (CL = 1) or clusters (CL = 2)
@@ -788,8 +796,9 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     }
     CUtensorMap ta, tb, ty;
     if (!make_map_u8(&ta, a, (uint64_t)D, (uint64_t)R, BK, BM)) return JET_ERR_CUDA;
-    if (CL == 2 && !make_map_out(&ty, out, (uint64_t)C, (uint64_t)R)) return JET_ERR_CUDA;
-    if (CL == 1) ty = ta;  // unused by the single-CTA kernel
+    constexpr bool kStagedOut = CL == 2 || MODE == kFwdGrouped;
+    if (kStagedOut && !make_map_out(&ty, out, (uint64_t)C, (uint64_t)R)) return JET_ERR_CUDA;
+    if (!kStagedOut) ty = ta;  // unused: this kernel stores from registers
     // grouped forward: B is the experts' weights stacked, [gE * C][D]
     const uint64_t b_rows = MODE == kFwdGrouped ? (uint64_t)gE * (uint64_t)C : (uint64_t)C;
     bool okb = MODE == kDgrad ? make_map_u8(&tb, b, (uint64_t)C, (uint64_t)D, 128, BK)
