@@ -82,6 +82,11 @@ def _load():
         lib.jo_quant_act_1x128.argtypes = [P, I, I, P, P, I, I]
         lib.jo_quant_w_128x128.argtypes = [P, I, I, P, P, I, I]
         lib.jo_requant_128x1.argtypes = [P, P, I, I, P, P, I, I]
+        lib.jo_exp_f32.argtypes = [ctypes.c_float]
+        lib.jo_exp_f32.restype = ctypes.c_float
+        lib.jo_silu_f32.argtypes = [ctypes.c_float]
+        lib.jo_silu_f32.restype = ctypes.c_float
+        lib.jo_swiglu_quant_1x128.argtypes = [P, P, I, I, I, P, P, I, I]
         for f in (lib.jo_gemm_fwd, lib.jo_gemm_dgrad, lib.jo_gemm_wgrad):
             f.argtypes = [P, P, P, P, I, I, I, P, I, I, P]
             f.restype = None
@@ -173,6 +178,39 @@ def quant_act_1x128(x_bits, nthreads=None):
     s = np.empty((K // 128, M), np.float32)
     _run(lambda a, b: lib.jo_quant_act_1x128(_ptr(x), M, K, _ptr(q), _ptr(s), a, b),
          M, nthreads)
+    return q, s
+
+
+def exp_f32(x):
+    """The binary32 e^x of the fused SwiGLU quantizer (x in [-104, 80]), elementwise.
+    Pinned against binary64 exp (within 1 ulp where the result is normal)."""
+    lib = _load()
+    return np.array([lib.jo_exp_f32(float(v)) for v in np.asarray(x, np.float32).ravel()],
+                    np.float32).reshape(np.shape(x))
+
+
+def silu_f32(g):
+    """The binary32 silu(g) = g / (1 + e^-g) of the fused SwiGLU quantizer, elementwise."""
+    lib = _load()
+    return np.array([lib.jo_silu_f32(float(v)) for v in np.asarray(g, np.float32).ravel()],
+                    np.float32).reshape(np.shape(g))
+
+
+def swiglu_quant_1x128(gate_bits, up_bits, nthreads=None):
+    """h = silu(gate) * up in binary32, then 1x128 groups of h ->
+    (q uint8 [M,F], s float32 [F/128, M]).  gate, up: BF16 bits [M,F]."""
+    lib = _load()
+    g = _as_bf16_bits(gate_bits)
+    u = _as_bf16_bits(up_bits)
+    if g.shape != u.shape:
+        raise ValueError("gate and up must have the same shape")
+    M, F = g.shape
+    if F % 128:
+        raise ValueError("F must be a multiple of 128")
+    q = np.empty((M, F), np.uint8)
+    s = np.empty((F // 128, M), np.float32)
+    _run(lambda a, b: lib.jo_swiglu_quant_1x128(_ptr(g), _ptr(u), F, M, F, _ptr(q), _ptr(s),
+                                                a, b), M, nthreads)
     return q, s
 
 

@@ -220,6 +220,100 @@ void jo_requant_128x1(const uint8_t *q, const float *s, int64_t M, int64_t K,
 }
 
 /* ------------------------------------------------------------------------ */
+/* SwiGLU with the 1x128 quantization of its output fused                   */
+/* ------------------------------------------------------------------------ */
+/* The pages fuse the quantization into the operator that produces a linear
+ * layer's input, so that the saved activation is FP8 straight away ("英伟达
+ * 破解AI训练效率难题" (163.com), section 三; "Jet-RL ..." (gist.science),
+ * "Quantisierungsschema").  For the MLP's down projection that operator is
+ * SwiGLU, h = silu(gate) * up.  The pages give no arithmetic for it; the
+ * reading here is a fully specified binary32 evaluation (below), after which
+ * the 128-wide groups of h are quantized exactly as activations are, from
+ * the binary32 values (no BF16 rounding of h in between). */
+
+/* e^x in binary32 for x in [-104, 80], by Cody-Waite argument reduction
+ * x = n ln2 + r (ln 2 split into a 16-bit head and a rounded tail, both
+ * products taken with fused multiply-adds), |r| <= ln2 / 2, the Taylor
+ * polynomial of e^r to degree 7 in Horner form (coefficients RN(1/k!)),
+ * and the scaling by 2^n as two exact powers of two, 2^(n/2) and
+ * 2^(n - n/2) (C division, truncating), so that the only rounding of the
+ * scaling is the final product's. */
+static float pow2i(int k) /* 2^k for -126 <= k <= 127 */
+{
+    uint32_t u = (uint32_t)(k + 127) << 23;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+float jo_exp_f32(float x)
+{
+    const float log2e = 0x1.715476p+0f;
+    const float ln2_hi = 0x1.62e4p-1f;
+    const float ln2_lo = 0x1.7f7d1cp-20f;
+    float n = rintf(x * log2e);
+    float r = fmaf(n, -ln2_hi, x);
+    r = fmaf(n, -ln2_lo, r);
+    float p = 0x1.a01a02p-13f;          /* 1/7! */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);    /* 1/6! */
+    p = fmaf(p, r, 0x1.111112p-7f);     /* 1/5! */
+    p = fmaf(p, r, 0x1.555556p-5f);     /* 1/4! */
+    p = fmaf(p, r, 0x1.555556p-3f);     /* 1/3! */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    int ni = (int)n;
+    int n1 = ni / 2;
+    p = p * pow2i(n1);
+    p = p * pow2i(ni - n1);
+    return p;
+}
+
+/* silu(g) = g / (1 + e^-g) in binary32.  For g < -80 the true value is
+ * below 1.5e-33 in magnitude and is taken as g * 0 (a signed zero).
+ * Otherwise the exponent -g is clamped below at -104 (where e^-g no longer
+ * changes 1 + e^-g), d = 1 + e^-g, and 1/d is taken from the bit-pattern
+ * seed 0x7EF311C7 - bits(d) refined by three Newton-Raphson steps
+ * y <- y + y (1 - d y) (fused multiply-adds); silu = g * (1/d). */
+float jo_silu_f32(float g)
+{
+    if (g < -80.0f)
+        return g * 0.0f;
+    float x = -g;
+    if (x < -104.0f)
+        x = -104.0f;
+    float d = 1.0f + jo_exp_f32(x);
+    uint32_t b;
+    memcpy(&b, &d, sizeof b);
+    b = 0x7EF311C7u - b;
+    float y;
+    memcpy(&y, &b, sizeof y);
+    for (int i = 0; i < 3; ++i)
+        y = fmaf(fmaf(-d, y, 1.0f), y, y);
+    return g * y;
+}
+
+/* h[m][f] = fl32(silu(gate[m][f]) * up[m][f]) for gate, up BF16 with rows
+ * ld elements apart (gate[m][f] = g[m * ld + f], up likewise from u), then
+ * 1x128 groups of h along f: q[M][F] codes, s[fb * M + m] scales.  Rows
+ * [m0, m1) only. */
+void jo_swiglu_quant_1x128(const uint16_t *g, const uint16_t *u, int64_t ld,
+                           int64_t M, int64_t F, uint8_t *q, float *s,
+                           int64_t m0, int64_t m1)
+{
+    float h[128];
+    int64_t Fb = F / 128;
+    for (int64_t m = m0; m < m1; ++m)
+        for (int64_t fb = 0; fb < Fb; ++fb) {
+            for (int i = 0; i < 128; ++i) {
+                int64_t at = m * ld + fb * 128 + i;
+                h[i] = jo_silu_f32(bf16_to_f32(g[at])) * bf16_to_f32(u[at]);
+            }
+            s[fb * M + m] = quant_group(h, 1, 128, q + m * F + fb * 128, 1);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
 /* GEMMs: binary64 product of the dequantized operands                       */
 /* ------------------------------------------------------------------------ */
 
