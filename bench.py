@@ -54,6 +54,7 @@ BYTES_PER_ELEM = {
     "quant_dual_1x128_128x1": 2 + 1 + 1 + 4 / 128 + 4 / 128,
     "token_mult_prob_error": 8,                  # two FP32 per token
     "token_mismatch_masked": 4 + 4 + 1 + 4,      # two FP32 and the mask in, the weight out
+    "swiglu_quant_1x128": 2 + 2 + 1 + 4 / 128,   # gate and up BF16 in, code + scale out
 }
 
 
@@ -363,10 +364,10 @@ class MoeStep:
     """Forward of the expert linears of one Qwen3-30B-A3B-shaped MoE layer
     (4096 tokens, top-8 of 128 experts, 32768 routed rows): 1x128
     quantization of the routed gate_up input, the grouped gate_up product
-    (N = 1536, K = 2048 per expert), 1x128 quantization of the routed down
-    input, the grouped down product (N = 2048, K = 768).  The routing (row
-    offsets per expert) and the experts' FP8 weights are prepared beforehand
-    and not timed."""
+    (N = 1536, K = 2048 per expert), SwiGLU of its two halves fused with the
+    1x128 quantization of the result, the grouped down product (N = 2048,
+    K = 768).  The routing (row offsets per expert) and the experts' FP8
+    weights are prepared beforehand and not timed."""
 
     def __init__(self, device, seed: int = 0):
         import torch
@@ -381,6 +382,7 @@ class MoeStep:
         self.lin = []
         flops = nbytes = 0
         counts = (off[1:] - off[:-1]).cpu()
+        used = int((counts > 0).sum())
         for name, x, w in lins:
             E, N, K = w.shape
             qw = e((E, N, K), torch.uint8)
@@ -391,14 +393,17 @@ class MoeStep:
                              "q": e((M, K), torch.uint8), "s": e((K // 128, M), torch.float32),
                              "y": e((M, N), torch.bfloat16)})
             flops += 2 * M * N * K
-            used = int((counts > 0).sum())
             nbytes += M * K + 4 * M * K // 128 + used * (N * K + 4 * N * K // 16384) + 2 * M * N
+        gu, dn = self.lin
+        assert gu["N"] == 2 * dn["K"]
+        self.F = F = dn["K"]
+        self.lin[1]["x"] = None   # the down input is the SwiGLU of the gate_up output
         torch.cuda.synchronize()
         self.flops = flops
         self.work = {"gemm_fp8_fwd_grouped": flops, "gemm_fp8_fwd_grouped_bytes": nbytes,
-                     "quant_act_1x128": sum(M * L["K"] for L in self.lin)
-                     * BYTES_PER_ELEM["quant_act_1x128"]}
-        self.launches_per_step = 2 * len(self.lin)
+                     "quant_act_1x128": M * gu["K"] * BYTES_PER_ELEM["quant_act_1x128"],
+                     "swiglu_quant_1x128": M * F * BYTES_PER_ELEM["swiglu_quant_1x128"]}
+        self.launches_per_step = 4
         self.primary = ("TFLOP/s", flops)
         tiles = int(((counts + 127) // 128).sum())
         self.config = {"workload": f"moe_qwen3_30b_a3b_T{wl.MOE_TOKENS}",
@@ -410,20 +415,24 @@ class MoeStep:
                        "l2": "no flush: per-step working set (~0.9 GB) > 129 MB L2"}
 
     def calls(self):
-        j, out = self.jet, []
-        for L in self.lin:
-            out.append(("quant_act_1x128", lambda L=L: j.jet_quant_act_1x128(L["x"], L["q"], L["s"]),
-                        "x_" + L["name"]))
-            out.append(("gemm_fp8_fwd_grouped", lambda L=L: j.jet_gemm_fp8_fwd_grouped(
-                L["q"], L["s"], L["qw"], L["sw"], self.off, L["y"]), L["name"]))
-        return out
+        j = self.jet
+        gu, dn, F = self.lin[0], self.lin[1], self.F
+        return [
+            ("quant_act_1x128", lambda: j.jet_quant_act_1x128(gu["x"], gu["q"], gu["s"]), "x_gate_up"),
+            ("gemm_fp8_fwd_grouped", lambda: j.jet_gemm_fp8_fwd_grouped(
+                gu["q"], gu["s"], gu["qw"], gu["sw"], self.off, gu["y"]), "gate_up"),
+            ("swiglu_quant_1x128", lambda: j.jet_swiglu_quant_1x128(
+                gu["y"][:, :F], gu["y"][:, F:], dn["q"], dn["s"]), "h"),
+            ("gemm_fp8_fwd_grouped", lambda: j.jet_gemm_fp8_fwd_grouped(
+                dn["q"], dn["s"], dn["qw"], dn["sw"], self.off, dn["y"]), "down"),
+        ]
 
     def host_io(self):
         import torch
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-        self.h_in = [(pin(L["x"]), L["x"]) for L in self.lin] + [(pin(self.off), self.off)]
-        self.h_out = [(torch.empty(L["y"].shape, dtype=L["y"].dtype, pin_memory=True), L["y"])
-                      for L in self.lin]
+        gu, dn = self.lin
+        self.h_in = [(pin(gu["x"]), gu["x"]), (pin(self.off), self.off)]
+        self.h_out = [(torch.empty(dn["y"].shape, dtype=dn["y"].dtype, pin_memory=True), dn["y"])]
         nbytes = lambda pairs: sum(h.numel() * h.element_size() for h, _ in pairs)
         return nbytes(self.h_in), nbytes(self.h_out)
 

@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     jet_quant_dual_1x128_128x1,
     jet_quant_w_128x128,
     jet_requant_128x1,
+    jet_swiglu_quant_1x128,
     jet_token_mismatch_masked,
     jet_token_mult_prob_error,
     load,
@@ -28,6 +29,7 @@ from .binding import (  # noqa: F401
     requant_128x1,
     selftest_bounded_wait,
     selftest_quotient,
+    swiglu_quant_1x128,
     token_mismatch_masked,
     token_mult_prob_error,
     workspace_bytes,

@@ -22,7 +22,8 @@ STATUS = {0: "JET_OK", 1: "JET_ERR_NULL", 2: "JET_ERR_SHAPE", 3: "JET_ERR_ALIGN"
           7: "JET_ERR_TIMEOUT"}
 OP = {"quant_act_1x128": 0, "quant_w_128x128": 1, "requant_128x1": 2,
       "gemm_fp8_fwd": 3, "gemm_fp8_dgrad": 4, "gemm_fp8_wgrad": 5,
-      "token_mult_prob_error": 6, "quant_dual_1x128_128x1": 7, "token_mismatch_masked": 8}
+      "token_mult_prob_error": 6, "quant_dual_1x128_128x1": 7, "token_mismatch_masked": 8,
+      "swiglu_quant_1x128": 9}
 
 # name -> argtypes (restype is int status unless listed in _RESTYPE)
 P, I, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
@@ -33,6 +34,7 @@ SIGNATURES = {
     "jet_quant_w_128x128": [P, I, I, P, P, P],
     "jet_requant_128x1": [P, P, I, I, P, P, P],
     "jet_quant_dual_1x128_128x1": [P, I, I, P, P, P, P, P],
+    "jet_swiglu_quant_1x128": [P, P, I, I, I, P, P, P],
     "jet_gemm_fp8_fwd": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_gemm_fp8_fwd_grouped": [P, P, P, P, P, I, I, I, I, P, P],
     "jet_gemm_fp8_dgrad": [P, P, P, P, I, I, I, P, P, Z, P],
@@ -181,6 +183,25 @@ def jet_quant_dual_1x128_128x1(x, q, s, qT, sT, stream=None):
         _ptr(x), M, K, _ptr(q), _ptr(s), _ptr(qT), _ptr(sT), _stream(stream)))
 
 
+def jet_swiglu_quant_1x128(gate, up, q, s, stream=None):
+    """gate, up: [M, F] BF16 views whose rows may be strided (e.g. the two
+    halves of a [M, 2F] gate_up product); both must share the row stride."""
+    import torch
+    M, F = gate.shape
+    for t, name in ((gate, "gate"), (up, "up")):
+        if t.dtype != torch.bfloat16 or tuple(t.shape) != (M, F):
+            raise ValueError(f"{name}: expected bfloat16 [{M}, {F}]")
+        if t.numel() and (not t.is_cuda or t.stride(1) != 1):
+            raise ValueError(f"{name}: must be a CUDA tensor with contiguous rows")
+    ld = gate.stride(0) if M > 1 else F
+    if M > 1 and up.stride(0) != ld:
+        raise ValueError("gate and up must have the same row stride")
+    _need(q, torch.uint8, (M, F), "q")
+    _need(s, torch.float32, (F // 128, M), "s")
+    _check("jet_swiglu_quant_1x128", load().jet_swiglu_quant_1x128(
+        _ptr(gate), _ptr(up), ld, M, F, _ptr(q), _ptr(s), _stream(stream)))
+
+
 def _gemm(name, a, sa, b, sb, M, N, K, out, ws, stream):
     if ws is None:  # the split-contraction partials of small-M products
         ws = _ws(name[4:], M, N, K, out.device)
@@ -323,6 +344,16 @@ def quant_dual_1x128_128x1(x, stream=None):
     sT = torch.empty((M // 128, K), dtype=torch.float32, device=x.device)
     jet_quant_dual_1x128_128x1(x, q, s, qT, sT, stream)
     return q, s, qT, sT
+
+
+def swiglu_quant_1x128(gate, up, stream=None):
+    """(q, s): the 1x128 form of silu(gate) * up."""
+    import torch
+    M, F = gate.shape
+    q = torch.empty((M, F), dtype=torch.uint8, device=gate.device)
+    s = torch.empty((F // 128, M), dtype=torch.float32, device=gate.device)
+    jet_swiglu_quant_1x128(gate, up, q, s, stream)
+    return q, s
 
 
 def _ws(op, M, N, K, device):

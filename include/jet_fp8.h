@@ -76,7 +76,8 @@ typedef enum {
     JET_OP_GEMM_WGRAD = 5,
     JET_OP_TOKEN_MULT_PROB_ERROR = 6,
     JET_OP_QUANT_DUAL_1X128_128X1 = 7,
-    JET_OP_TOKEN_MISMATCH_MASKED = 8
+    JET_OP_TOKEN_MISMATCH_MASKED = 8,
+    JET_OP_SWIGLU_QUANT_1X128 = 9
 } jet_op;
 
 /* A cudaStream_t handle passed as an opaque pointer. */
@@ -128,6 +129,27 @@ JET_API jet_status jet_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K,
 JET_API jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M,
                              int64_t K, uint8_t *qT, float *sT,
                              jet_stream_t stream);
+
+/*
+ * SwiGLU with the 1x128 quantization of its output fused: the input of an
+ * MLP's down projection, h = silu(gate) * up, written directly as the
+ * jet_quant_act_1x128 form (no BF16 copy of h).  Source: 163.com article,
+ * section 三, and gist.science summary, "Quantisierungsschema" (the quantizer
+ * fused into the operator that produces a linear layer's input).  h is
+ * evaluated in binary32 by a fixed sequence of IEEE operations (Cody-Waite
+ * e^x with a degree-7 Taylor polynomial; 1/(1 + e^-g) by a bit-pattern seed
+ * and three Newton-Raphson steps; g < -80 gives a signed zero), within 3 ulps
+ * of silu(g) * up; its 128-wide groups then follow the 1x128 group rule.
+ *   gate, up  BF16 bits, row m at gate + m*ld and up + m*ld (in).  For the
+ *       concatenated [M][2F] output of a gate_up product pass gate = base,
+ *       up = base + F, ld = 2F.  ld >= F, a multiple of 8.
+ *   q   [M][F] E4M3 codes, s [F/128][M] FP32 scales (out).  M, F >= 0, F a
+ *       multiple of 128.  Non-finite h (overflowing products) is a
+ *       precondition violation with unspecified codes.
+ */
+JET_API jet_status jet_swiglu_quant_1x128(const uint16_t *gate, const uint16_t *up, int64_t ld,
+                                          int64_t M, int64_t F, uint8_t *q, float *s,
+                                          jet_stream_t stream);
 
 /*
  * Both quantizations of one tensor from a single read: the 1x128 form of

@@ -147,6 +147,19 @@ def test_gemm_checks(lib, name):
         assert f(*args, 16, 1024, 1024, fake(A), fake(MIS), need, None) == ALIGN
 
 
+def test_swiglu_quant_checks(lib):
+    f = lib.jet_swiglu_quant_1x128
+    assert f(None, fake(B), 256, 4, 256, fake(C), fake(D), None) == NULL
+    assert f(fake(A), fake(B), 256, 4, 256, fake(C), None, None) == NULL
+    assert f(fake(A), fake(B), 256, -1, 256, fake(C), fake(D), None) == SHAPE
+    assert f(fake(A), fake(B), 256, 4, 200, fake(C), fake(D), None) == SHAPE   # F % 128
+    assert f(fake(A), fake(B), 128, 4, 256, fake(C), fake(D), None) == SHAPE   # ld < F
+    assert f(fake(A), fake(B), 260, 4, 256, fake(C), fake(D), None) == ALIGN   # rows not 16 B apart
+    assert f(fake(MIS), fake(B), 256, 4, 256, fake(C), fake(D), None) == ALIGN
+    assert f(fake(A), fake(MIS), 512, 4, 256, fake(C), fake(D), None) == ALIGN
+    assert lib.jet_workspace_bytes(binding.OP["swiglu_quant_1x128"], 4, 0, 256) == 0
+
+
 def test_grouped_gemm_checks(lib):
     f = lib.jet_gemm_fp8_fwd_grouped
     args = [fake(A), fake(B), fake(C), fake(D)]
@@ -206,6 +219,8 @@ def test_no_device_is_reported():
                                 fake(A), fake(B), need, None) == DEVICE
     assert lib.jet_gemm_fp8_fwd_grouped(fake(A), fake(B), fake(C), fake(D), fake(A), 4, 256,
                                         128, 128, fake(A), None) == DEVICE
+    assert lib.jet_swiglu_quant_1x128(fake(A), fake(B), 512, 4, 256, fake(C), fake(D),
+                                      None) == DEVICE
     assert lib.jet_device_status(None, None) == DEVICE
 
 

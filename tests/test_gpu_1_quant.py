@@ -257,3 +257,85 @@ def test_act_near_division_fast_path_threshold(jet):
     amax_target = np.float32(448.0 * 2.0 ** -90) * np.exp2(rng.uniform(-3, 3, (M, 1))).astype(np.float32)
     x = x / np.abs(x).max(axis=1, keepdims=True) * amax_target
     check_act(jet, torch.from_numpy(x).to(torch.bfloat16))
+
+
+# ------------------------------------------------ SwiGLU + 1x128, fused --
+
+def check_swiglu(jet, g_cpu, u_cpu, fused=False, rows=None):
+    """The fused SwiGLU quantizer against the oracle's binary32 SwiGLU and
+    1x128 group rule; `fused` passes gate and up as the two halves of one
+    [M, 2F] tensor (the layout of a gate_up product)."""
+    M, F = g_cpu.shape
+    if fused:
+        gu = torch.cat([g_cpu, u_cpu], dim=1).cuda()
+        q, s = jet.swiglu_quant_1x128(gu[:, :F], gu[:, F:])
+    else:
+        q, s = jet.swiglu_quant_1x128(g_cpu.cuda(), u_cpu.cuda())
+    torch.cuda.synchronize()
+    gb, ub = bits(g_cpu), bits(u_cpu)
+    if rows is None:
+        q_ref, s_ref = oracle.swiglu_quant_1x128(gb, ub)
+        assert_codes_equal(q, q_ref, "swiglu codes")
+        assert_scales_equal(s, s_ref, "swiglu scales")
+    else:
+        q_ref, s_ref = oracle.swiglu_quant_1x128(gb[rows], ub[rows])
+        r = torch.as_tensor(rows).cuda()
+        assert_codes_equal(q[r], q_ref, "swiglu codes")
+        assert_scales_equal(s[:, r], s_ref, "swiglu scales")
+
+
+@pytest.mark.parametrize("M,F", [(1, 128), (37, 384), (256, 768), (300, 1536), (130, 14336)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_swiglu_shapes(jet, M, F, fused):
+    g = wl.activations(M, F, seed=M + F, config=6, tensor_id=30)
+    u = wl.activations(M, F, seed=M + F, config=6, tensor_id=31)
+    check_swiglu(jet, g * 3, u, fused=fused)
+
+
+def test_swiglu_edge_values(jet):
+    M, F = 64, 384
+    gen = torch.Generator().manual_seed(11)
+    g = torch.randn((M, F), generator=gen) * 4
+    u = torch.randn((M, F), generator=gen)
+    g[0] = -100.0                                  # silu -> signed zero
+    g[1, :128] = torch.linspace(-90, -70, 128)     # across the -80 cut
+    g[2] = 0.0
+    g[3] = -0.0
+    u[4] = 0.0                                     # all-zero groups: scale 1
+    g[5] = 1e4                                     # silu(g) = g
+    u[5] = torch.linspace(-3, 3, F)
+    g[6, :] = torch.linspace(-104.5, 104.5, F)     # both clamps of the exponent
+    g[7] = 1e-38                                   # subnormal products
+    u[7] = 1e-3
+    g[8, ::2] = 30.0
+    u[8, ::2] = 14.9                               # exact products, ties in E4M3
+    check_swiglu(jet, g.to(torch.bfloat16), u.to(torch.bfloat16))
+    check_swiglu(jet, g.to(torch.bfloat16), u.to(torch.bfloat16), fused=True)
+
+
+def test_swiglu_every_bf16_gate(jet):
+    """Every finite BF16 gate value (65,280 of them) through the binary32
+    sequence, with up = 1 and up = -1.5; the gates sorted in 128-groups so
+    that most groups span a narrow range and small values set their scale."""
+    b = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16)
+    v = b.view(torch.bfloat16).float()
+    v = v[torch.isfinite(v)]
+    v = v[torch.argsort(v)]
+    n = (v.numel() // 128) * 128
+    g = v[:n].view(-1, 128).to(torch.bfloat16)
+    for up in (1.0, -0.75):
+        check_swiglu(jet, g, torch.full_like(g, up))
+
+
+def test_swiglu_moe_sized_sampled(jet):
+    g = wl.activations(32768, 768, seed=0, config=6, tensor_id=32)
+    u = wl.activations(32768, 768, seed=0, config=6, tensor_id=33)
+    rows = np.sort(np.random.default_rng(1).choice(32768, 2048, replace=False))
+    rows[-1] = 32767
+    check_swiglu(jet, g, u, fused=True, rows=rows)
+
+
+def test_swiglu_empty(jet):
+    e = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    q, s = jet.swiglu_quant_1x128(e, e)
+    assert q.shape == (0, 256) and s.shape == (2, 0)
