@@ -802,9 +802,19 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def source_hash(files) -> str:
+    """sha256 (first 16 hex digits) over the given csrc files, in order."""
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(ROOT, "fp8_block_quantized_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def measured_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it matches the
-    current kernel source; otherwise null."""
+    current kernel sources (the kernel's file and the headers it includes);
+    otherwise null."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -814,12 +824,10 @@ def measured_traffic(kernel: str, workload: str):
         ent = d.get(workload, {}).get(kernel)
         if not ent:
             return None
-        src = os.path.join(ROOT, "fp8_block_quantized_gb300", "csrc", ent["source"])
-        with open(src, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest()[:16] != ent["source_sha256_16"]:
-                return None
+        if source_hash(ent["sources"]) != ent["sources_sha256_16"]:
+            return None
         return ent["dram_bytes_per_launch"]
-    except (OSError, KeyError, ValueError):
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 
