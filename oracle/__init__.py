@@ -303,6 +303,58 @@ def gemm_fwd_grouped(qx, sx, qw, sw, offsets, nthreads=None):
     return out
 
 
+def gemm_dgrad_grouped(qdy, sdy, qw, sw, offsets, nthreads=None):
+    """Grouped DGrad of expert linears: for every expert e,
+    dX[o_e:o_{e+1}] = dq(dY[o_e:o_{e+1}]) . dq(W_e) in binary64.
+
+    dY [Mtot,N] holds the output gradients of all experts' tokens in expert
+    order (sdy [N/128, Mtot]); W [E,N,K] (sw [E,N/128,K/128]); offsets as in
+    gemm_fwd_grouped.  Each expert's rows are the plain DGrad product of its
+    own rows and weights."""
+    qw = np.asarray(qw)
+    sw = np.asarray(sw)
+    E, N, K = qw.shape
+    off = np.asarray(offsets, np.int64)
+    assert off.shape == (E + 1,) and off[0] == 0 and (np.diff(off) >= 0).all()
+    assert np.shape(qdy) == (off[-1], N) and np.shape(sdy) == (N // 128, off[-1])
+    assert sw.shape == (E, N // 128, K // 128)
+    out = np.zeros((int(off[-1]), K), np.float64)
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            out[a:b] = gemm_dgrad(np.ascontiguousarray(qdy[a:b]),
+                                  np.ascontiguousarray(sdy[:, a:b]), qw[e], sw[e],
+                                  nthreads=nthreads)
+    return out
+
+
+def gemm_wgrad_grouped(qdyT, sdyT, qxT, sxT, offsets, nthreads=None):
+    """Grouped WGrad of expert linears: for every expert e, the contraction
+    over its own tokens, dW_e = dq(dYT[:, o_e:o_{e+1}]) . dq(XT[:, o_e:o_{e+1}])^T
+    in binary64, from the 128x1 (transposed) forms of the expert-ordered
+    tensors: dYT [N,Mtot] (sdyT [Mtot/128, N]), XT [K,Mtot] (sxT [Mtot/128, K]).
+    The 128-token groups of those forms may not straddle two experts, so every
+    offset is a multiple of 128 (experts padded to whole token blocks).
+    Returns float64 [E, N, K]; an expert without tokens gets zeros."""
+    off = np.asarray(offsets, np.int64)
+    E = off.size - 1
+    N, Mt = np.shape(qdyT)
+    K = np.shape(qxT)[0]
+    if off[0] != 0 or off[-1] != Mt or (np.diff(off) < 0).any() or (off % 128).any():
+        raise ValueError("offsets must run from 0 to Mtot, non-decreasing, in multiples of 128")
+    assert np.shape(qxT) == (K, Mt) and np.shape(sdyT) == (Mt // 128, N)
+    assert np.shape(sxT) == (Mt // 128, K)
+    out = np.zeros((E, N, K), np.float64)
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            out[e] = gemm_wgrad(np.ascontiguousarray(qdyT[:, a:b]),
+                                np.ascontiguousarray(sdyT[a // 128:b // 128]),
+                                np.ascontiguousarray(qxT[:, a:b]),
+                                np.ascontiguousarray(sxT[a // 128:b // 128]), nthreads=nthreads)
+    return out
+
+
 def gemm_dgrad(qdy, sdy, qw, sw, rows=None, nthreads=None):
     """dX = dq(dY) . dq(W) in binary64; dY [M,N] (sdy [N/128,M]), W [N,K]."""
     M, N = np.shape(qdy)

@@ -7,6 +7,7 @@ so Y = dq(X) * 448 exactly), and the transposition relations between the
 forward, dgrad and wgrad definitions.
 """
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -138,3 +139,49 @@ def test_grouped_forward_is_per_expert_forward():
     assert not np.allclose(y2[:off[1]], y[:off[1]])
     one = oracle.gemm_fwd_grouped(qx[:3], sx[:, :3].copy(), qw[:1], sw[:1], np.array([0, 3]))
     assert np.array_equal(one, oracle.gemm_fwd(qx[:3], sx[:, :3].copy(), qw[0], sw[0]))
+
+
+def test_grouped_dgrad_is_per_expert_dgrad():
+    rng = np.random.default_rng(6)
+    E, N, K = 3, 256, 384
+    off = np.array([0, 129, 129, 200])
+    Mt = int(off[-1])
+    qdy = rand_q(rng, (Mt, N))
+    sdy = rng.uniform(0.01, 1, (N // 128, Mt)).astype(np.float32)
+    qw = rand_q(rng, (E, N, K))
+    sw = rng.uniform(0.01, 1, (E, N // 128, K // 128)).astype(np.float32)
+    dx = oracle.gemm_dgrad_grouped(qdy, sdy, qw, sw, off)
+    assert dx.shape == (Mt, K)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b > a:
+            ref = dq_rows(qdy[a:b], sdy[:, a:b]) @ dq_blocks(qw[e], sw[e])
+            assert rel_err(dx[a:b], ref) < 1e-12
+    one = oracle.gemm_dgrad_grouped(qdy, sdy, qw[2:3], sw[2:3], np.array([0, Mt]))
+    assert np.array_equal(one, oracle.gemm_dgrad(qdy, sdy, qw[2], sw[2]))
+
+
+def test_grouped_wgrad_is_per_expert_wgrad_and_sums_to_wgrad():
+    """Expert e's dW uses only its own token blocks; an expert without tokens
+    gets zeros; the experts' dW add up to the WGrad over all tokens."""
+    rng = np.random.default_rng(7)
+    N, K = 128, 256
+    off = np.array([0, 256, 256, 384, 768])
+    E, Mt = off.size - 1, int(off[-1])
+    qdyT = rand_q(rng, (N, Mt))
+    sdyT = rng.uniform(0.01, 1, (Mt // 128, N)).astype(np.float32)
+    qxT = rand_q(rng, (K, Mt))
+    sxT = rng.uniform(0.01, 1, (Mt // 128, K)).astype(np.float32)
+    dw = oracle.gemm_wgrad_grouped(qdyT, sdyT, qxT, sxT, off)
+    assert dw.shape == (E, N, K)
+    assert (dw[1] == 0).all()
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if b > a:
+            ref = (dq_cols(qdyT[:, a:b], sdyT[a // 128:b // 128])
+                   @ dq_cols(qxT[:, a:b], sxT[a // 128:b // 128]).T)
+            assert rel_err(dw[e], ref) < 1e-12
+    total = oracle.gemm_wgrad(qdyT, sdyT, qxT, sxT)
+    assert rel_err(dw.sum(axis=0), total) < 1e-12
+    with pytest.raises(ValueError):
+        oracle.gemm_wgrad_grouped(qdyT, sdyT, qxT, sxT, np.array([0, 100, 768]))
