@@ -437,6 +437,135 @@ class MoeStep:
         return nbytes(self.h_in), nbytes(self.h_out)
 
 
+class MoeTrainStep:
+    """One training step of the expert linears of the Qwen3-30B-A3B-shaped MoE
+    layer (4096 tokens, top-8 of 128 experts), in the padded layout that the
+    expert WGrad needs (each expert's rows padded with zero rows to whole
+    128-token groups: 41984 rows for 32768 routed ones):
+      weight sync   128x128 quantization of both stacked expert weights
+      forward       1x128 quantization of X, grouped gate_up, SwiGLU fused
+                    with the 1x128 quantization, grouped down
+      backward      both forms of dY_down, grouped DGrad and WGrad of down
+                    (the SwiGLU output re-quantized 128x1); both forms of
+                    dY_gate_up, grouped DGrad and WGrad of gate_up (X
+                    re-quantized 128x1)
+    dY_gate_up stands for the SwiGLU backward's output (not on this path) and
+    is a synthetic input, like dY_down.  `value` counts the FLOPs of the
+    routed rows only (padding rows are work the layout costs)."""
+
+    def __init__(self, device, seed: int = 0):
+        import torch
+        from fp8_block_quantized_gb300 import workloads as wl
+        import fp8_block_quantized_gb300 as jet
+
+        self.jet = jet
+        off, lins = wl.moe_layer(seed=seed, device="cpu")
+        pad = wl.moe_pad_offsets(off)
+        M, Mp = int(off[-1]), int(pad[-1])
+        self.M = M
+        (_, x_gu, w_gu), (_, _, w_dn) = lins
+        E, Ng, Kg = w_gu.shape
+        _, Nd, Kd = w_dn.shape
+        assert Ng == 2 * Kd
+        self.F = F = Kd
+        cfg = wl.CONFIG_ID["moe"]
+        sc = lambda t: wl.moe_scatter_padded(t, off, pad).to(device)
+        self.x = sc(x_gu)
+        self.dy_dn = sc(wl.grad_output(M, Nd, seed=seed, config=cfg, tensor_id=210))
+        self.dy_gu = sc(wl.grad_output(M, Ng, seed=seed, config=cfg, tensor_id=211))
+        self.w_gu, self.w_dn = w_gu.to(device), w_dn.to(device)
+        self.pad = pad.to(device)
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        b = self.buf = {
+            "qw_gu": e((E, Ng, Kg), u8), "sw_gu": e((E, Ng // 128, Kg // 128), f32),
+            "qw_dn": e((E, Nd, Kd), u8), "sw_dn": e((E, Nd // 128, Kd // 128), f32),
+            "qx": e((Mp, Kg), u8), "sx": e((Kg // 128, Mp), f32),
+            "qxT": e((Kg, Mp), u8), "sxT": e((Mp // 128, Kg), f32),
+            "y_gu": e((Mp, Ng), bf), "qh": e((Mp, F), u8), "sh": e((F // 128, Mp), f32),
+            "qhT": e((F, Mp), u8), "shT": e((Mp // 128, F), f32), "y_dn": e((Mp, Nd), bf),
+            "qdd": e((Mp, Nd), u8), "sdd": e((Nd // 128, Mp), f32),
+            "qddT": e((Nd, Mp), u8), "sddT": e((Mp // 128, Nd), f32),
+            "qdg": e((Mp, Ng), u8), "sdg": e((Ng // 128, Mp), f32),
+            "qdgT": e((Ng, Mp), u8), "sdgT": e((Mp // 128, Ng), f32),
+            "dh": e((Mp, F), bf), "dx": e((Mp, Kg), bf),
+            "dw_dn": e((E, Nd, Kd), bf), "dw_gu": e((E, Ng, Kg), bf)}
+        torch.cuda.synchronize()
+        counts = (off[1:] - off[:-1])
+        used = int((counts > 0).sum())
+        fl_gu, fl_dn = 2 * M * Ng * Kg, 2 * M * Nd * Kd
+        self.flops = 3 * (fl_gu + fl_dn)
+        wbytes = lambda n, k: used * (n * k + 4 * n * k // 16384)
+        act = lambda rows, k: rows * k + 4 * rows * k // 128
+        self.work = {
+            "quant_w_128x128": E * (Ng * Kg + Nd * Kd) * BYTES_PER_ELEM["quant_w_128x128"],
+            "quant_act_1x128": Mp * Kg * BYTES_PER_ELEM["quant_act_1x128"],
+            "swiglu_quant_1x128": Mp * F * BYTES_PER_ELEM["swiglu_quant_1x128"],
+            "quant_dual_1x128_128x1": Mp * (Nd + Ng) * BYTES_PER_ELEM["quant_dual_1x128_128x1"],
+            "requant_128x1": Mp * (F + Kg) * BYTES_PER_ELEM["requant_128x1"],
+            "gemm_fp8_fwd_grouped": fl_gu + fl_dn,
+            "gemm_fp8_fwd_grouped_bytes": act(Mp, Kg) + wbytes(Ng, Kg) + 2 * Mp * Ng
+                                          + act(Mp, F) + wbytes(Nd, Kd) + 2 * Mp * Nd,
+            "gemm_fp8_dgrad_grouped": fl_gu + fl_dn,
+            "gemm_fp8_dgrad_grouped_bytes": act(Mp, Nd) + wbytes(Nd, Kd) + 2 * Mp * Kd
+                                            + act(Mp, Ng) + wbytes(Ng, Kg) + 2 * Mp * Kg,
+            "gemm_fp8_wgrad_grouped": fl_gu + fl_dn,
+            "gemm_fp8_wgrad_grouped_bytes": act(Mp, Nd) + act(Mp, Kd) + 2 * E * Nd * Kd
+                                            + act(Mp, Ng) + act(Mp, Kg) + 2 * E * Ng * Kg}
+        self.launches_per_step = 14
+        self.primary = ("TFLOP/s", self.flops)
+        self.config = {"workload": f"moe_train_qwen3_30b_a3b_T{wl.MOE_TOKENS}",
+                       "tokens": wl.MOE_TOKENS, "experts": E, "topk": wl.MOE_TOPK,
+                       "routed_rows": M, "padded_rows": Mp,
+                       "linears": [("gate_up", Ng, Kg), ("down", Nd, Kd)],
+                       "gemm_tflop_per_step": round(self.flops / 1e12, 4),
+                       "l2": "no flush: per-step working set (~2 GB) > 129 MB L2"}
+
+    def calls(self):
+        j, b, F = self.jet, self.buf, self.F
+        E, Ng, Kg = self.w_gu.shape
+        _, Nd, Kd = self.w_dn.shape
+        return [
+            ("quant_w_128x128", lambda: j.jet_quant_w_128x128(
+                self.w_gu.view(E * Ng, Kg), b["qw_gu"].view(E * Ng, Kg),
+                b["sw_gu"].view(E * Ng // 128, Kg // 128)), "w_gate_up"),
+            ("quant_w_128x128", lambda: j.jet_quant_w_128x128(
+                self.w_dn.view(E * Nd, Kd), b["qw_dn"].view(E * Nd, Kd),
+                b["sw_dn"].view(E * Nd // 128, Kd // 128)), "w_down"),
+            ("quant_act_1x128", lambda: j.jet_quant_act_1x128(self.x, b["qx"], b["sx"]), "x"),
+            ("gemm_fp8_fwd_grouped", lambda: j.jet_gemm_fp8_fwd_grouped(
+                b["qx"], b["sx"], b["qw_gu"], b["sw_gu"], self.pad, b["y_gu"]), "gate_up"),
+            ("swiglu_quant_1x128", lambda: j.jet_swiglu_quant_1x128(
+                b["y_gu"][:, :F], b["y_gu"][:, F:], b["qh"], b["sh"]), "h"),
+            ("gemm_fp8_fwd_grouped", lambda: j.jet_gemm_fp8_fwd_grouped(
+                b["qh"], b["sh"], b["qw_dn"], b["sw_dn"], self.pad, b["y_dn"]), "down"),
+            ("quant_dual_1x128_128x1", lambda: j.jet_quant_dual_1x128_128x1(
+                self.dy_dn, b["qdd"], b["sdd"], b["qddT"], b["sddT"]), "dy_down"),
+            ("gemm_fp8_dgrad_grouped", lambda: j.jet_gemm_fp8_dgrad_grouped(
+                b["qdd"], b["sdd"], b["qw_dn"], b["sw_dn"], self.pad, b["dh"]), "down"),
+            ("requant_128x1", lambda: j.jet_requant_128x1(b["qh"], b["sh"], b["qhT"], b["shT"]), "h"),
+            ("gemm_fp8_wgrad_grouped", lambda: j.jet_gemm_fp8_wgrad_grouped(
+                b["qddT"], b["sddT"], b["qhT"], b["shT"], self.pad, b["dw_dn"]), "down"),
+            ("quant_dual_1x128_128x1", lambda: j.jet_quant_dual_1x128_128x1(
+                self.dy_gu, b["qdg"], b["sdg"], b["qdgT"], b["sdgT"]), "dy_gate_up"),
+            ("gemm_fp8_dgrad_grouped", lambda: j.jet_gemm_fp8_dgrad_grouped(
+                b["qdg"], b["sdg"], b["qw_gu"], b["sw_gu"], self.pad, b["dx"]), "gate_up"),
+            ("requant_128x1", lambda: j.jet_requant_128x1(b["qx"], b["sx"], b["qxT"], b["sxT"]), "x"),
+            ("gemm_fp8_wgrad_grouped", lambda: j.jet_gemm_fp8_wgrad_grouped(
+                b["qdgT"], b["sdgT"], b["qxT"], b["sxT"], self.pad, b["dw_gu"]), "gate_up"),
+        ]
+
+    def host_io(self):
+        import torch
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        ins = [self.x, self.dy_dn, self.dy_gu, self.w_gu, self.w_dn, self.pad]
+        self.h_in = [(pin(t), t) for t in ins]
+        outs = [self.buf[k] for k in ("y_dn", "dx", "dw_gu", "dw_dn")]
+        self.h_out = [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t) for t in outs]
+        nbytes = lambda pairs: sum(h.numel() * h.element_size() for h, _ in pairs)
+        return nbytes(self.h_in), nbytes(self.h_out)
+
+
 class MetricStep:
     """token-mult-prob-error over n = 4,194,304 tokens, and the masked variant
     with per-token importance weights (75% of the tokens in the mask)."""
@@ -489,6 +618,8 @@ def make_step(args, device, rank):
         return SyncStep(device, seed=args.seed + rank)
     if args.workload == "moe":
         return MoeStep(device, seed=args.seed + rank)
+    if args.workload == "moe_train":
+        return MoeTrainStep(device, seed=args.seed + rank)
     return MetricStep(device, seed=args.seed + rank)
 
 
@@ -919,10 +1050,12 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("jet", "reference"), default="jet")
-    ap.add_argument("--workload", choices=("train8b", "train32b", "rollout", "sync", "metric", "moe"),
+    ap.add_argument("--workload", choices=("train8b", "train32b", "rollout", "sync", "metric", "moe",
+                                           "moe_train"),
                     default="train8b",
                     help="train8b (default, the benchmark's workload), train32b, or the "
-                         "rollout / weight-sync / metric / MoE expert-forward configurations")
+                         "rollout / weight-sync / metric / MoE expert forward / MoE expert "
+                         "training configurations")
     ap.add_argument("--tokens", type=int, default=2048, help="M for --workload rollout")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")

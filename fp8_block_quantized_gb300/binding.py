@@ -37,6 +37,8 @@ SIGNATURES = {
     "jet_swiglu_quant_1x128": [P, P, I, I, I, P, P, P],
     "jet_gemm_fp8_fwd": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_gemm_fp8_fwd_grouped": [P, P, P, P, P, I, I, I, I, P, P],
+    "jet_gemm_fp8_dgrad_grouped": [P, P, P, P, P, I, I, I, I, P, P],
+    "jet_gemm_fp8_wgrad_grouped": [P, P, P, P, P, I, I, I, I, P, P],
     "jet_gemm_fp8_dgrad": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_gemm_fp8_wgrad": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_token_mult_prob_error": [P, P, I, P, P, Z, P],
@@ -239,6 +241,39 @@ def jet_gemm_fp8_fwd_grouped(qx, sx, qw, sw, offsets, y, stream=None):
         _stream(stream)))
 
 
+def jet_gemm_fp8_dgrad_grouped(qdy, sdy, qw, sw, offsets, dx, stream=None):
+    """Expert-grouped DGrad; ``offsets`` as in jet_gemm_fp8_fwd_grouped."""
+    import torch
+    M, N = qdy.shape
+    E, K = qw.shape[0], qw.shape[2]
+    _need(qdy, torch.uint8, (M, N), "qdy")
+    _need(sdy, torch.float32, (N // 128, M), "sdy")
+    _need(qw, torch.uint8, (E, N, K), "qw")
+    _need(sw, torch.float32, (E, N // 128, K // 128), "sw")
+    _need(offsets, torch.int64, (E + 1,), "offsets")
+    _need(dx, torch.bfloat16, (M, K), "dx")
+    _check("jet_gemm_fp8_dgrad_grouped", load().jet_gemm_fp8_dgrad_grouped(
+        _ptr(qdy), _ptr(sdy), _ptr(qw), _ptr(sw), _ptr(offsets), E, M, N, K, _ptr(dx),
+        _stream(stream)))
+
+
+def jet_gemm_fp8_wgrad_grouped(qdyT, sdyT, qxT, sxT, offsets, dw, stream=None):
+    """Expert-grouped WGrad over each expert's tokens; offsets in multiples of 128."""
+    import torch
+    N, M = qdyT.shape
+    K = qxT.shape[0]
+    E = offsets.shape[0] - 1
+    _need(qdyT, torch.uint8, (N, M), "qdyT")
+    _need(sdyT, torch.float32, (M // 128, N), "sdyT")
+    _need(qxT, torch.uint8, (K, M), "qxT")
+    _need(sxT, torch.float32, (M // 128, K), "sxT")
+    _need(offsets, torch.int64, (E + 1,), "offsets")
+    _need(dw, torch.bfloat16, (E, N, K), "dw")
+    _check("jet_gemm_fp8_wgrad_grouped", load().jet_gemm_fp8_wgrad_grouped(
+        _ptr(qdyT), _ptr(sdyT), _ptr(qxT), _ptr(sxT), _ptr(offsets), E, M, N, K, _ptr(dw),
+        _stream(stream)))
+
+
 def jet_gemm_fp8_dgrad(qdy, sdy, qw, sw, dx, ws=None, stream=None):
     import torch
     M, N = qdy.shape
@@ -378,6 +413,24 @@ def gemm_fp8_fwd_grouped(qx, sx, qw, sw, offsets, stream=None):
     y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device)
     jet_gemm_fp8_fwd_grouped(qx, sx, qw, sw, offsets, y, stream)
     return y
+
+
+def gemm_fp8_dgrad_grouped(qdy, sdy, qw, sw, offsets, stream=None):
+    """dX [M][K] BF16: every expert's token rows times that expert's weights."""
+    import torch
+    M, K = qdy.shape[0], qw.shape[2]
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=qdy.device)
+    jet_gemm_fp8_dgrad_grouped(qdy, sdy, qw, sw, offsets, dx, stream)
+    return dx
+
+
+def gemm_fp8_wgrad_grouped(qdyT, sdyT, qxT, sxT, offsets, stream=None):
+    """dW [E][N][K] BF16: every expert's weight gradient over its own tokens."""
+    import torch
+    N, K, E = qdyT.shape[0], qxT.shape[0], offsets.shape[0] - 1
+    dw = torch.empty((E, N, K), dtype=torch.bfloat16, device=qdyT.device)
+    jet_gemm_fp8_wgrad_grouped(qdyT, sdyT, qxT, sxT, offsets, dw, stream)
+    return dw
 
 
 def gemm_fp8_dgrad(qdy, sdy, qw, sw, stream=None):

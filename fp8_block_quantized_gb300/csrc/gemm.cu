@@ -58,9 +58,14 @@ namespace {
 using namespace jet;
 using namespace jet::ptx;
 
-// kFwdGrouped: the forward product of several expert linears in one launch
-// (tokens concatenated in expert order, weights stacked [E][N][K]).
-enum Mode { kFwd = 0, kDgrad = 1, kWgrad = 2, kFwdGrouped = 3 };
+// The grouped modes run the product of several expert linears in one launch
+// (tokens concatenated in expert order, weights stacked [E][N][K]):
+// kFwdGrouped and kDgradGrouped split the rows by expert, kWgradGrouped the
+// contraction (each expert's dW over its own tokens, outputs stacked).
+enum Mode { kFwd = 0, kDgrad = 1, kWgrad = 2, kFwdGrouped = 3, kDgradGrouped = 4, kWgradGrouped = 5 };
+constexpr int base_mode(int mode) {
+    return mode == kFwdGrouped ? kFwd : mode == kDgradGrouped ? kDgrad : mode == kWgradGrouped ? kWgrad : mode;
+}
 constexpr int kMaxGroups = 384;  // one expert per thread of the unit-count scan
 
 constexpr int kThreads = 384;
@@ -194,7 +199,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 uint16_t *__restrict__ out, int R, int C, int D, Raster raster, int splits,
                 float *__restrict__ partial, const int64_t *__restrict__ goff, int gE,
                 unsigned *status) {
-    using CF = Cfg<BN, CL, CL == 2 || MODE == kFwdGrouped>;
+    using CF = Cfg<BN, CL, CL == 2 || MODE >= kFwdGrouped>;
     constexpr int S = CF::kStages;
     constexpr int SS = CF::kScaleSlots;
     constexpr bool kPair = CL == 2;
@@ -205,8 +210,9 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     // grouped forward: per expert, its first row and the prefix of its units
-    constexpr bool kGrp = MODE == kFwdGrouped;
-    constexpr bool kFwdLike = MODE == kFwd || kGrp;
+    constexpr bool kGrp = MODE >= kFwdGrouped;
+    constexpr int BASE = base_mode(MODE);
+    constexpr bool kFwdLike = BASE == kFwd;
     constexpr int kGT = kGrp ? kMaxGroups + 1 : 1;
     __shared__ int g_off[kGT], g_pre[kGT];
     __shared__ int g_warp[kThreads / 32];
@@ -265,15 +271,18 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     griddep_launch_dependents();
     griddep_wait();
     if (kGrp) {
-        // Expert e owns rows off[e] .. off[e+1] (clamped to [0, R], so that
-        // nothing outside the output is ever written) and
-        // ceil(rows / 128) * tiles_n units; one expert per thread, then a
-        // block-wide inclusive scan of the unit counts.
+        // Expert e owns tokens off[e] .. off[e+1], clamped to the token
+        // count (R, or D for WGrad) so that nothing outside the operands
+        // and the output is ever touched.  Forward / DGrad: the expert's
+        // rows make ceil(rows / 128) * tiles_n units; one expert per thread,
+        // then a block-wide inclusive scan of the unit counts.  WGrad: every
+        // expert has the same units (its whole dW).
         const int i = threadIdx.x;
-        auto clampr = [&](int64_t v) { return (int)(v < 0 ? 0 : (v > R ? R : v)); };
+        const int glim = BASE == kWgrad ? D : R;
+        auto clampr = [&](int64_t v) { return (int)(v < 0 ? 0 : (v > glim ? glim : v)); };
         int cnt = 0;
         for (int j = i; j <= gE; j += kThreads) g_off[j] = clampr(goff[j]);  // gE + 1 entries
-        if (i < gE) {
+        if (BASE != kWgrad && i < gE) {
             const int rows = clampr(goff[i + 1]) - clampr(goff[i]);
             cnt = rows > 0 ? (rows + BM - 1) / BM * tiles_n : 0;
         }
@@ -290,12 +299,24 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (i < gE) g_pre[i + 1] = before + incl;
         if (i == 0) g_pre[0] = 0;
         __syncthreads();
-        total = g_pre[gE];
+        total = BASE == kWgrad ? gE * units_m * tiles_n : g_pre[gE];
     }
-    // Work unit t -> row tile origin m0 (absolute row), column origin n0, its
-    // slice range, its row limit and the expert whose weights it uses.
-    auto coords = [&](int t, int &m0, int &n0, int &kb0, int &kb1, int &rlim, int &grp) {
-        if (kGrp) {
+    // Work unit t -> row tile origin m0 (row of A), column origin n0, its
+    // slice range, the expert whose weights it uses, and in output rows its
+    // origin mo and row limit rlim.
+    auto coords = [&](int t, int &m0, int &n0, int &kb0, int &kb1, int &grp, int &mo,
+                      int &rlim) {
+        if (kGrp && BASE == kWgrad) {
+            const int per = units_m * tiles_n;
+            grp = t / per;
+            const int u = t - grp * per, mu = u / tiles_n;
+            m0 = (mu * CL + (int)rank) * BM;
+            n0 = (u - mu * tiles_n) * BN;
+            kb0 = g_off[grp] / BK;
+            kb1 = (g_off[grp + 1] > g_off[grp] ? g_off[grp + 1] : g_off[grp]) / BK;
+            mo = grp * R + m0;
+            rlim = grp * R + R;
+        } else if (kGrp) {
             int lo = 0, hi = gE - 1;  // the expert e with g_pre[e] <= t < g_pre[e+1]
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -308,6 +329,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             rlim = g_off[lo + 1] > g_off[lo] ? g_off[lo + 1] : g_off[lo];
             kb0 = 0;
             kb1 = nkb;
+            mo = m0;
         } else {
             int mu, nt;
             unit_coords(t, splits, nkb, units_m, tiles_n, raster, mu, nt, kb0, kb1);
@@ -315,6 +337,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             n0 = nt * BN;
             rlim = R;
             grp = 0;
+            mo = m0;
         }
     };
 
@@ -332,8 +355,12 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t it = 0;
             bool ok = true;
             for (int t = unit0; ok && t < total; t += unit_step) {
-                int m0, n0, kb0, kb1, rlim, grp;
-                coords(t, m0, n0, kb0, kb1, rlim, grp);
+                int m0, n0, kb0, kb1, grp, mo, rlim;
+                coords(t, m0, n0, kb0, kb1, grp, mo, rlim);
+                // the expert's weights in the stacked B: rows (forward) or,
+                // read MN-major, the contraction axis (DGrad)
+                const int brow0 = kGrp && BASE == kFwd ? grp * C : 0;
+                const int bk0 = kGrp && BASE == kDgrad ? grp * D : 0;
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
@@ -356,7 +383,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                   r < R ? 4u : 0u);
                     }
                     const uint32_t scol = slot + CF::kScaleRowBytes;
-                    if (MODE == kWgrad) {
+                    if (BASE == kWgrad) {
                         const float *src = sb + (size_t)kb * C + n0;
 #pragma unroll
                         for (int j = 0; j < BN / 128; ++j)
@@ -364,7 +391,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     } else if (lane < BN / 128) {
                         const float *src =
                             kFwdLike ? sb + ((size_t)grp * (C / 128) + n0 / 128 + lane) * nkb + kb
-                                     : sb + (size_t)kb * (C / 128) + n0 / 128 + lane;
+                                     : sb + ((size_t)grp * nkb + kb) * (C / 128) + n0 / 128 + lane;
                         cp_async4(scol + lane * 4, src, 4u);
                     }
                     cp_async_arrive_noinc(&sfull_bar[ss]);
@@ -377,22 +404,22 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             const uint32_t fb = map_to_cta(&full_bar[s], 0);
                             if (leader) mbar_arrive_expect_tx(&full_bar[s], 2 * CF::kStageBytes);
                             tma_load_2d_pair(a_s, &tmA, fb, kb * BK, m0, pol_a);
-                            if (MODE == kDgrad)
+                            if (BASE == kDgrad)
                                 tma_load_2d_pair(b_s, &tmB, fb, n0 + CF::kBRows * (int)rank,
-                                                 kb * BK, pol_b);
+                                                 bk0 + kb * BK, pol_b);
                             else
                                 tma_load_2d_pair(b_s, &tmB, fb, kb * BK,
-                                                 n0 + CF::kBRows * (int)rank, pol_b);
+                                                 brow0 + n0 + CF::kBRows * (int)rank, pol_b);
                         } else {
                             mbar_arrive_expect_tx(&full_bar[s], CF::kStageBytes);
                             tma_load_2d(a_s, &tmA, &full_bar[s], kb * BK, m0, pol_a);
-                            if (MODE == kDgrad) {
+                            if (BASE == kDgrad) {
 #pragma unroll
                                 for (int h = 0; h < BN / 128; ++h)
                                     tma_load_2d(b_s + h * 128 * BK, &tmB, &full_bar[s],
-                                                n0 + 128 * h, kb * BK, pol_b);
+                                                n0 + 128 * h, bk0 + kb * BK, pol_b);
                             } else {
-                                tma_load_2d(b_s, &tmB, &full_bar[s], kb * BK, grp * C + n0,
+                                tma_load_2d(b_s, &tmB, &full_bar[s], kb * BK, brow0 + n0,
                                             pol_b);
                             }
                         }
@@ -410,14 +437,14 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         } else if (warp == 1 && leader) {
             // --------------------------------------------------- MMA issuer
             // (in a pair only the leader issues; the MMA spans both CTAs)
-            constexpr bool kMN = MODE == kDgrad;
+            constexpr bool kMN = BASE == kDgrad;
             constexpr uint32_t kIdesc =
                 kPair ? idesc_e4m3_f32(2 * BM, BN, kMN) : idesc_e4m3_f32(BM, kMN ? 128 : BN, kMN);
             uint32_t it = 0;
             bool ok = true;
             for (int t = unit0; ok && t < total; t += unit_step) {
-                int m0, n0, kb0, kb1, rlim, grp;
-                coords(t, m0, n0, kb0, kb1, rlim, grp);
+                int m0, n0, kb0, kb1, grp, mo, rlim;
+                coords(t, m0, n0, kb0, kb1, grp, mo, rlim);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t use = it / S;
@@ -498,9 +525,9 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         uint32_t it = 0;
         bool ok = true;
         for (int t = unit0; ok && t < total; t += unit_step) {
-            int m0, n0, kb0, kb1, rlim, grp;
-            coords(t, m0, n0, kb0, kb1, rlim, grp);
-            const int row = m0 + quad * 32 + lane;
+            int m0, n0, kb0, kb1, grp, mo, rlim;
+            coords(t, m0, n0, kb0, kb1, grp, mo, rlim);
+            const int row = mo + quad * 32 + lane;  // output row
             const bool row_ok = row < rlim;
             const int col0 = n0 + ch * H;
             float2 acc[H / 2];
@@ -522,7 +549,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const float rs = slot[quad * 32 + lane];
                 const float *scol = slot + BM;
                 float sc = 0.0f;
-                if (MODE != kWgrad) {
+                if (BASE != kWgrad) {
                     sc = rs * scol[(ch * H) / 128];
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sempty_bar[ss]);
@@ -536,7 +563,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * BN + ch * H;
                 uint32_t p0[16], p1[16];
                 tmem_ld16(taddr, p0);
-                if (MODE != kWgrad) {
+                if (BASE != kWgrad) {
                     const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
                     for (int c = 0; c < NCH; c += 2) {
@@ -573,11 +600,11 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         mbar_arrive_cluster_relaxed(tempty_remote[buf]);
                     else
                         mbar_arrive(&tempty_bar[buf]);
-                    if (MODE == kWgrad) mbar_arrive(&sempty_bar[ss]);
+                    if (BASE == kWgrad) mbar_arrive(&sempty_bar[ss]);
                 }
             }
             if (!ok) break;
-            if (kPair || (kGrp && m0 + quad * 32 + 31 < rlim)) {
+            if ((kPair && !kGrp) || (kGrp && mo + quad * 32 + 31 < rlim)) {
                 // Stage this warp's 32 rows x H columns (64-column boxes,
                 // 128-byte swizzle: 16-byte chunk j of row r goes to j ^ (r % 8))
                 // and hand them to the TMA; rows past R are clipped by it.  (A
@@ -604,7 +631,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 if (lane == 0) {
 #pragma unroll
                     for (int h = 0; h < H / 64; ++h)
-                        tma_store_2d_hint(&tmY, wbuf + 4096 * h, col0 + 64 * h, m0 + quad * 32,
+                        tma_store_2d_hint(&tmY, wbuf + 4096 * h, col0 + 64 * h, mo + quad * 32,
                                           pol_out);
                     bulk_commit_group();
                 }
@@ -755,7 +782,7 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
                   const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D, int splits,
                   float *partial, cudaStream_t stream, const int64_t *goff = nullptr,
                   int gE = 0) {
-    using CF = Cfg<BN, CL, CL == 2 || MODE == kFwdGrouped>;
+    using CF = Cfg<BN, CL, CL == 2 || MODE >= kFwdGrouped>;
     auto kernel = gemm_fp8_kernel<BN, MODE, CL>;
     static std::mutex mu;
     static int max_units[64] = {};  // co-resident CTAs (CL = 1) or clusters (CL = 2)
@@ -796,16 +823,24 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     }
     CUtensorMap ta, tb, ty;
     if (!make_map_u8(&ta, a, (uint64_t)D, (uint64_t)R, BK, BM)) return JET_ERR_CUDA;
-    constexpr bool kStagedOut = CL == 2 || MODE == kFwdGrouped;
-    if (kStagedOut && !make_map_out(&ty, out, (uint64_t)C, (uint64_t)R)) return JET_ERR_CUDA;
+    constexpr int BASE = base_mode(MODE);
+    constexpr bool kStagedOut = CL == 2 || MODE >= kFwdGrouped;
+    // grouped WGrad writes the experts' dW stacked, [gE * R][C]
+    const uint64_t out_rows = MODE == kWgradGrouped ? (uint64_t)gE * (uint64_t)R : (uint64_t)R;
+    if (kStagedOut && !make_map_out(&ty, out, (uint64_t)C, out_rows)) return JET_ERR_CUDA;
     if (!kStagedOut) ty = ta;  // unused: this kernel stores from registers
-    // grouped forward: B is the experts' weights stacked, [gE * C][D]
+    // grouped forward / DGrad: B is the experts' weights stacked, [gE * C][D]
+    // (forward) or, read MN-major, [gE * D][C] (DGrad)
     const uint64_t b_rows = MODE == kFwdGrouped ? (uint64_t)gE * (uint64_t)C : (uint64_t)C;
-    bool okb = MODE == kDgrad ? make_map_u8(&tb, b, (uint64_t)C, (uint64_t)D, 128, BK)
+    const uint64_t b_kdim = MODE == kDgradGrouped ? (uint64_t)gE * (uint64_t)D : (uint64_t)D;
+    bool okb = BASE == kDgrad ? make_map_u8(&tb, b, (uint64_t)C, b_kdim, 128, BK)
                               : make_map_u8(&tb, b, (uint64_t)D, b_rows, BK, CF::kBRows);
     if (!okb) return JET_ERR_CUDA;
-    // (grouped: at most one unit per expert more than the dense count)
-    const int64_t units = ((R + BM * CL - 1) / (BM * CL) + gE) * (C / BN) * splits;
+    // grouped forward / DGrad: at most one unit per expert more than the
+    // dense count; grouped WGrad: every expert's whole dW
+    const int64_t tiles_mn = (R + BM * CL - 1) / (BM * CL) * (C / BN);
+    const int64_t units = MODE == kWgradGrouped ? gE * tiles_mn
+                          : ((R + BM * CL - 1) / (BM * CL) + gE) * (C / BN) * splits;
     const int64_t grid_units = units < max_units[dev.ordinal] ? units : max_units[dev.ordinal];
     cfg.gridDim = dim3((unsigned)(grid_units * CL));
     const Raster raster = choose_raster(R, C, D);
@@ -959,6 +994,71 @@ jet_status jet_gemm_fp8_fwd_grouped(const uint8_t *qx, const float *sx, const ui
                                            (int)E);
     return launch<128, kFwdGrouped, 1>(dev, qx, sx, qw, sw, y, M, N, K, 1, nullptr, s, offsets,
                                        (int)E);
+}
+
+jet_status jet_gemm_fp8_dgrad_grouped(const uint8_t *qdy, const float *sdy, const uint8_t *qw,
+                                      const float *sw, const int64_t *offsets, int64_t E,
+                                      int64_t M, int64_t N, int64_t K, uint16_t *dx,
+                                      jet_stream_t stream) {
+    JET_REQUIRE(M >= 0 && N >= 0 && K >= 0 && E >= 1 && E <= kMaxGroups, JET_ERR_SHAPE);
+    const bool out_empty = (M == 0 || K == 0), in_empty = out_empty || N == 0;
+    JET_REQUIRE(out_empty || (dx && offsets), JET_ERR_NULL);
+    JET_REQUIRE(in_empty || (qdy && sdy && qw && sw), JET_ERR_NULL);
+    JET_REQUIRE(N % 128 == 0 && K % 128 == 0 && M < kMaxDim && N < kMaxDim && K < kMaxDim &&
+                    E * N < kMaxDim,
+                JET_ERR_SHAPE);
+    JET_REQUIRE(aligned16(qdy) && aligned16(sdy) && aligned16(qw) && aligned16(sw) &&
+                    aligned16(offsets) && aligned16(dx),
+                JET_ERR_ALIGN);
+    DeviceInfo dev;
+    jet_status st = current_device(&dev);
+    if (st != JET_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    if (out_empty) return JET_OK;
+    if (N == 0)  // empty contraction: the product is zero
+        return cudaMemsetAsync(dx, 0, (size_t)M * K * 2, s) == cudaSuccess ? JET_OK : JET_ERR_CUDA;
+    // rows R = tokens, columns C = K, contraction D = N
+    if (K % 256 == 0)
+        return launch<256, kDgradGrouped, 1>(dev, qdy, sdy, qw, sw, dx, M, K, N, 1, nullptr, s,
+                                             offsets, (int)E);
+    return launch<128, kDgradGrouped, 1>(dev, qdy, sdy, qw, sw, dx, M, K, N, 1, nullptr, s,
+                                         offsets, (int)E);
+}
+
+jet_status jet_gemm_fp8_wgrad_grouped(const uint8_t *qdyT, const float *sdyT, const uint8_t *qxT,
+                                      const float *sxT, const int64_t *offsets, int64_t E,
+                                      int64_t M, int64_t N, int64_t K, uint16_t *dw,
+                                      jet_stream_t stream) {
+    JET_REQUIRE(M >= 0 && N >= 0 && K >= 0 && E >= 1 && E <= kMaxGroups, JET_ERR_SHAPE);
+    const bool out_empty = (N == 0 || K == 0), in_empty = out_empty || M == 0;
+    JET_REQUIRE(out_empty || (dw && offsets), JET_ERR_NULL);
+    JET_REQUIRE(in_empty || (qdyT && sdyT && qxT && sxT), JET_ERR_NULL);
+    JET_REQUIRE(M % 128 == 0 && N % 128 == 0 && K % 128 == 0 && M < kMaxDim && N < kMaxDim &&
+                    K < kMaxDim && E * N < kMaxDim,
+                JET_ERR_SHAPE);
+    JET_REQUIRE(aligned16(qdyT) && aligned16(sdyT) && aligned16(qxT) && aligned16(sxT) &&
+                    aligned16(offsets) && aligned16(dw),
+                JET_ERR_ALIGN);
+    DeviceInfo dev;
+    jet_status st = current_device(&dev);
+    if (st != JET_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    if (out_empty) return JET_OK;
+    if (M == 0)  // no tokens: every expert's gradient is zero
+        return cudaMemsetAsync(dw, 0, (size_t)E * N * K * 2, s) == cudaSuccess ? JET_OK
+                                                                             : JET_ERR_CUDA;
+    // rows R = N (per expert), columns C = K, contraction D = M (the expert's
+    // token blocks); CTA pairs over 256 rows of an expert's dW when K is a
+    // multiple of 256 and N has at least two row tiles
+    if (K % 256 == 0) {
+        if (N > BM)
+            return launch<256, kWgradGrouped, 2>(dev, qdyT, sdyT, qxT, sxT, dw, N, K, M, 1,
+                                                 nullptr, s, offsets, (int)E);
+        return launch<256, kWgradGrouped, 1>(dev, qdyT, sdyT, qxT, sxT, dw, N, K, M, 1, nullptr,
+                                             s, offsets, (int)E);
+    }
+    return launch<128, kWgradGrouped, 1>(dev, qdyT, sdyT, qxT, sxT, dw, N, K, M, 1, nullptr, s,
+                                         offsets, (int)E);
 }
 
 jet_status jet_gemm_fp8_dgrad(const uint8_t *qdy, const float *sdy, const uint8_t *qw,

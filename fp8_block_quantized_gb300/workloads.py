@@ -213,6 +213,25 @@ def moe_layer(seed=0, device="cpu", tokens=MOE_TOKENS, experts=MOE_EXPERTS, topk
     return off, out
 
 
+def moe_pad_offsets(off: torch.Tensor, group: int = 128) -> torch.Tensor:
+    """Offsets of the same experts with each expert's rows padded up to a
+    whole number of `group`-token groups (the layout the expert WGrad needs)."""
+    counts = (off[1:] - off[:-1] + group - 1) // group * group
+    pad = torch.zeros_like(off)
+    pad[1:] = torch.cumsum(counts, 0)
+    return pad
+
+
+def moe_scatter_padded(t: torch.Tensor, off: torch.Tensor, pad: torch.Tensor) -> torch.Tensor:
+    """Rows of each expert moved from `off` to its padded start in `pad`; the
+    padding rows are zero."""
+    out = torch.zeros((int(pad[-1]),) + tuple(t.shape[1:]), dtype=t.dtype, device=t.device)
+    for e in range(off.numel() - 1):
+        a, b, p = int(off[e]), int(off[e + 1]), int(pad[e])
+        out[p:p + b - a] = t[a:b]
+    return out
+
+
 def bf16_bits(t: torch.Tensor):
     """uint16 numpy view of a BF16 tensor's bit patterns (host copy)."""
     import numpy as np

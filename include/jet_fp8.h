@@ -222,6 +222,47 @@ JET_API jet_status jet_gemm_fp8_fwd_grouped(const uint8_t *qx, const float *sx,
                                             jet_stream_t stream);
 
 /*
+ * Grouped DGrad of expert linears, one launch: for every expert e and its
+ * tokens m in [offsets[e], offsets[e+1]),
+ *   dX[m][k] = sum_nb sdy[nb][m] * sw[e][nb][k/128] * sum_{n in nb} qdy[m][n] qw[e][n][k]
+ * with the arithmetic of jet_gemm_fp8_dgrad.  Source and layout as
+ * jet_gemm_fp8_fwd_grouped (the backward of the same expert linears).
+ *   qdy [M][N], sdy [Nb][M]: the output gradients of all experts' tokens in
+ *     expert order.  qw [E][N][K], sw [E][Nb][Kb] as in the forward.
+ *   offsets [E+1] int64 DEVICE array, as in jet_gemm_fp8_fwd_grouped.
+ *   dx [M][K] BF16 bits (out).  1 <= E <= 384; N, K multiples of 128.
+ */
+JET_API jet_status jet_gemm_fp8_dgrad_grouped(const uint8_t *qdy, const float *sdy,
+                                              const uint8_t *qw, const float *sw,
+                                              const int64_t *offsets, int64_t E, int64_t M,
+                                              int64_t N, int64_t K, uint16_t *dx,
+                                              jet_stream_t stream);
+
+/*
+ * Grouped WGrad of expert linears, one launch: every expert's weight
+ * gradient over its own tokens,
+ *   dW[e][n][k] = sum_{mb in expert e} sdyT[mb][n] * sxT[mb][k]
+ *                 * sum_{m in mb} qdyT[n][m] qxT[k][m]
+ * with the arithmetic of jet_gemm_fp8_wgrad.  Source as
+ * jet_gemm_fp8_fwd_grouped; 128x1 groups as jet_gemm_fp8_wgrad.
+ *   qdyT [N][M], sdyT [Mb][N] and qxT [K][M], sxT [Mb][K]: the 128x1 forms
+ *     (jet_requant_128x1 / jet_quant_dual_1x128_128x1) of the expert-ordered
+ *     output gradients and inputs.
+ *   offsets [E+1] int64 DEVICE array: offsets[0] = 0, non-decreasing,
+ *     offsets[E] = M, every offset a multiple of 128 (a 128-token group never
+ *     straddles two experts: experts are padded to whole groups, with zero
+ *     rows).  Offsets are clamped to [0, M]; other violations give
+ *     unspecified results, never a write outside dw.
+ *   dw [E][N][K] BF16 bits (out); an expert without tokens gets zeros.
+ *   M, N, K multiples of 128; 1 <= E <= 384.
+ */
+JET_API jet_status jet_gemm_fp8_wgrad_grouped(const uint8_t *qdyT, const float *sdyT,
+                                              const uint8_t *qxT, const float *sxT,
+                                              const int64_t *offsets, int64_t E, int64_t M,
+                                              int64_t N, int64_t K, uint16_t *dw,
+                                              jet_stream_t stream);
+
+/*
  * DGrad GEMM  dX = dY W :
  *   dX[m][k] = sum_nb sdy[nb][m] * sw[nb][k/128] * sum_{n in nb} qdy[m][n] qw[n][k]
  * FP32 accumulation, BF16 out.  Source: gist.science summary,

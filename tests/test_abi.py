@@ -178,6 +178,22 @@ def test_grouped_gemm_checks(lib):
     assert f(None, None, None, None, None, 8, 0, 128, 128, None, None) in (OK, DEVICE)
 
 
+@pytest.mark.parametrize("name", ["jet_gemm_fp8_dgrad_grouped", "jet_gemm_fp8_wgrad_grouped"])
+def test_grouped_backward_checks(lib, name):
+    f = getattr(lib, name)
+    args = [fake(A), fake(B), fake(C), fake(D)]
+    assert f(*args, fake(A), 8, 256, 128, 128, None, None) == NULL
+    assert f(*args, None, 8, 256, 128, 128, fake(A), None) == NULL
+    assert f(*args, fake(A), 0, 256, 128, 128, fake(A), None) == SHAPE
+    assert f(*args, fake(A), 385, 256, 128, 128, fake(A), None) == SHAPE
+    assert f(*args, fake(A), 8, 256, 100, 128, fake(A), None) == SHAPE
+    assert f(*args, fake(A), 8, 256, 128, 100, fake(A), None) == SHAPE
+    assert f(*args, fake(MIS), 8, 256, 128, 128, fake(A), None) == ALIGN
+    assert f(*args, fake(A), 8, 256, 128, 128, fake(MIS), None) == ALIGN
+    if name == "jet_gemm_fp8_wgrad_grouped":   # tokens are the 128x1 group axis
+        assert f(*args, fake(A), 8, 200, 128, 128, fake(A), None) == SHAPE
+
+
 def test_metric_checks(lib):
     f = lib.jet_token_mult_prob_error
     assert f(None, fake(B), 16, fake(C), fake(D), 8, None) == NULL
@@ -221,6 +237,9 @@ def test_no_device_is_reported():
                                         128, 128, fake(A), None) == DEVICE
     assert lib.jet_swiglu_quant_1x128(fake(A), fake(B), 512, 4, 256, fake(C), fake(D),
                                       None) == DEVICE
+    for name in ("jet_gemm_fp8_dgrad_grouped", "jet_gemm_fp8_wgrad_grouped"):
+        assert getattr(lib, name)(fake(A), fake(B), fake(C), fake(D), fake(A), 4, 256, 128,
+                                  128, fake(A), None) == DEVICE
     assert lib.jet_device_status(None, None) == DEVICE
 
 

@@ -323,3 +323,117 @@ def test_grouped_moe_layer_sampled(jet, lin):
     counts = (off[1:] - off[:-1]).numpy()
     experts = sorted({int(counts.argmin()), int(counts.argmax()), 0, 63, 127})
     run_grouped(jet, x, w, off.numpy(), rows_per_expert=6, experts=experts)
+
+
+# -------------------------------------- grouped DGrad / WGrad (expert backward) --
+
+def run_grouped_dgrad(jet, dy, w, off, rows_per_expert=None, experts=None):
+    qdy, sdy = oracle.quant_act_1x128(bits(dy))
+    E = w.shape[0]
+    pairs = [oracle.quant_w_128x128(bits(w[e])) for e in range(E)]
+    qw, sw = np.stack([p[0] for p in pairs]), np.stack([p[1] for p in pairs])
+    off = np.asarray(off, np.int64)
+    dx = jet.gemm_fp8_dgrad_grouped(to_dev(qdy), to_dev(sdy), to_dev(qw), to_dev(sw),
+                                    torch.from_numpy(off).cuda())
+    torch.cuda.synchronize()
+    if rows_per_expert is None:
+        assert_gemm_close(dx, oracle.gemm_dgrad_grouped(qdy, sdy, qw, sw, off), "grouped dgrad")
+        return
+    for e in experts:
+        a, b = int(off[e]), int(off[e + 1])
+        if b == a:
+            continue
+        r = sample_rows(b - a, rows_per_expert, seed=e)
+        r = np.arange(b - a) if r is None else r
+        ref = oracle.gemm_dgrad(np.ascontiguousarray(qdy[a:b]), np.ascontiguousarray(sdy[:, a:b]),
+                                qw[e], sw[e], rows=r)
+        assert_gemm_close(dx[torch.as_tensor(a + r).cuda()], ref, f"grouped dgrad, expert {e}")
+
+
+@pytest.mark.parametrize("K", [256, 384])
+def test_grouped_dgrad_ragged_and_empty_experts(jet, K):
+    off = [0, 5, 5, 133, 300, 300, 301, 556, 700]
+    E, N = len(off) - 1, 256
+    dy = wl.grad_output(off[-1], N, seed=K, config=6)
+    w = wl.weights(E * N, K, seed=K, config=6).view(E, N, K)
+    run_grouped_dgrad(jet, dy, w, off)
+
+
+def transposed_forms(x_bf16):
+    """The oracle's 128x1 form (codes [K][M], scales [M/128][K]) of x."""
+    q, s = oracle.quant_act_1x128(bits(x_bf16))
+    return oracle.requant_128x1(q, s)
+
+
+def run_grouped_wgrad(jet, dy, x, off, rows=None, experts=None):
+    qdyT, sdyT = transposed_forms(dy)
+    qxT, sxT = transposed_forms(x)
+    off = np.asarray(off, np.int64)
+    dw = jet.gemm_fp8_wgrad_grouped(to_dev(qdyT), to_dev(sdyT), to_dev(qxT), to_dev(sxT),
+                                    torch.from_numpy(off).cuda())
+    torch.cuda.synchronize()
+    E = off.size - 1
+    assert dw.shape == (E, qdyT.shape[0], qxT.shape[0])
+    if rows is None:
+        ref = oracle.gemm_wgrad_grouped(qdyT, sdyT, qxT, sxT, off)
+        for e in range(E):
+            if off[e + 1] == off[e]:
+                assert (dw[e] == 0).all(), f"expert {e} without tokens"
+            else:
+                assert_gemm_close(dw[e], ref[e], f"grouped wgrad, expert {e}")
+        return dw
+    for e in experts:
+        a, b = int(off[e]), int(off[e + 1])
+        r = sample_rows(qdyT.shape[0], rows, seed=e)
+        ref = oracle.gemm_wgrad(np.ascontiguousarray(qdyT[:, a:b]),
+                                np.ascontiguousarray(sdyT[a // 128:b // 128]),
+                                np.ascontiguousarray(qxT[:, a:b]),
+                                np.ascontiguousarray(sxT[a // 128:b // 128]), rows=r)
+        assert_gemm_close(dw[e][torch.as_tensor(r).cuda()], ref, f"grouped wgrad, expert {e}")
+    return dw
+
+
+@pytest.mark.parametrize("N,K", [(256, 256), (384, 256), (128, 384), (512, 512)])
+def test_grouped_wgrad_padded_experts(jet, N, K):
+    # experts padded to whole 128-token groups, two of them empty
+    off = [0, 256, 256, 384, 896, 896, 1024]
+    dy = wl.grad_output(off[-1], N, seed=N + K, config=6)
+    x = wl.activations(off[-1], K, seed=N + K, config=6)
+    run_grouped_wgrad(jet, dy, x, off)
+
+
+def test_grouped_wgrad_sums_to_dense_wgrad(jet):
+    """One expert over all tokens is the plain WGrad, bit for bit."""
+    M, N, K = 512, 256, 256
+    dy, x = wl.grad_output(M, N, seed=3, config=6), wl.activations(M, K, seed=3, config=6)
+    qdyT, sdyT = (to_dev(a) for a in transposed_forms(dy))
+    qxT, sxT = (to_dev(a) for a in transposed_forms(x))
+    g = jet.gemm_fp8_wgrad_grouped(qdyT, sdyT, qxT, sxT, torch.tensor([0, M], device="cuda"))
+    d = jet.gemm_fp8_wgrad(qdyT, sdyT, qxT, sxT)
+    assert torch.equal(g[0].view(torch.int16), d.view(torch.int16))
+
+
+def test_grouped_backward_empty_cases(jet):
+    # no tokens at all: WGrad writes zeros for every expert
+    z8 = torch.empty((256, 0), dtype=torch.uint8, device="cuda")
+    zs = torch.empty((0, 256), dtype=torch.float32, device="cuda")
+    dw = torch.full((2, 256, 256), 3.0, dtype=torch.bfloat16, device="cuda")
+    jet.jet_gemm_fp8_wgrad_grouped(z8, zs, z8, zs, torch.zeros(3, dtype=torch.int64, device="cuda"), dw)
+    assert (dw == 0).all()
+
+
+def test_grouped_backward_moe_layer_sampled(jet):
+    """gate_up backward of the Qwen3-30B-A3B-shaped layer at full size: DGrad
+    on the routed rows, WGrad on the rows padded to whole token groups."""
+    off, lins = wl.moe_layer()
+    _, x, w = lins[0]
+    E, N, K = w.shape
+    off = off.numpy()
+    counts = off[1:] - off[:-1]
+    experts = sorted({int(counts.argmin()), int(counts.argmax()), 0, 77})
+    dy = wl.grad_output(int(off[-1]), N, seed=0, config=6, tensor_id=210)
+    run_grouped_dgrad(jet, dy, w, off, rows_per_expert=4, experts=experts)
+    o = torch.from_numpy(off)
+    pad = wl.moe_pad_offsets(o)
+    run_grouped_wgrad(jet, wl.moe_scatter_padded(dy, o, pad), wl.moe_scatter_padded(x, o, pad),
+                      pad.numpy(), rows=4, experts=experts)
