@@ -667,9 +667,31 @@ def make_graphs(calls, steps, torch, detail):
     return g_step, g_fam, g_detail, ev
 
 
+def bind_to_gpu_numa_node(torch, device):
+    """Restrict this process to the host CPUs that sysfs lists as local to
+    the GPU (so that pinned buffers are first touched, hence placed, in that
+    node's memory).  Returns the CPU list, or None if sysfs has none."""
+    try:
+        p = torch.cuda.get_device_properties(device)
+        bdf = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bdf}/local_cpulist") as f:
+            text = f.read().strip()
+        cpus = set()
+        for part in text.split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        if not cpus or len(cpus) >= (os.cpu_count() or 1):
+            return None  # nothing to restrict
+        os.sched_setaffinity(0, cpus)
+        return text
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
 def run_e2e(args, step_a, step_b, world, device, unit, amount, scale, torch, barrier):
     """End-to-end rate through the C-ABI calls with pinned host buffers."""
     insts = [step_a, step_b]
+    host_cpus = bind_to_gpu_numa_node(torch, device)
     h2d = d2h = 0
     for st in insts:
         h2d, d2h = st.host_io()
@@ -714,6 +736,8 @@ def run_e2e(args, step_a, step_b, world, device, unit, amount, scale, torch, bar
     e_ms = max_over_ranks(e0.elapsed_time(e1) / n, world, device)
     return {"value": round(job_rate(world, amount, e_ms, scale), 2), "unit": unit,
             "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "host_copy_gbs": round((h2d + d2h) / (e_ms * 1e-3) / 1e9, 1),
+            "host_cpus": host_cpus,
             "steps": n, "pipelining": "2 buffer sets; copy-in, compute and copy-out streams"}
 
 
