@@ -87,6 +87,8 @@ def _load():
         lib.jo_silu_f32.argtypes = [ctypes.c_float]
         lib.jo_silu_f32.restype = ctypes.c_float
         lib.jo_swiglu_quant_1x128.argtypes = [P, P, I, I, I, P, P, I, I]
+        lib.jo_kv_calibrate.argtypes = [P, I, I, I, P]
+        lib.jo_kv_cache_write.argtypes = [P, P, P, I, I, I, P, I]
         for f in (lib.jo_gemm_fwd, lib.jo_gemm_dgrad, lib.jo_gemm_wgrad):
             f.argtypes = [P, P, P, P, I, I, I, P, I, I, P]
             f.restype = None
@@ -403,3 +405,33 @@ def token_mismatch_masked(logp_train, logp_rollout, mask=None, cap: float = 0.0)
     metric = _load().jo_token_mismatch_masked(_ptr(a), _ptr(b), None if m is None else _ptr(m),
                                               a.size, float(cap), _ptr(w), ctypes.byref(count))
     return float(metric), int(count.value), w
+
+
+# --------------------------------------------------------------------------
+# FP8 KV cache, scales recalibrated after each model update
+# --------------------------------------------------------------------------
+
+def kv_calibrate(x_bits):
+    """Per-head scales s_h = amax_h / 448 (1 if amax_h = 0) of x [T, H, D]
+    (BF16 bits): the calibration after a model update."""
+    x = _as_bf16_bits(x_bits)
+    T, H, D = x.shape
+    s = np.empty(H, np.float32)
+    _load().jo_kv_calibrate(_ptr(x), T, H, D, _ptr(s))
+    return s
+
+
+def kv_cache_write(x_bits, scale, slots, cache):
+    """Write the new entries x [T, H, D] (BF16 bits) into ``cache`` [S, H, D]
+    (uint8, modified in place) at rows ``slots`` [T] as E4(fl32(x / s_h));
+    slots outside [0, S) are skipped.  Returns ``cache``."""
+    x = _as_bf16_bits(x_bits)
+    T, H, D = x.shape
+    scale = np.ascontiguousarray(scale, np.float32)
+    slots = np.ascontiguousarray(slots, np.int64)
+    if not (cache.flags["C_CONTIGUOUS"] and cache.dtype == np.uint8):
+        raise TypeError("cache must be a C-contiguous uint8 array")
+    S = cache.shape[0]
+    assert cache.shape == (S, H, D) and scale.shape == (H,) and slots.shape == (T,)
+    _load().jo_kv_cache_write(_ptr(x), _ptr(scale), _ptr(slots), T, H, D, _ptr(cache), S)
+    return cache

@@ -436,3 +436,48 @@ double jo_token_mismatch_masked(const float *a, const float *b, const uint8_t *m
     *count = c;
     return c > 0 ? sum / (double)c : NAN;
 }
+
+/* ------------------------------------------------------------------------ */
+/* FP8 KV cache with the scales recalibrated after each model update         */
+/* ------------------------------------------------------------------------ */
+/* The FP8-RL article extends the compressed format to the KV cache: the
+ * scale factors are calibrated again after every model update and the cache
+ * entries are stored compressed with them ("FP8-RL" article (m.66260.cn), the
+ * KV-cache paragraph; the nmedialink page, "FP8探索新维度：KV缓存与注意力机制赋能").
+ * They give no granularity.  Reading: one binary32 scale per KV head (for K
+ * and for V separately), s_h = amax_h / 448 over the calibration tokens
+ * (all tokens and all D channels of head h; s_h = 1 when amax_h = 0), the
+ * group rule's scale; entries written afterwards are E4(fl32(x / s_h)),
+ * saturating at +-448 when they exceed the calibrated range. */
+
+/* scale[h] for x[T][H][D] (BF16 bits). */
+void jo_kv_calibrate(const uint16_t *x, int64_t T, int64_t H, int64_t D, float *scale)
+{
+    for (int64_t h = 0; h < H; ++h) {
+        float amax = 0.0f;
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t d = 0; d < D; ++d) {
+                float a = fabsf(bf16_to_f32(x[(t * H + h) * D + d]));
+                if (a > amax)
+                    amax = a;
+            }
+        scale[h] = jo_group_scale(amax);
+    }
+}
+
+/* cache[slot[t]][h][d] = E4(fl32(x[t][h][d] / scale[h])) for the T new
+ * entries x[T][H][D] (BF16 bits); cache has S slots of H x D codes.  A slot
+ * outside [0, S) is skipped. */
+void jo_kv_cache_write(const uint16_t *x, const float *scale, const int64_t *slot, int64_t T,
+                       int64_t H, int64_t D, uint8_t *cache, int64_t S)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        if (slot[t] < 0 || slot[t] >= S)
+            continue;
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t d = 0; d < D; ++d) {
+                float v = bf16_to_f32(x[(t * H + h) * D + d]);
+                cache[(slot[t] * H + h) * D + d] = jo_e4m3_encode(v / scale[h]);
+            }
+    }
+}
