@@ -566,6 +566,52 @@ class MoeTrainStep:
         return nbytes(self.h_in), nbytes(self.h_out)
 
 
+class KvCacheStep:
+    """FP8 KV cache of one layer of the 8B model (8 KV heads x 128 channels)
+    after a model update: recalibrate the K and V scales on a 65536-token
+    prefill, then write its keys and values into a 131072-slot cache at
+    scattered slots."""
+
+    def __init__(self, device, seed: int = 0, T: int = 65536, H: int = 8, D: int = 128):
+        import torch
+        import fp8_block_quantized_gb300 as jet
+
+        self.jet, self.M = jet, T
+        g = torch.Generator(device="cpu").manual_seed(seed + 7000)
+        mk = lambda: (torch.randn((T, H, D), generator=g)
+                      * torch.exp2(torch.rand((1, H, 1), generator=g) * 6 - 3)).to(torch.bfloat16)
+        self.k, self.v = mk().to(device), mk().to(device)
+        S = 2 * T
+        self.slots = torch.randperm(S, generator=g)[:T].to(device)
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
+        self.sk, self.sv = e((H,), torch.float32), e((H,), torch.float32)
+        self.ck, self.cv = e((S, H, D), torch.uint8), e((S, H, D), torch.uint8)
+        n = T * H * D
+        self.work = {"kv_calibrate": 2 * n * 2.0, "kv_cache_write": 2 * (n * 3.0 + 8 * T)}
+        self.bytes = sum(self.work.values())
+        self.flops = 0
+        self.launches_per_step = 6   # a calibration is two kernels
+        self.primary = ("GB/s", self.bytes)
+        self.config = {"workload": f"kvcache8b_T{T}", "tokens": T, "kv_heads": H, "head_dim": D,
+                       "cache_slots": S, "l2": "no flush: 268 MB of K/V read per step > 129 MB L2"}
+
+    def calls(self):
+        j = self.jet
+        return [("kv_calibrate", lambda: j.jet_kv_calibrate(self.k, self.sk), "k"),
+                ("kv_calibrate", lambda: j.jet_kv_calibrate(self.v, self.sv), "v"),
+                ("kv_cache_write", lambda: j.jet_kv_cache_write(self.k, self.sk, self.slots, self.ck), "k"),
+                ("kv_cache_write", lambda: j.jet_kv_cache_write(self.v, self.sv, self.slots, self.cv), "v")]
+
+    def host_io(self):
+        import torch
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        self.h_in = [(pin(t), t) for t in (self.k, self.v, self.slots)]
+        self.h_out = [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t)
+                      for t in (self.sk, self.sv, self.ck, self.cv)]
+        nbytes = lambda pairs: sum(h.numel() * h.element_size() for h, _ in pairs)
+        return nbytes(self.h_in), nbytes(self.h_out)
+
+
 class MetricStep:
     """token-mult-prob-error over n = 4,194,304 tokens, and the masked variant
     with per-token importance weights (75% of the tokens in the mask)."""
@@ -620,6 +666,8 @@ def make_step(args, device, rank):
         return MoeStep(device, seed=args.seed + rank)
     if args.workload == "moe_train":
         return MoeTrainStep(device, seed=args.seed + rank)
+    if args.workload == "kvcache":
+        return KvCacheStep(device, seed=args.seed + rank)
     return MetricStep(device, seed=args.seed + rank)
 
 
@@ -1075,11 +1123,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("jet", "reference"), default="jet")
     ap.add_argument("--workload", choices=("train8b", "train32b", "rollout", "sync", "metric", "moe",
-                                           "moe_train"),
+                                           "moe_train", "kvcache"),
                     default="train8b",
                     help="train8b (default, the benchmark's workload), train32b, or the "
                          "rollout / weight-sync / metric / MoE expert forward / MoE expert "
-                         "training configurations")
+                         "training / FP8 KV-cache configurations")
     ap.add_argument("--tokens", type=int, default=2048, help="M for --workload rollout")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")

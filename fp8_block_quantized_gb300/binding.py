@@ -23,7 +23,7 @@ STATUS = {0: "JET_OK", 1: "JET_ERR_NULL", 2: "JET_ERR_SHAPE", 3: "JET_ERR_ALIGN"
 OP = {"quant_act_1x128": 0, "quant_w_128x128": 1, "requant_128x1": 2,
       "gemm_fp8_fwd": 3, "gemm_fp8_dgrad": 4, "gemm_fp8_wgrad": 5,
       "token_mult_prob_error": 6, "quant_dual_1x128_128x1": 7, "token_mismatch_masked": 8,
-      "swiglu_quant_1x128": 9}
+      "swiglu_quant_1x128": 9, "kv_calibrate": 10, "kv_cache_write": 11}
 
 # name -> argtypes (restype is int status unless listed in _RESTYPE)
 P, I, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
@@ -35,6 +35,8 @@ SIGNATURES = {
     "jet_requant_128x1": [P, P, I, I, P, P, P],
     "jet_quant_dual_1x128_128x1": [P, I, I, P, P, P, P, P],
     "jet_swiglu_quant_1x128": [P, P, I, I, I, P, P, P],
+    "jet_kv_calibrate": [P, I, I, I, P, P],
+    "jet_kv_cache_write": [P, P, P, I, I, I, P, I, P],
     "jet_gemm_fp8_fwd": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_gemm_fp8_fwd_grouped": [P, P, P, P, P, I, I, I, I, P, P],
     "jet_gemm_fp8_dgrad_grouped": [P, P, P, P, P, I, I, I, I, P, P],
@@ -202,6 +204,37 @@ def jet_swiglu_quant_1x128(gate, up, q, s, stream=None):
     _need(s, torch.float32, (F // 128, M), "s")
     _check("jet_swiglu_quant_1x128", load().jet_swiglu_quant_1x128(
         _ptr(gate), _ptr(up), ld, M, F, _ptr(q), _ptr(s), _stream(stream)))
+
+
+def jet_kv_calibrate(x, scale, stream=None):
+    """Per-head scales of the calibration batch x [T, H, D] (BF16) into scale [H]."""
+    import torch
+    T, H, D = x.shape
+    _need(x, torch.bfloat16, (T, H, D), "x")
+    _need(scale, torch.float32, (H,), "scale")
+    _check("jet_kv_calibrate", load().jet_kv_calibrate(_ptr(x), T, H, D, _ptr(scale),
+                                                       _stream(stream)))
+
+
+def jet_kv_cache_write(x, scale, slots, cache, stream=None):
+    """Write x [T, H, D] (BF16) as E4M3 codes into cache [S, H, D] at rows slots [T]."""
+    import torch
+    T, H, D = x.shape
+    S = cache.shape[0]
+    _need(x, torch.bfloat16, (T, H, D), "x")
+    _need(scale, torch.float32, (H,), "scale")
+    _need(slots, torch.int64, (T,), "slots")
+    _need(cache, torch.uint8, (S, H, D), "cache")
+    _check("jet_kv_cache_write", load().jet_kv_cache_write(
+        _ptr(x), _ptr(scale), _ptr(slots), T, H, D, _ptr(cache), S, _stream(stream)))
+
+
+def kv_calibrate(x, stream=None):
+    """scale [H] FP32 of the calibration batch x [T, H, D]."""
+    import torch
+    scale = torch.empty((x.shape[1],), dtype=torch.float32, device=x.device)
+    jet_kv_calibrate(x, scale, stream)
+    return scale
 
 
 def _gemm(name, a, sa, b, sb, M, N, K, out, ws, stream):

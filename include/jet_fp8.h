@@ -77,7 +77,9 @@ typedef enum {
     JET_OP_TOKEN_MULT_PROB_ERROR = 6,
     JET_OP_QUANT_DUAL_1X128_128X1 = 7,
     JET_OP_TOKEN_MISMATCH_MASKED = 8,
-    JET_OP_SWIGLU_QUANT_1X128 = 9
+    JET_OP_SWIGLU_QUANT_1X128 = 9,
+    JET_OP_KV_CALIBRATE = 10,
+    JET_OP_KV_CACHE_WRITE = 11
 } jet_op;
 
 /* A cudaStream_t handle passed as an opaque pointer. */
@@ -150,6 +152,32 @@ JET_API jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M
 JET_API jet_status jet_swiglu_quant_1x128(const uint16_t *gate, const uint16_t *up, int64_t ld,
                                           int64_t M, int64_t F, uint8_t *q, float *s,
                                           jet_stream_t stream);
+
+/*
+ * FP8 KV cache, scales recalibrated after each model update.  Source: FP8-RL
+ * article (m.66260.cn), KV-cache paragraph (scale factors calibrated again
+ * after every model update); nmedialink page, section "FP8探索新维度：KV缓存与
+ * 注意力机制赋能" (FP8 KV cache).  The pages give no granularity; here one
+ * FP32 scale per KV head, for K and for V separately.
+ *
+ * jet_kv_calibrate: scale[h] = amax_h / 448 (IEEE division; 1 when the head
+ * is all zero), amax_h over all T tokens and D channels of head h of the
+ * calibration batch x [T][H][D] (BF16 bits).  Writes scale [H] FP32 (device;
+ * also used as scratch during the call).
+ *
+ * jet_kv_cache_write: cache[slots[t]][h][d] = E4(fl32(x[t][h][d] / scale[h]))
+ * for the T new entries x [T][H][D] (BF16 bits); entries beyond the
+ * calibrated range saturate to +-448.  slots [T] int64 DEVICE array of
+ * distinct cache rows; a slot outside [0, S) is skipped.  cache [S][H][D]
+ * E4M3 codes (in/out; other rows untouched).
+ *
+ * T, S >= 0; 0 <= H <= 1024; D a multiple of 16.
+ */
+JET_API jet_status jet_kv_calibrate(const uint16_t *x, int64_t T, int64_t H, int64_t D,
+                                    float *scale, jet_stream_t stream);
+JET_API jet_status jet_kv_cache_write(const uint16_t *x, const float *scale,
+                                      const int64_t *slots, int64_t T, int64_t H, int64_t D,
+                                      uint8_t *cache, int64_t S, jet_stream_t stream);
 
 /*
  * Both quantizations of one tensor from a single read: the 1x128 form of

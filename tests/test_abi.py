@@ -194,6 +194,21 @@ def test_grouped_backward_checks(lib, name):
         assert f(*args, fake(A), 8, 200, 128, 128, fake(A), None) == SHAPE
 
 
+def test_kv_cache_checks(lib):
+    cal, wr = lib.jet_kv_calibrate, lib.jet_kv_cache_write
+    assert cal(fake(A), 4, 8, 100, fake(B), None) == SHAPE       # D % 16
+    assert cal(fake(A), 4, 1025, 128, fake(B), None) == SHAPE    # too many heads
+    assert cal(fake(A), -1, 8, 128, fake(B), None) == SHAPE
+    assert cal(None, 4, 8, 128, fake(B), None) == NULL
+    assert cal(fake(A), 4, 8, 128, None, None) == NULL
+    assert cal(fake(MIS), 4, 8, 128, fake(B), None) == ALIGN
+    assert wr(fake(A), fake(B), fake(C), 4, 8, 128, None, 16, None) == NULL
+    assert wr(fake(A), fake(B), None, 4, 8, 128, fake(D), 16, None) == NULL
+    assert wr(fake(A), fake(B), fake(C), 4, 8, 128, fake(D), -1, None) == SHAPE
+    assert wr(fake(A), fake(B), fake(MIS), 4, 8, 128, fake(D), 16, None) == ALIGN
+    assert lib.jet_workspace_bytes(binding.OP["kv_cache_write"], 4, 8, 128) == 0
+
+
 def test_metric_checks(lib):
     f = lib.jet_token_mult_prob_error
     assert f(None, fake(B), 16, fake(C), fake(D), 8, None) == NULL
@@ -237,6 +252,9 @@ def test_no_device_is_reported():
                                         128, 128, fake(A), None) == DEVICE
     assert lib.jet_swiglu_quant_1x128(fake(A), fake(B), 512, 4, 256, fake(C), fake(D),
                                       None) == DEVICE
+    assert lib.jet_kv_calibrate(fake(A), 4, 8, 128, fake(B), None) == DEVICE
+    assert lib.jet_kv_cache_write(fake(A), fake(B), fake(C), 4, 8, 128, fake(D), 16,
+                                  None) == DEVICE
     for name in ("jet_gemm_fp8_dgrad_grouped", "jet_gemm_fp8_wgrad_grouped"):
         assert getattr(lib, name)(fake(A), fake(B), fake(C), fake(D), fake(A), 4, 256, 128,
                                   128, fake(A), None) == DEVICE
