@@ -997,7 +997,7 @@ def run_gpu(args):
     if args.detail:
         line["detail_ms_per_step"] = {f"{fam}/{label}": round(ms / args.steps, 4)
                                       for (fam, label), ms in detail_ms.items()}
-    if not args.no_cpu_baseline and args.workload in ("train8b", "train32b"):
+    if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, seconds=args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -1038,50 +1038,200 @@ def measured_traffic(kernel: str, workload: str):
 # CPU oracle: baseline and reference arm
 # --------------------------------------------------------------------------
 
-def cpu_sample_inputs(workload: str, seed: int = 0, tokens: int = 128):
-    """First `tokens` rows of the workload's q-projection chain (host copies)."""
+def workload_name(args) -> str:
+    """The `config.workload` string of each workload (both arms use it)."""
     from fp8_block_quantized_gb300 import workloads as wl
-    name, N, K = wl.layer_linears(workload)[0]
-    cfg = wl.CONFIG_ID[workload]
-    x = wl.activations(tokens, K, seed=seed, config=cfg, tensor_id=0)
-    w = wl.weights(N, K, seed=seed, config=cfg, tensor_id=100)
-    dy = wl.grad_output(tokens, N, seed=seed, config=cfg, tensor_id=200)
-    return (wl.bf16_bits(x), wl.bf16_bits(w), wl.bf16_bits(dy)), 3 * 2 * tokens * N * K
+    return {"train8b": "train8b_layer_M8192", "train32b": "train32b_layer_M16384",
+            "rollout": f"rollout8b_M{args.tokens}", "sync": "sync8b_32layers",
+            "metric": "metric_n4194304", "moe": f"moe_qwen3_30b_a3b_T{wl.MOE_TOKENS}",
+            "moe_train": f"moe_train_qwen3_30b_a3b_T{wl.MOE_TOKENS}",
+            "kvcache": "kvcache8b_T65536"}[args.workload]
 
 
-def cpu_sample_step(sample, nthreads):
-    """The oracle's pass over the sample: weight sync, forward, backward."""
-    import oracle
-    xb, wb, dyb = sample
-    qw, sw = oracle.quant_w_128x128(wb, nthreads=nthreads)
-    qx, sx = oracle.quant_act_1x128(xb, nthreads=nthreads)
-    oracle.gemm_fwd(qx, sx, qw, sw, nthreads=nthreads)
-    qdy, sdy = oracle.quant_act_1x128(dyb, nthreads=nthreads)
-    oracle.gemm_dgrad(qdy, sdy, qw, sw, nthreads=nthreads)
-    qxT, sxT = oracle.requant_128x1(qx, sx, nthreads=nthreads)
-    qdyT, sdyT = oracle.requant_128x1(qdy, sdy, nthreads=nthreads)
-    oracle.gemm_wgrad(qdyT, sdyT, qxT, sxT, nthreads=nthreads)
+class CpuSample:
+    """A bounded sample of a workload for the CPU oracle: `step(nthreads)`
+    runs the oracle's pass over it, `amount` is its work in the workload's
+    unit (FLOPs or bytes, the GPU arm's algorithmic count), `desc` says
+    what the sample is."""
+
+    def __init__(self, workload: str, seed: int = 0):
+        import numpy as np
+        import torch
+        from fp8_block_quantized_gb300 import workloads as wl
+        self.unit = "TFLOP/s"
+        b = wl.bf16_bits
+        if workload in ("train8b", "train32b", "rollout"):
+            kind = "train8b" if workload == "rollout" else workload
+            name, N, K = wl.layer_linears(kind)[0]
+            cfg, T = wl.CONFIG_ID[workload], 128
+            self.x = b(wl.activations(T, K, seed=seed, config=cfg, tensor_id=0))
+            self.w = b(wl.weights(N, K, seed=seed, config=cfg, tensor_id=100))
+            if workload == "rollout":
+                import oracle
+                self.qw, self.sw = oracle.quant_w_128x128(self.w)
+                self.run = self._rollout
+                self.amount = 2 * T * N * K
+                self.desc = (f"{name} projection at {T} tokens: 1x128 quantization of X and the "
+                             f"binary64 forward product (weights quantized beforehand)")
+            else:
+                self.dy = b(wl.grad_output(T, N, seed=seed, config=cfg, tensor_id=200))
+                self.run = self._train
+                self.amount = 3 * 2 * T * N * K
+                self.desc = (f"{name} projection chain (N={N}, K={K}) at {T} tokens: 128x128 "
+                             f"weight quantization, 1x128 of X and dY, 128x1 requant of both, "
+                             f"binary64 forward/dgrad/wgrad")
+        elif workload == "sync":
+            self.unit = "GB/s"
+            self.w = b(wl.weights(4096, 4096, seed=seed, config=5, tensor_id=1000))
+            self.x = b(wl.heavy_activations(128, 14336, seed=seed))
+            self.run = self._sync
+            self.amount = (4096 * 4096 * BYTES_PER_ELEM["quant_w_128x128"]
+                           + 128 * 14336 * BYTES_PER_ELEM["quant_act_1x128"])
+            self.desc = "one 4096 x 4096 weight (128x128) and 128 x 14336 activations (1x128)"
+        elif workload == "metric":
+            self.unit = "GB/s"
+            n = 262144
+            a, c = wl.logprobs(n, seed=seed)
+            self.a, self.c = a.numpy(), c.numpy()
+            g = torch.Generator().manual_seed(seed + 5000)
+            self.mask = (torch.rand(n, generator=g) < 0.75).to(torch.uint8).numpy()
+            self.run = self._metric
+            self.amount = n * (BYTES_PER_ELEM["token_mult_prob_error"]
+                               + BYTES_PER_ELEM["token_mismatch_masked"])
+            self.desc = f"n = {n} tokens: the plain and the masked metric (binary64)"
+        elif workload in ("moe", "moe_train"):
+            import oracle
+            E, T = 4, 128                      # experts, tokens per expert (whole groups)
+            (gn, Ng, Kg), (dn, Nd, Kd) = wl.MOE_LINEARS
+            cfg = wl.CONFIG_ID["moe"]
+            self.off = np.arange(0, (E + 1) * T, T, dtype=np.int64)
+            M = E * T
+            self.x = b(wl.activations(M, Kg, seed=seed, config=cfg, tensor_id=0))
+            wg = wl.weights(E * Ng, Kg, seed=seed, config=cfg, tensor_id=100)
+            wd = wl.weights(E * Nd, Kd, seed=seed, config=cfg, tensor_id=101)
+            self.wg = b(wg).reshape(E, Ng, Kg)
+            self.wd = b(wd).reshape(E, Nd, Kd)
+            self.F = Kd
+            fl = 2 * M * (Ng * Kg + Nd * Kd)
+            if workload == "moe":
+                qs = [oracle.quant_w_128x128(self.wg[e]) for e in range(E)]
+                self.qwg, self.swg = np.stack([q for q, _ in qs]), np.stack([s for _, s in qs])
+                qs = [oracle.quant_w_128x128(self.wd[e]) for e in range(E)]
+                self.qwd, self.swd = np.stack([q for q, _ in qs]), np.stack([s for _, s in qs])
+                self.run = self._moe
+                self.amount = fl
+                self.desc = (f"{E} experts x {T} tokens: 1x128 quantization, grouped gate_up, "
+                             f"SwiGLU + 1x128, grouped down (binary64 products)")
+            else:
+                self.dyd = b(wl.grad_output(M, Nd, seed=seed, config=cfg, tensor_id=210))
+                self.dyg = b(wl.grad_output(M, Ng, seed=seed, config=cfg, tensor_id=211))
+                self.run = self._moe_train
+                self.amount = 3 * fl
+                self.desc = (f"{E} experts x {T} tokens: weight quantization, forward, grouped "
+                             f"DGrad and WGrad of gate_up and down (binary64 products)")
+        elif workload == "kvcache":
+            self.unit = "GB/s"
+            T, H, D = 4096, 8, 128
+            g = torch.Generator().manual_seed(seed + 7000)
+            mk = lambda: (torch.randn((T, H, D), generator=g)
+                          * torch.exp2(torch.rand((1, H, 1), generator=g) * 6 - 3)).to(torch.bfloat16)
+            self.k, self.v = b(mk()), b(mk())
+            self.slots = torch.randperm(2 * T, generator=g)[:T].numpy()
+            self.cache = np.zeros((2 * T, H, D), np.uint8)
+            self.run = self._kv
+            n = T * H * D
+            self.amount = 2 * n * 2.0 + 2 * (n * 3.0 + 8 * T)
+            self.desc = f"{T} tokens x {H} heads x {D}: calibration and cache write of K and V"
+        else:
+            raise ValueError(workload)
+
+    def _train(self, nt):
+        import oracle
+        qw, sw = oracle.quant_w_128x128(self.w, nthreads=nt)
+        qx, sx = oracle.quant_act_1x128(self.x, nthreads=nt)
+        oracle.gemm_fwd(qx, sx, qw, sw, nthreads=nt)
+        qdy, sdy = oracle.quant_act_1x128(self.dy, nthreads=nt)
+        oracle.gemm_dgrad(qdy, sdy, qw, sw, nthreads=nt)
+        qxT, sxT = oracle.requant_128x1(qx, sx, nthreads=nt)
+        qdyT, sdyT = oracle.requant_128x1(qdy, sdy, nthreads=nt)
+        oracle.gemm_wgrad(qdyT, sdyT, qxT, sxT, nthreads=nt)
+
+    def _rollout(self, nt):
+        import oracle
+        qx, sx = oracle.quant_act_1x128(self.x, nthreads=nt)
+        oracle.gemm_fwd(qx, sx, self.qw, self.sw, nthreads=nt)
+
+    def _sync(self, nt):
+        import oracle
+        oracle.quant_w_128x128(self.w, nthreads=nt)
+        oracle.quant_act_1x128(self.x, nthreads=nt)
+
+    def _metric(self, nt):
+        import oracle
+        oracle.token_mult_prob_error(self.a, self.c)
+        oracle.token_mismatch_masked(self.a, self.c, self.mask)
+
+    def _moe_forward(self, qwg, swg, qwd, swd, nt):
+        import numpy as np
+        import oracle
+        from fp8_block_quantized_gb300.workloads import bf16_bits as wl_bf16
+        qx, sx = oracle.quant_act_1x128(self.x, nthreads=nt)
+        y = oracle.gemm_fwd_grouped(qx, sx, qwg, swg, self.off, nthreads=nt)
+        import torch
+        yb = wl_bf16(torch.from_numpy(y.astype(np.float32)).to(torch.bfloat16))
+        F = self.F
+        qh, sh = oracle.swiglu_quant_1x128(np.ascontiguousarray(yb[:, :F]),
+                                           np.ascontiguousarray(yb[:, F:]), nthreads=nt)
+        oracle.gemm_fwd_grouped(qh, sh, qwd, swd, self.off, nthreads=nt)
+        return qx, sx, qh, sh
+
+    def _moe(self, nt):
+        self._moe_forward(self.qwg, self.swg, self.qwd, self.swd, nt)
+
+    def _moe_train(self, nt):
+        import numpy as np
+        import oracle
+        E = self.wg.shape[0]
+        qs = [oracle.quant_w_128x128(self.wg[e], nthreads=nt) for e in range(E)]
+        qwg, swg = np.stack([q for q, _ in qs]), np.stack([s for _, s in qs])
+        qs = [oracle.quant_w_128x128(self.wd[e], nthreads=nt) for e in range(E)]
+        qwd, swd = np.stack([q for q, _ in qs]), np.stack([s for _, s in qs])
+        qx, sx, qh, sh = self._moe_forward(qwg, swg, qwd, swd, nt)
+        for dy, qw, sw, qa, sa in ((self.dyd, qwd, swd, qh, sh), (self.dyg, qwg, swg, qx, sx)):
+            qdy, sdy = oracle.quant_act_1x128(dy, nthreads=nt)
+            oracle.gemm_dgrad_grouped(qdy, sdy, qw, sw, self.off, nthreads=nt)
+            qdyT, sdyT = oracle.requant_128x1(qdy, sdy, nthreads=nt)
+            qaT, saT = oracle.requant_128x1(qa, sa, nthreads=nt)
+            oracle.gemm_wgrad_grouped(qdyT, sdyT, qaT, saT, self.off, nthreads=nt)
+
+    def _kv(self, nt):
+        import oracle
+        for x in (self.k, self.v):
+            s = oracle.kv_calibrate(x)
+            oracle.kv_cache_write(x, s, self.slots, self.cache)
+
+    def step(self, nthreads):
+        self.run(nthreads)
+
+    def rate(self, reps, seconds):
+        return reps * self.amount / seconds / (1e12 if self.unit == "TFLOP/s" else 1e9)
 
 
 def cpu_baseline(workload: str, seconds: float = 12.0):
     import oracle
     oracle.build()
     nthreads = os.cpu_count() or 1
-    sample, flops = cpu_sample_inputs(workload)
+    smp = CpuSample(workload)
     reps, t0 = 0, time.perf_counter()
     while True:
-        cpu_sample_step(sample, nthreads)
+        smp.step(nthreads)
         reps += 1
         el = time.perf_counter() - t0
-        if el >= seconds or reps >= 50:
+        if el >= seconds or reps >= 200:
             break
-    from fp8_block_quantized_gb300 import workloads as wl
-    name, N, K = wl.layer_linears(workload)[0]
-    return {"value": round(reps * flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": nthreads,
+    return {"value": round(smp.rate(reps, el), 6), "unit": smp.unit, "cores": nthreads,
             "kind": "oracle", "seconds": round(el, 2), "reps": reps,
-            "sample": f"{name} projection chain (N={N}, K={K}) at 128 tokens: 128x128 weight "
-                      f"quantization, 1x128 of X and dY, 128x1 requant of both, binary64 "
-                      f"forward/dgrad/wgrad; {reps} passes"}
+            "sample": f"{smp.desc}; {reps} passes"}
 
 
 def run_reference(args):
@@ -1091,27 +1241,24 @@ def run_reference(args):
     import oracle
     oracle.build()
     nthreads = os.cpu_count() or 1
-    sample, flops = cpu_sample_inputs(args.workload)
+    smp = CpuSample(args.workload, seed=args.seed)
     for _ in range(args.warmup):
-        cpu_sample_step(sample, nthreads)
+        smp.step(nthreads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        cpu_sample_step(sample, nthreads)
+        smp.step(nthreads)
     el = time.perf_counter() - t0
-    value = args.steps * flops / el / 1e12
-    from fp8_block_quantized_gb300 import workloads as wl
-    name, N, K = wl.layer_linears(args.workload)[0]
-    sample_desc = (f"{name} projection chain (N={N}, K={K}) at 128 tokens per step: the oracle's "
-                   f"weight quantization, 1x128/128x1 quantization and binary64 GEMMs")
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+    value = smp.rate(args.steps, el)
+    sample_desc = f"{smp.desc}, one pass per step"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": smp.unit,
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{args.workload}_layer (CPU sample)", "tokens": 128},
-            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": nthreads,
+            "config": {"workload": workload_name(args), "sample": sample_desc},
+            "cpu_baseline": {"value": round(value, 6), "unit": smp.unit, "cores": nthreads,
                              "kind": "oracle", "sample": sample_desc},
-            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+            "e2e": {"value": round(value, 6), "unit": smp.unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
