@@ -21,6 +21,7 @@
 #include <cuda_bf16.h>
 
 #include "jet_common.cuh"
+#include "stream_ld.cuh"
 
 namespace {
 
@@ -30,14 +31,6 @@ constexpr int kGemvThreads = 256;
 // the converted token codes need the registers)
 template <int MT>
 constexpr int gemv_ctas_per_sm() { return MT <= 2 ? 2 : 1; }
-
-__device__ __forceinline__ uint4 ld_stream16(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 // Four E4M3 codes -> two f16x2 words (exact), lowest code in the low half.
 __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t four, uint32_t &lo, uint32_t &hi) {

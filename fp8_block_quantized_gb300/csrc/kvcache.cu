@@ -16,6 +16,7 @@
 // head's scale with the group rule's correctly rounded division.  Both are
 // bound by HBM.
 #include "jet_common.cuh"
+#include "stream_ld.cuh"
 #include "quant_rule.cuh"
 
 namespace {
@@ -23,14 +24,6 @@ namespace {
 constexpr int kKvThreads = 256;
 constexpr int kKvCtasPerSm = 4;
 constexpr int64_t kKvMaxHeads = 1024;
-
-__device__ __forceinline__ uint4 ld_stream16(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 // max(|x|) of eight BF16 values, as a bit pattern (non-negative float)
 __device__ __forceinline__ uint32_t amax8_bits(const uint4 &v) {

@@ -31,20 +31,13 @@
 #include <cuda_bf16.h>
 
 #include "jet_common.cuh"
+#include "stream_ld.cuh"
 #include "quant_rule.cuh"
 
 namespace {
 
 constexpr int kSwThreads = 256;
 constexpr int kSwCtasPerSm = 4;
-__device__ __forceinline__ uint4 ld_stream16(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
 // e^x for two arguments in [-87, 80], packed f32x2 arithmetic.  There
