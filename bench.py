@@ -99,6 +99,8 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        import threading
+        self.lines = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
@@ -106,23 +108,44 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+
+        def read():
+            for l in self.proc.stdout:
+                if l.strip():
+                    self.lines.append(l)
+        self.reader = threading.Thread(target=read, daemon=True)
+        self.reader.start()
         return self
 
+    def wait_first(self, timeout: float = 5.0):
+        """Block until the sampler has produced a line (it takes a moment to
+        start), so that samples cover the region that follows."""
+        t0 = time.perf_counter()
+        while self.proc is not None and not self.lines and time.perf_counter() - t0 < timeout:
+            time.sleep(0.01)
+
+    def count(self):
+        return len(self.lines)
+
+    def mark(self):
+        """Only samples taken from now on enter the summary."""
+        self.start = len(self.lines)
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                self.proc.wait()
+            self.reader.join(timeout=5)
 
     def summary(self):
         sm, smax, reasons = [], None, set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for l in getattr(self, "lines", []):
+        for l in self.lines[getattr(self, "start", 0):]:
             p = [x.strip() for x in l.split(",")]
             if len(p) < 9:
                 continue
@@ -845,16 +868,26 @@ def run_gpu(args):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     with ClockSampler(local) as clk:
+        clk.wait_first()
         if graphs is not None:
             g_step.replay()          # one untimed replay: graph upload
             for g in g_fam.values():
                 g.replay()
             barrier()
+            clk.mark()
             t0.record(stream)
             for k in range(args.steps):
                 g_step.replay()
             t1.record(stream)
             barrier()
+            # A timed region shorter than a few sampling periods is followed
+            # by untimed replays of the same step, so that the clock samples
+            # describe the GPU under this load.
+            n0, tw = clk.count(), time.perf_counter()
+            while clk.count() - n0 < 3 and time.perf_counter() - tw < 2.0:
+                for k in range(args.steps):
+                    g_step.replay()
+                barrier()
             for fam, g in g_fam.items():
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -872,6 +905,7 @@ def run_gpu(args):
                 g_detail.replay()
             barrier()
         else:
+            clk.mark()
             t0.record(stream)
             for k in range(args.steps):
                 for (fam, f, _), (a, b) in zip(calls, ev[k]):
