@@ -209,6 +209,20 @@ def test_kv_cache_checks(lib):
     assert lib.jet_workspace_bytes(binding.OP["kv_cache_write"], 4, 8, 128) == 0
 
 
+def test_size_limits(lib):
+    """Sizes past the documented limits are refused before anything runs."""
+    big = 1 << 31
+    assert lib.jet_quant_act_1x128(fake(A), big, 128, fake(B), fake(C), None) == SHAPE
+    assert lib.jet_quant_w_128x128(fake(A), 128, big, fake(B), fake(C), None) == SHAPE
+    g = lib.jet_gemm_fp8_fwd
+    assert g(fake(A), fake(B), fake(C), fake(D), 1 << 30, 128, 128, fake(A), None, 0, None) == SHAPE
+    assert g(fake(A), fake(B), fake(C), fake(D), 128, 1 << 30, 128, fake(A), None, 0, None) == SHAPE
+    assert lib.jet_swiglu_quant_1x128(fake(A), fake(B), 256, big, 256, fake(C), fake(D),
+                                      None) == SHAPE
+    assert lib.jet_kv_cache_write(fake(A), fake(B), fake(C), 4, 1024, 1 << 20, fake(D), 16,
+                                  None) == SHAPE
+
+
 def test_metric_checks(lib):
     f = lib.jet_token_mult_prob_error
     assert f(None, fake(B), 16, fake(C), fake(D), 8, None) == NULL

@@ -77,6 +77,14 @@ def test_act_train8b_full_sampled_rows(jet):
     check_act(jet, x, rows)
 
 
+def test_act_sync_heavy_activation_full_sampled_rows(jet):
+    """The weight-sync sweep's 16384 x 14336 Student-t(3) activation matrix."""
+    x = wl.heavy_activations(16384, 14336, seed=0)
+    rows = np.sort(np.random.default_rng(3).choice(16384, 1024, replace=False))
+    rows[0], rows[-1] = 0, 16383
+    check_act(jet, x, rows)
+
+
 def test_act_heavy_tailed_gradients(jet):
     dy = wl.grad_output(8192, 1024, seed=0, config=3, tensor_id=201)
     check_act(jet, dy)

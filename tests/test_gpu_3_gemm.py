@@ -214,6 +214,23 @@ def test_train32b_kv_proj_wgrad(jet):
               wl.activations(M, K, seed=0, config=4), nrows=8)
 
 
+def test_train8b_down_proj_fwd_dgrad_wgrad(jet):
+    """The widest contraction of the 8B layer (K = 14336) in all three products."""
+    layer = wl.training_layer("train8b")
+    d = layer[6]
+    assert (d.name, d.M, d.N, d.K) == ("down", 8192, 4096, 14336)
+    run_fwd(jet, d.x, d.w, nrows=16)
+    run_dgrad(jet, d.dy, d.w, nrows=16)
+    run_wgrad(jet, d.dy, d.x, nrows=8)
+
+
+def test_train32b_gate_proj_fwd(jet):
+    """The widest output of the 32B layer (N = 25600) at M = 16384."""
+    M, N, K = 16384, 25600, 5120
+    run_fwd(jet, wl.activations(M, K, seed=0, config=4, tensor_id=2),
+            wl.weights(N, K, seed=0, config=4, tensor_id=104), nrows=8)
+
+
 # ------------------------------------------ grouped forward (expert linears) --
 
 def quant_experts(x, w):
