@@ -759,10 +759,41 @@ def bind_to_gpu_numa_node(torch, device):
         return None
 
 
+def gpu_numa_node(torch, device):
+    """The GPU's NUMA node as sysfs lists it, or None."""
+    try:
+        p = torch.cuda.get_device_properties(device)
+        bdf = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bdf}/numa_node") as f:
+            return int(f.read().strip())
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
+def host_link_gbs(torch, device, nbytes=1 << 30):
+    """Plain pinned-host <-> device copy rates (GB/s), one direction at a time:
+    what bounds the end-to-end leg."""
+    h = torch.empty((nbytes,), dtype=torch.uint8, pin_memory=True)
+    d = torch.empty((nbytes,), dtype=torch.uint8, device=device)
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        dst.copy_(src, non_blocking=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        out[name] = round(3 * nbytes / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
+    del h, d
+    return out
+
+
 def run_e2e(args, step_a, step_b, world, device, unit, amount, scale, torch, barrier):
     """End-to-end rate through the C-ABI calls with pinned host buffers."""
     insts = [step_a, step_b]
     host_cpus = bind_to_gpu_numa_node(torch, device)
+    link = host_link_gbs(torch, device)
     h2d = d2h = 0
     for st in insts:
         h2d, d2h = st.host_io()
@@ -808,7 +839,8 @@ def run_e2e(args, step_a, step_b, world, device, unit, amount, scale, torch, bar
     return {"value": round(job_rate(world, amount, e_ms, scale), 2), "unit": unit,
             "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "host_copy_gbs": round((h2d + d2h) / (e_ms * 1e-3) / 1e9, 1),
-            "host_cpus": host_cpus,
+            "host_link_gbs": link, "host_cpus": host_cpus,
+            "gpu_numa_node": gpu_numa_node(torch, device),
             "steps": n, "pipelining": "2 buffer sets; copy-in, compute and copy-out streams"}
 
 
