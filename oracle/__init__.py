@@ -407,6 +407,29 @@ def token_mismatch_masked(logp_train, logp_rollout, mask=None, cap: float = 0.0)
     return float(metric), int(count.value), w
 
 
+def token_mismatch_per_sequence(logp_train, logp_rollout, seq_offsets, mask=None,
+                                cap: float = 0.0):
+    """(metrics [S], counts [S], w [n]): the masked token-mult-prob-error of
+    every sequence s (tokens seq_offsets[s] .. seq_offsets[s+1]), its number
+    of masked tokens, and the per-token importance weights, binary64.  Each
+    sequence's figures are token_mismatch_masked over that sequence alone."""
+    a = np.ascontiguousarray(logp_train, np.float32).reshape(-1)
+    b = np.ascontiguousarray(logp_rollout, np.float32).reshape(-1)
+    off = np.asarray(seq_offsets, np.int64)
+    if off[0] != 0 or off[-1] != a.size or (np.diff(off) < 0).any():
+        raise ValueError("offsets must run from 0 to n, non-decreasing")
+    S = off.size - 1
+    m = None if mask is None else np.ascontiguousarray(mask, np.uint8).reshape(-1)
+    metrics = np.empty(S, np.float64)
+    counts = np.empty(S, np.int64)
+    w = np.empty(a.size, np.float64)
+    for s in range(S):
+        lo, hi = int(off[s]), int(off[s + 1])
+        r, c, ws = token_mismatch_masked(a[lo:hi], b[lo:hi], None if m is None else m[lo:hi], cap)
+        metrics[s], counts[s], w[lo:hi] = r, c, ws
+    return metrics, counts, w
+
+
 # --------------------------------------------------------------------------
 # FP8 KV cache, scales recalibrated after each model update
 # --------------------------------------------------------------------------

@@ -113,3 +113,33 @@ def test_masked_metric_subset_and_empty():
     assert abs(m - direct) <= 1e-14 * direct
     m0, c0, w0 = oracle.token_mismatch_masked(a, b, np.zeros(1000, np.uint8))
     assert c0 == 0 and math.isnan(m0) and (w0 == 0).all()
+
+
+def test_per_sequence_metric_pins():
+    """Per-sequence metrics: one sequence is the masked metric over all
+    tokens; the count-weighted mean of the sequences' metrics is that metric;
+    a constant gap d in a sequence gives e^|d|; an empty or fully masked-out
+    sequence gives NaN with count 0."""
+    rng = np.random.default_rng(9)
+    lens = np.array([5, 0, 130, 1, 64, 17])
+    off = np.concatenate([[0], np.cumsum(lens)])
+    n = int(off[-1])
+    b = np.log(rng.uniform(1e-4, 1, n)).astype(np.float32)
+    a = (b + rng.normal(0, 0.05, n)).astype(np.float32)
+    mask = (rng.uniform(size=n) < 0.7).astype(np.uint8)
+    mask[off[4]:off[5]] = 0                       # sequence 4 fully masked out
+    r, c, w = oracle.token_mismatch_per_sequence(a, b, off, mask, cap=2.0)
+    whole, count, w_all = oracle.token_mismatch_masked(a, b, mask, cap=2.0)
+    assert np.array_equal(w, w_all)
+    ok = c > 0
+    assert np.isclose((r[ok] * c[ok]).sum() / c.sum(), whole, rtol=1e-14)
+    assert c.sum() == count and c[1] == 0 and c[4] == 0
+    assert np.isnan(r[1]) and np.isnan(r[4])
+    one, cnt1, _ = oracle.token_mismatch_per_sequence(a, b, np.array([0, n]), mask, cap=2.0)
+    assert one[0] == whole and cnt1[0] == count
+    d = np.float32(0.25)
+    bb = np.zeros(10, np.float32) - 3.0
+    aa = bb + d
+    rr, cc, _ = oracle.token_mismatch_per_sequence(aa, bb, np.array([0, 4, 10]))
+    dd = float(np.float64(aa[0]) - np.float64(bb[0]))
+    assert np.allclose(rr, [np.exp(abs(dd))] * 2, rtol=1e-15) and cc.tolist() == [4, 6]
