@@ -636,8 +636,9 @@ class KvCacheStep:
 
 
 class MetricStep:
-    """token-mult-prob-error over n = 4,194,304 tokens, and the masked variant
-    with per-token importance weights (75% of the tokens in the mask)."""
+    """token-mult-prob-error over n = 4,194,304 tokens, the masked variant
+    with per-token importance weights (75% of the tokens in the mask), and the
+    per-sequence variant over 2048 sequences of log-normal lengths."""
 
     def __init__(self, device, seed: int = 0, n: int = 4_194_304):
         import torch
@@ -656,16 +657,30 @@ class MetricStep:
         self.mcount = torch.empty((1,), dtype=torch.int64, device=device)
         self.mws = torch.empty((max(jet.workspace_bytes("token_mismatch_masked", n), 16),),
                                dtype=torch.uint8, device=device)
+        # per sequence: 2048 sequences of log-normal lengths over the same tokens
+        rng = torch.Generator().manual_seed(seed + 6000)
+        lens = torch.exp(torch.randn(2048, generator=rng, dtype=torch.float64) * 0.8 + 7.3)
+        lens = (lens * (n / lens.sum())).floor().clamp(min=1).to(torch.int64)
+        lens[-1] += n - int(lens.sum())
+        self.seq_off = torch.zeros((2049,), dtype=torch.int64)
+        self.seq_off[1:] = torch.cumsum(lens, 0)
+        self.seq_off = self.seq_off.to(device)
+        self.S = 2048
+        self.sout = torch.empty((self.S,), dtype=torch.float32, device=device)
+        self.scount = torch.empty((self.S,), dtype=torch.int64, device=device)
+        self.sw = torch.empty((n,), dtype=torch.float32, device=device)
         # an L2-sized scratch written before each call so that its inputs are
         # read from HBM every step
         self.flush = torch.empty((256 << 20,), dtype=torch.uint8, device=device)
         self.work = {"token_mult_prob_error": n * BYTES_PER_ELEM["token_mult_prob_error"],
-                     "token_mismatch_masked": n * BYTES_PER_ELEM["token_mismatch_masked"]}
+                     "token_mismatch_masked": n * BYTES_PER_ELEM["token_mismatch_masked"],
+                     "token_mismatch_per_sequence": n * BYTES_PER_ELEM["token_mismatch_masked"]}
         self.bytes = sum(self.work.values())
         self.flops = 0
-        self.launches_per_step = 4
+        self.launches_per_step = 5
         self.primary = ("GB/s", self.bytes)
         self.config = {"workload": f"metric_n{n}", "tokens": n, "masked_fraction": 0.75,
+                       "sequences": self.S,
                        "l2": "flushed: 256 MB written before each call, outside the kernels' events"}
 
     def calls(self):
@@ -675,7 +690,11 @@ class MetricStep:
                     self.a, self.b, self.out, self.ws), "n"),
                 ("l2_flush", lambda: self.flush.fill_(1), "flush"),
                 ("token_mismatch_masked", lambda: j.jet_token_mismatch_masked(
-                    self.a, self.b, self.mask, 0.0, self.w, self.mout, self.mcount, self.mws), "n")]
+                    self.a, self.b, self.mask, 0.0, self.w, self.mout, self.mcount, self.mws), "n"),
+                ("l2_flush", lambda: self.flush.fill_(1), "flush"),
+                ("token_mismatch_per_sequence", lambda: j.jet_token_mismatch_per_sequence(
+                    self.a, self.b, self.mask, self.seq_off, 0.0, self.sw, self.sout,
+                    self.scount), "S2048")]
 
 
 def make_step(args, device, rank):

@@ -23,7 +23,8 @@ STATUS = {0: "JET_OK", 1: "JET_ERR_NULL", 2: "JET_ERR_SHAPE", 3: "JET_ERR_ALIGN"
 OP = {"quant_act_1x128": 0, "quant_w_128x128": 1, "requant_128x1": 2,
       "gemm_fp8_fwd": 3, "gemm_fp8_dgrad": 4, "gemm_fp8_wgrad": 5,
       "token_mult_prob_error": 6, "quant_dual_1x128_128x1": 7, "token_mismatch_masked": 8,
-      "swiglu_quant_1x128": 9, "kv_calibrate": 10, "kv_cache_write": 11}
+      "swiglu_quant_1x128": 9, "kv_calibrate": 10, "kv_cache_write": 11,
+      "token_mismatch_per_sequence": 12}
 
 # name -> argtypes (restype is int status unless listed in _RESTYPE)
 P, I, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
@@ -36,6 +37,7 @@ SIGNATURES = {
     "jet_quant_dual_1x128_128x1": [P, I, I, P, P, P, P, P],
     "jet_swiglu_quant_1x128": [P, P, I, I, I, P, P, P],
     "jet_kv_calibrate": [P, I, I, I, P, P],
+    "jet_token_mismatch_per_sequence": [P, P, P, P, I, I, ctypes.c_float, P, P, P, P],
     "jet_kv_cache_write": [P, P, P, I, I, I, P, I, P],
     "jet_gemm_fp8_fwd": [P, P, P, P, I, I, I, P, P, Z, P],
     "jet_gemm_fp8_fwd_grouped": [P, P, P, P, P, I, I, I, I, P, P],
@@ -227,6 +229,40 @@ def jet_kv_cache_write(x, scale, slots, cache, stream=None):
     _need(cache, torch.uint8, (S, H, D), "cache")
     _check("jet_kv_cache_write", load().jet_kv_cache_write(
         _ptr(x), _ptr(scale), _ptr(slots), T, H, D, _ptr(cache), S, _stream(stream)))
+
+
+def jet_token_mismatch_per_sequence(logp_train, logp_rollout, mask, seq_offsets, cap, w, out,
+                                    count, stream=None):
+    """Per-sequence mismatch metric and importance weights (see the header)."""
+    import torch
+    n = logp_train.numel()
+    S = seq_offsets.numel() - 1
+    _need(logp_train, torch.float32, (n,), "logp_train")
+    _need(logp_rollout, torch.float32, (n,), "logp_rollout")
+    if mask is not None:
+        _need(mask, torch.uint8, (n,), "mask")
+    _need(seq_offsets, torch.int64, (S + 1,), "seq_offsets")
+    if w is not None:
+        _need(w, torch.float32, (n,), "w")
+    _need(out, torch.float32, (S,), "out")
+    if count is not None:
+        _need(count, torch.int64, (S,), "count")
+    _check("jet_token_mismatch_per_sequence", load().jet_token_mismatch_per_sequence(
+        _ptr(logp_train), _ptr(logp_rollout), _ptr(mask), _ptr(seq_offsets), S, n,
+        float(cap), _ptr(w), _ptr(out), _ptr(count), _stream(stream)))
+
+
+def token_mismatch_per_sequence(logp_train, logp_rollout, seq_offsets, mask=None, cap=0.0,
+                                stream=None):
+    """(metric [S], count [S], w [n]) on the device."""
+    import torch
+    n, S, dev = logp_train.numel(), seq_offsets.numel() - 1, logp_train.device
+    out = torch.empty((S,), dtype=torch.float32, device=dev)
+    count = torch.empty((S,), dtype=torch.int64, device=dev)
+    w = torch.empty((n,), dtype=torch.float32, device=dev)
+    jet_token_mismatch_per_sequence(logp_train, logp_rollout, mask, seq_offsets, cap, w, out,
+                                    count, stream)
+    return out, count, w
 
 
 def kv_calibrate(x, stream=None):

@@ -248,6 +248,83 @@ tmm_final_kernel(const double *__restrict__ partial, int nblocks, float *out, in
 
 }  // namespace
 
+namespace {
+
+// Per-sequence variant: one block per sequence (grid-stride over sequences,
+// so that a long sequence is streamed by 256 threads rather than one warp),
+// threads striding over the sequence's tokens four at a time (all loads of a
+// step issued before use); exp|a-b| of a step's four tokens summed in FP32,
+// the steps in FP64; the block's sums combined in a fixed order
+// (deterministic).
+constexpr int kSeqUnroll = 4;
+
+__global__ void __launch_bounds__(kThreads)
+tms_kernel(const float *__restrict__ a, const float *__restrict__ b,
+           const uint8_t *__restrict__ mask, const int64_t *__restrict__ off, int64_t S,
+           int64_t n, float cap, float *__restrict__ w, float *__restrict__ out,
+           int64_t *__restrict__ count) {
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
+    auto clampn = [&](int64_t v) { return v < 0 ? (int64_t)0 : (v > n ? n : v); };
+    for (int64_t s = blockIdx.x; s < S; s += gridDim.x) {
+        const int64_t lo = clampn(off[s]);
+        const int64_t hi = max(lo, clampn(off[s + 1]));
+        double sum = 0.0;
+        int cnt = 0;
+        for (int64_t i0 = lo + threadIdx.x; i0 < hi; i0 += (int64_t)kThreads * kSeqUnroll) {
+            float x[kSeqUnroll], y[kSeqUnroll];
+            bool on[kSeqUnroll];
+#pragma unroll
+            for (int u = 0; u < kSeqUnroll; ++u) {
+                const int64_t i = i0 + (int64_t)kThreads * u;
+                const bool in = i < hi;
+                x[u] = in ? a[i] : 0.0f;
+                y[u] = in ? b[i] : 0.0f;
+                on[u] = in && (mask == nullptr || mask[i] != 0);
+            }
+            float part = 0.0f;
+#pragma unroll
+            for (int u = 0; u < kSeqUnroll; ++u) {
+                const int64_t i = i0 + (int64_t)kThreads * u;
+                const float d = x[u] - y[u];
+                if (w && i < hi) w[i] = on[u] ? is_weight(d, cap) : 0.0f;
+                part += on[u] ? expf(fabsf(d)) : 0.0f;
+                cnt += on[u] ? 1 : 0;
+            }
+            sum += (double)part;
+        }
+        const double t = block_sum(sum);
+        __syncthreads();  // block_sum's shared scratch is reused below
+        const double c = block_sum((double)cnt);
+        if (threadIdx.x == 0) {
+            out[s] = c > 0.0 ? (float)(t / c) : __int_as_float(0x7fc00000);
+            if (count) count[s] = (int64_t)c;
+        }
+        __syncthreads();  // before the next sequence reuses the scratch
+    }
+}
+
+}  // namespace
+
+extern "C" jet_status jet_token_mismatch_per_sequence(
+    const float *logp_train, const float *logp_rollout, const uint8_t *mask,
+    const int64_t *seq_offsets, int64_t S, int64_t n, float cap, float *w, float *out,
+    int64_t *count, jet_stream_t stream) {
+    JET_REQUIRE(S >= 1 && n >= 0, JET_ERR_SHAPE);
+    JET_REQUIRE(seq_offsets && out && (n == 0 || (logp_train && logp_rollout)), JET_ERR_NULL);
+    JET_REQUIRE(jet::aligned16(logp_train) && jet::aligned16(logp_rollout) &&
+                    jet::aligned16(mask) && jet::aligned16(seq_offsets) && jet::aligned16(w) &&
+                    jet::aligned16(out) && jet::aligned16(count),
+                JET_ERR_ALIGN);
+    jet::DeviceInfo dev;
+    jet_status st = jet::current_device(&dev);
+    if (st != JET_OK) return st;
+    const int64_t cap_blocks = (int64_t)dev.num_sms * 8;
+    return jet::launch_pdl(tms_kernel, dim3((unsigned)(S < cap_blocks ? S : cap_blocks)),
+                           dim3(kThreads), 0, jet::as_stream(stream), logp_train, logp_rollout,
+                           mask, seq_offsets, S, n, cap, w, out, count);
+}
+
 // Workspace of jet_token_mismatch_masked: a sum and a count per first-pass block.
 size_t jet_mismatch_masked_workspace(int64_t n) {
     return n > 0 ? (size_t)jet_metric_blocks(n) * 2 * sizeof(double) : 0;

@@ -79,7 +79,8 @@ typedef enum {
     JET_OP_TOKEN_MISMATCH_MASKED = 8,
     JET_OP_SWIGLU_QUANT_1X128 = 9,
     JET_OP_KV_CALIBRATE = 10,
-    JET_OP_KV_CACHE_WRITE = 11
+    JET_OP_KV_CACHE_WRITE = 11,
+    JET_OP_TOKEN_MISMATCH_PER_SEQUENCE = 12
 } jet_op;
 
 /* A cudaStream_t handle passed as an opaque pointer. */
@@ -388,6 +389,28 @@ JET_API jet_status jet_token_mismatch_masked(const float *logp_train, const floa
                                              const uint8_t *mask, int64_t n, float cap, float *w,
                                              float *out, int64_t *count, void *ws,
                                              size_t ws_bytes, jet_stream_t stream);
+
+/*
+ * Per-sequence form of jet_token_mismatch_masked, one pass: for every
+ * sequence s (tokens seq_offsets[s] .. seq_offsets[s+1]) the mean of
+ * exp|logp_train_i - logp_rollout_i| over its masked tokens, and the same
+ * per-token importance weights.  Source: nmedialink page, "FP8面临的关键挑战：
+ * 数值分歧" (the metric) and its importance-sampling paragraph; FP8-RL article
+ * (the probability ratio).  Computed as jet_token_mismatch_masked: exp in
+ * FP32 per token, sums in FP64, result FP32; deterministic.
+ *   logp_train, logp_rollout [n] FP32; mask [n] uint8 or NULL (every token).
+ *   seq_offsets [S+1] int64 DEVICE array: 0, non-decreasing, n (offsets are
+ *     clamped to [0, n]; a decreasing pair is an empty sequence).
+ *   cap: importance weights min(w, cap) when cap > 0.
+ *   w [n] FP32 or NULL (out); out [S] FP32 (out; NaN for a sequence without
+ *   masked tokens); count [S] int64 or NULL (out).  S >= 1, n >= 0.
+ */
+JET_API jet_status jet_token_mismatch_per_sequence(const float *logp_train,
+                                                   const float *logp_rollout,
+                                                   const uint8_t *mask,
+                                                   const int64_t *seq_offsets, int64_t S,
+                                                   int64_t n, float cap, float *w, float *out,
+                                                   int64_t *count, jet_stream_t stream);
 
 /*
  * Workspace bytes an operation needs for the given sizes (0 if none).

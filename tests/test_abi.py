@@ -223,6 +223,16 @@ def test_size_limits(lib):
                                   None) == SHAPE
 
 
+def test_per_sequence_metric_checks(lib):
+    f = lib.jet_token_mismatch_per_sequence
+    assert f(fake(A), fake(B), None, None, 4, 16, 0.0, None, fake(C), None, None) == NULL
+    assert f(fake(A), fake(B), None, fake(D), 4, 16, 0.0, None, None, None, None) == NULL
+    assert f(None, fake(B), None, fake(D), 4, 16, 0.0, None, fake(C), None, None) == NULL
+    assert f(fake(A), fake(B), None, fake(D), 0, 16, 0.0, None, fake(C), None, None) == SHAPE
+    assert f(fake(A), fake(B), None, fake(D), 4, -1, 0.0, None, fake(C), None, None) == SHAPE
+    assert f(fake(A), fake(B), fake(MIS), fake(D), 4, 16, 0.0, None, fake(C), None, None) == ALIGN
+
+
 def test_metric_checks(lib):
     f = lib.jet_token_mult_prob_error
     assert f(None, fake(B), 16, fake(C), fake(D), 8, None) == NULL
@@ -266,6 +276,8 @@ def test_no_device_is_reported():
                                         128, 128, fake(A), None) == DEVICE
     assert lib.jet_swiglu_quant_1x128(fake(A), fake(B), 512, 4, 256, fake(C), fake(D),
                                       None) == DEVICE
+    assert lib.jet_token_mismatch_per_sequence(fake(A), fake(B), None, fake(D), 4, 16, 0.0, None,
+                                               fake(C), None, None) == DEVICE
     assert lib.jet_kv_calibrate(fake(A), 4, 8, 128, fake(B), None) == DEVICE
     assert lib.jet_kv_cache_write(fake(A), fake(B), fake(C), 4, 8, 128, fake(D), 16,
                                   None) == DEVICE

@@ -129,3 +129,55 @@ def test_masked_optional_outputs(jet):
     jet.jet_token_mismatch_masked(a.cuda(), b.cuda(), mask, 0.0, None, out, None, ws)
     ref, _, _ = oracle.token_mismatch_masked(a.numpy(), b.numpy(), mask.cpu().numpy())
     assert abs(float(out.cpu()[0]) - ref) <= 1e-5 * ref
+
+
+# ---------------------------------------------------------- per sequence --
+
+def check_per_sequence(jet, a, b, off, mask=None, cap=0.0):
+    o = torch.from_numpy(np.asarray(off, np.int64)).cuda()
+    m = None if mask is None else torch.from_numpy(mask).cuda()
+    r, c, w = jet.token_mismatch_per_sequence(a.cuda(), b.cuda(), o, m, cap)
+    r, c, w = r.cpu().numpy(), c.cpu().numpy(), w.cpu().numpy()
+    rr, cc, ww = oracle.token_mismatch_per_sequence(a.numpy(), b.numpy(), off, mask, cap)
+    assert np.array_equal(c, cc), "per-sequence counts"
+    empty = cc == 0
+    assert np.isnan(r[empty]).all()
+    assert (np.abs(r[~empty] - rr[~empty]) <= 1e-5 * rr[~empty]).all(), "per-sequence metrics"
+    assert np.allclose(w.astype(np.float64), ww, rtol=2e-6, atol=0), "importance weights"
+    return r, c, w
+
+
+def test_per_sequence_ragged_and_empty(jet):
+    lens = np.array([5, 0, 130, 1, 64, 17, 0, 2049, 3])
+    off = np.concatenate([[0], np.cumsum(lens)])
+    n = int(off[-1])
+    a, b = wl.logprobs(n, seed=11)
+    mask = (np.random.default_rng(11).random(n) < 0.7).astype(np.uint8)
+    mask[off[5]:off[6]] = 0                          # a fully masked-out sequence
+    check_per_sequence(jet, a, b, off, mask, cap=1.02)
+    check_per_sequence(jet, a, b, off, None)
+
+
+def test_per_sequence_4m_tokens(jet):
+    """2048 sequences of log-normal lengths (about 2048 tokens each), prompt
+    tokens masked out, the weights capped."""
+    rng = np.random.default_rng(12)
+    lens = np.maximum(1, rng.lognormal(7.3, 0.8, 2048)).astype(np.int64)
+    lens = (lens * (4_194_304 / lens.sum())).astype(np.int64)
+    lens[-1] += 4_194_304 - lens.sum()
+    off = np.concatenate([[0], np.cumsum(lens)])
+    a, b = wl.logprobs(4_194_304, seed=12)
+    mask = np.ones(4_194_304, np.uint8)
+    for s in range(2048):                            # the first quarter of each sequence: prompt
+        mask[off[s]:off[s] + lens[s] // 4] = 0
+    check_per_sequence(jet, a, b, off, mask, cap=1.05)
+
+
+def test_per_sequence_one_sequence_and_determinism(jet):
+    a, b = wl.logprobs(100_003, seed=13)
+    off = torch.tensor([0, 100_003], device="cuda")
+    r1, c1, w1 = jet.token_mismatch_per_sequence(a.cuda(), b.cuda(), off)
+    r2, _, w2 = jet.token_mismatch_per_sequence(a.cuda(), b.cuda(), off)
+    assert torch.equal(r1, r2) and torch.equal(w1, w2)
+    plain = float(jet.token_mult_prob_error(a.cuda(), b.cuda()).cpu()[0])
+    assert abs(float(r1.cpu()[0]) - plain) <= 1e-6 * plain and int(c1.cpu()[0]) == 100_003
