@@ -173,6 +173,15 @@ def test_per_sequence_4m_tokens(jet):
     check_per_sequence(jet, a, b, off, mask, cap=1.05)
 
 
+def test_per_sequence_chunk_edges(jet):
+    """Sequences ending and starting exactly on, and one token either side of,
+    the 4096-token chunk edges, empty ones there, and one spanning chunks."""
+    lens = np.array([4096, 0, 4095, 1, 1, 4094, 0, 3, 20000, 4096])
+    off = np.concatenate([[0], np.cumsum(lens)])
+    a, b = wl.logprobs(int(off[-1]), seed=14)
+    check_per_sequence(jet, a, b, off)
+
+
 def test_per_sequence_one_sequence_and_determinism(jet):
     a, b = wl.logprobs(100_003, seed=13)
     off = torch.tensor([0, 100_003], device="cuda")
