@@ -860,6 +860,7 @@ def run_e2e(args, step_a, step_b, world, device, unit, amount, scale, torch, bar
             "host_copy_gbs": round((h2d + d2h) / (e_ms * 1e-3) / 1e9, 1),
             "host_link_gbs": link, "host_cpus": host_cpus,
             "gpu_numa_node": gpu_numa_node(torch, device),
+            "max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS"),
             "steps": n, "pipelining": "2 buffer sets; copy-in, compute and copy-out streams"}
 
 
