@@ -27,3 +27,14 @@ def test_reference_line(workload, unit):
     import bench
     args = type("A", (), {"workload": workload, "tokens": 2048})()
     assert line["config"]["workload"] == bench.workload_name(args)
+
+
+def test_reference_other_ranks_exit_without_work():
+    """Under torchrun only rank 0 runs the reference arm; the others exit 0
+    and print nothing."""
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "metric",
+                        "--steps", "1"], cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
