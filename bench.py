@@ -262,14 +262,17 @@ class LayerStep:
         return out
 
     def host_io(self):
-        """Pinned host copies of the step's inputs and buffers for its results."""
+        """Pinned host copies of the step's inputs (X, the BF16 master weights,
+        dY and both log-probability vectors) and a buffer for its result, the
+        mismatch metric; Y, dX and dW stay on the device, where the next
+        layer, the previous layer and the optimizer read them."""
         import torch
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
         self.h_in = [(pin(v["x"]), v["x"]) for v in self.inputs.values()]
         self.h_in += [(pin(L["w"]), L["w"]) for L in self.lin]
         self.h_in += [(pin(L["dy"]), L["dy"]) for L in self.lin]
         self.h_in += [(pin(self.logp_train), self.logp_train), (pin(self.logp_rollout), self.logp_rollout)]
-        outs = [self.metric_out] + [L[k] for L in self.lin for k in ("y", "dx", "dw")]
+        outs = [self.metric_out]
         self.h_out = [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t) for t in outs]
         nbytes = lambda pairs: sum(h.numel() * h.element_size() for h, _ in pairs)
         return nbytes(self.h_in), nbytes(self.h_out)
