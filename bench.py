@@ -1057,7 +1057,7 @@ def run_gpu(args):
         ach = dom_work_launch / (dom_ms_launch * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(ach / hbm, 4), "peak_note": f"{pk_kind} copy bandwidth"}
-    roof["traffic"] = measured_traffic(dom, args.workload)
+    roof["traffic"] = measured_traffic(dom, workload_name(args))
     quant_fams = [f for f in fam_ms if not f.startswith("gemm") and f != "token_mult_prob_error"]
     q_bytes = sum(step.work[f] for f in quant_fams)
     q_ms = sum(fam_ms[f] for f in quant_fams) / args.steps

@@ -11,15 +11,15 @@ import bench
 
 def test_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
     d = json.load(open(os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")))
-    ent = d["train8b"]["gemm_fp8_wgrad"]
-    assert bench.measured_traffic("gemm_fp8_wgrad", "train8b") in (ent["dram_bytes_per_launch"], None)
+    ent = d["train8b_layer_M8192"]["gemm_fp8_wgrad"]
+    assert bench.measured_traffic("gemm_fp8_wgrad", "train8b_layer_M8192") in (ent["dram_bytes_per_launch"], None)
     # a hash that does not match the sources gives no traffic
-    fake = {"train8b": {"gemm_fp8_wgrad": dict(ent, sources_sha256_16="0" * 16)}}
+    fake = {"train8b_layer_M8192": {"gemm_fp8_wgrad": dict(ent, sources_sha256_16="0" * 16)}}
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(fake))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.measured_traffic("gemm_fp8_wgrad", "train8b") is None
-    assert bench.measured_traffic("gemm_fp8_fwd", "train8b") is None
+    assert bench.measured_traffic("gemm_fp8_wgrad", "train8b_layer_M8192") is None
+    assert bench.measured_traffic("gemm_fp8_fwd", "train8b_layer_M8192") is None
 
 
 def test_source_hash_covers_every_listed_file():
