@@ -7,24 +7,33 @@ One step = one pass of the whole hot path over one training layer of the
 
   weight sync   128x128 quantization of the 7 BF16 master weights
   forward       1x128 quantization of the 4 distinct inputs, 7 forward GEMMs
-  backward      1x128 quantization of the 7 output gradients, 7 DGrad GEMMs,
-                128x1 re-quantization of the 4 inputs and 7 gradients,
-                7 WGrad GEMMs
+  backward      both forms (1x128 and 128x1) of the 7 output gradients from
+                one read each, 7 DGrad GEMMs, 128x1 re-quantization of the 4
+                inputs, 7 WGrad GEMMs
   metric        token-mult-prob-error over the step's M tokens
 
-Inputs are synthetic (seeded, resident in HBM before timing).  The step's
-working set (~1.5 GB for train8b) is far larger than the 129 MB L2, so
-consecutive steps do not hit in L2; no extra flush is done.
+Other workloads (--workload): rollout (the 7 forward products at --tokens
+M), sync (the weight-sync quantizations of 32 layers), metric (the plain,
+masked and per-sequence mismatch metric over 4M tokens), moe and moe_train
+(the expert linears of a Qwen3-30B-A3B-shaped MoE layer, forward or a whole
+training step), kvcache (FP8 KV-cache recalibration and writes of one
+layer).
 
-Printed JSON (rank 0): value = GEMM FLOPs of the step / step time (TFLOP/s,
-quantization and metric time included); per-kernel rates with CUDA events
-recorded on the launch stream inside the timed region; a roofline for the
-dominant kernel; the end-to-end rate through the same C-ABI calls with pinned
-host buffers copied in and results copied out every step; the CPU oracle
-timed on a bounded sample on the host cores.
+Inputs are synthetic (seeded, resident in HBM before timing); every
+workload's working set is larger than the 129 MB L2 or L2 is flushed between
+calls (the `l2` key of `config` says which).
 
---impl reference times that CPU oracle as the reference arm (on a bounded
-sample per step, see cpu_sample_step).
+Printed JSON (rank 0): value = the step's GEMM FLOPs (or algorithmic bytes)
+/ step time, everything in the step included; per-kernel-family rates from
+CUDA events around graph replays of each family; a roofline for the family
+with the largest share, with its measured DRAM traffic where an ncu capture
+of the current sources exists; the end-to-end rate through the same C-ABI
+calls with the step's inputs copied in from pinned host buffers and its
+result copied out every step; the SM clocks sampled during the timed
+region; the CPU oracle timed on a bounded sample on the host cores.
+
+--impl reference times that CPU oracle as the reference arm (a bounded
+sample of the same workload per step, see CpuSample).
 """
 from __future__ import annotations
 
