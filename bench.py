@@ -1315,10 +1315,18 @@ class CpuSample:
         return reps * self.amount / seconds / (1e12 if self.unit == "TFLOP/s" else 1e9)
 
 
+def usable_cores() -> int:
+    """Host cores this process may run on (its affinity mask)."""
+    try:
+        return len(os.sched_getaffinity(0)) or 1
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(workload: str, seconds: float = 12.0):
     import oracle
     oracle.build()
-    nthreads = os.cpu_count() or 1
+    nthreads = usable_cores()
     smp = CpuSample(workload)
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -1338,7 +1346,7 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    nthreads = os.cpu_count() or 1
+    nthreads = usable_cores()
     smp = CpuSample(args.workload, seed=args.seed)
     for _ in range(args.warmup):
         smp.step(nthreads)
