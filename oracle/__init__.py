@@ -87,6 +87,10 @@ def _load():
         lib.jo_silu_f32.argtypes = [ctypes.c_float]
         lib.jo_silu_f32.restype = ctypes.c_float
         lib.jo_swiglu_quant_1x128.argtypes = [P, P, I, I, I, P, P, I, I]
+        lib.jo_rmsnorm_f32.argtypes = [P, P, I, I, ctypes.c_float, P, I, I]
+        lib.jo_rmsnorm_f32.restype = None
+        lib.jo_rmsnorm_quant_1x128.argtypes = [P, P, I, I, ctypes.c_float, P, P, I, I]
+        lib.jo_rmsnorm_quant_1x128.restype = None
         lib.jo_kv_calibrate.argtypes = [P, I, I, I, P]
         lib.jo_kv_cache_write.argtypes = [P, P, P, I, I, I, P, I]
         for f in (lib.jo_gemm_fwd, lib.jo_gemm_dgrad, lib.jo_gemm_wgrad):
@@ -213,6 +217,44 @@ def swiglu_quant_1x128(gate_bits, up_bits, nthreads=None):
     s = np.empty((F // 128, M), np.float32)
     _run(lambda a, b: lib.jo_swiglu_quant_1x128(_ptr(g), _ptr(u), F, M, F, _ptr(q), _ptr(s),
                                                 a, b), M, nthreads)
+    return q, s
+
+
+def _rms_args(x_bits, g_bits, eps):
+    x = _as_bf16_bits(x_bits)
+    g = _as_bf16_bits(g_bits).reshape(-1)
+    if x.ndim != 2 or g.size != x.shape[1]:
+        raise ValueError("x must be [M, K] and g [K]")
+    if not (np.isfinite(eps) and eps >= 0):
+        raise ValueError("eps must be finite and >= 0")
+    return x, np.ascontiguousarray(g), np.float32(eps)
+
+
+def rmsnorm_f32(x_bits, g_bits, eps, nthreads=None):
+    """The binary32 RMSNorm y = x * g / sqrt(mean(x^2) + eps) of the fused
+    RMSNorm quantizer (its fixed order of operations; see jet_oracle.c):
+    y float32 [M, K].  x: BF16 bits [M, K]; g: BF16 bits [K]."""
+    lib = _load()
+    x, g, e = _rms_args(x_bits, g_bits, eps)
+    M, K = x.shape
+    y = np.empty((M, K), np.float32)
+    _run(lambda a, b: lib.jo_rmsnorm_f32(_ptr(x), _ptr(g), M, K, float(e), _ptr(y), a, b),
+         M, nthreads)
+    return y
+
+
+def rmsnorm_quant_1x128(x_bits, g_bits, eps, nthreads=None):
+    """RMSNorm of x (binary32, as rmsnorm_f32), then 1x128 groups of y ->
+    (q uint8 [M,K], s float32 [K/128, M])."""
+    lib = _load()
+    x, g, e = _rms_args(x_bits, g_bits, eps)
+    M, K = x.shape
+    if K % 128:
+        raise ValueError("K must be a multiple of 128")
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((K // 128, M), np.float32)
+    _run(lambda a, b: lib.jo_rmsnorm_quant_1x128(_ptr(x), _ptr(g), M, K, float(e), _ptr(q),
+                                                 _ptr(s), a, b), M, nthreads)
     return q, s
 
 

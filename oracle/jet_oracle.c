@@ -314,6 +314,90 @@ void jo_swiglu_quant_1x128(const uint16_t *g, const uint16_t *u, int64_t ld,
 }
 
 /* ------------------------------------------------------------------------ */
+/* RMSNorm with the 1x128 quantization of its output fused                  */
+/* ------------------------------------------------------------------------ */
+/* The pages' system runs fused activation and RMSNorm operators
+ * ("Jet-RL ..." (gist.science), "Implementierung") and quantizes a linear
+ * layer's input in the operator that produces it ("英伟达破解AI训练效率难题"
+ * (163.com), section 五).  RMSNorm produces the inputs of the q/k/v and the
+ * gate/up projections.  The pages give no arithmetic for it; the reading here
+ * is RMSNorm y = x * g / sqrt(mean(x^2) + eps) evaluated in binary32 by one
+ * fixed sequence of IEEE operations, after which the 128-wide groups of the
+ * binary32 y are quantized exactly as activations are (no BF16 rounding of y
+ * in between):
+ *   - sum of squares of a row of K values: 32 partial sums; partial l adds,
+ *     in this order, the squares of the elements 8 (32 j + l) + t for
+ *     j = 0, 1, ... (while 8 (32 j + l) < K) and t = 0 .. 7, one binary32
+ *     rounding per addition (the square of a BF16 value is exact in
+ *     binary32); then five butterfly levels d = 16, 8, 4, 2, 1 replace
+ *     partial l by partial l + partial (l xor d) (every partial ends equal,
+ *     addition being commutative) and ss is partial 0;
+ *   - ms = fl32(ss / K), v = fl32(ms + eps), r = fl32(1 / fl32(sqrt(v)))
+ *     (IEEE division and square root), r = 0 when v == 0;
+ *   - y_k = fl32(fl32(x_k * r) * g_k).
+ * Rows whose sum of squares overflows binary32 are outside the contract. */
+static float rms_factor(const uint16_t *xr, int64_t K, float eps)
+{
+    float part[32];
+    for (int l = 0; l < 32; ++l) {
+        float acc = 0.0f;
+        for (int64_t j = 0; 8 * (32 * j + l) < K; ++j)
+            for (int t = 0; t < 8; ++t) {
+                float v = bf16_to_f32(xr[8 * (32 * j + l) + t]);
+                acc = acc + v * v;
+            }
+        part[l] = acc;
+    }
+    for (int d = 16; d >= 1; d /= 2) {
+        float nxt[32];
+        for (int l = 0; l < 32; ++l)
+            nxt[l] = part[l] + part[l ^ d];
+        memcpy(part, nxt, sizeof part);
+    }
+    float ms = part[0] / (float)K;
+    float v = ms + eps;
+    if (v == 0.0f)
+        return 0.0f;
+    float root = sqrtf(v);
+    return 1.0f / root;
+}
+
+/* y[m][k] (binary32) of rows [m0, m1) of x[M][K] with gain g[K] (BF16). */
+void jo_rmsnorm_f32(const uint16_t *x, const uint16_t *g, int64_t M, int64_t K,
+                    float eps, float *y, int64_t m0, int64_t m1)
+{
+    (void)M;
+    for (int64_t m = m0; m < m1; ++m) {
+        float r = rms_factor(x + m * K, K, eps);
+        for (int64_t k = 0; k < K; ++k) {
+            float t = bf16_to_f32(x[m * K + k]) * r;
+            y[m * K + k] = t * bf16_to_f32(g[k]);
+        }
+    }
+}
+
+/* RMSNorm of x[M][K] with gain g[K] (BF16 bits), then 1x128 groups of y:
+ * q[M][K] codes, s[kb * M + m] scales.  Rows [m0, m1) only. */
+void jo_rmsnorm_quant_1x128(const uint16_t *x, const uint16_t *g, int64_t M,
+                            int64_t K, float eps, uint8_t *q, float *s,
+                            int64_t m0, int64_t m1)
+{
+    float y[128];
+    int64_t Kb = K / 128;
+    for (int64_t m = m0; m < m1; ++m) {
+        float r = rms_factor(x + m * K, K, eps);
+        for (int64_t kb = 0; kb < Kb; ++kb) {
+            for (int i = 0; i < 128; ++i) {
+                int64_t k = kb * 128 + i;
+                float t = bf16_to_f32(x[m * K + k]) * r;
+                y[i] = t * bf16_to_f32(g[k]);
+            }
+            s[kb * M + m] = quant_group(y, 1, 128, q + m * K + kb * 128, 1);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* GEMMs: binary64 product of the dequantized operands                       */
 /* ------------------------------------------------------------------------ */
 
