@@ -270,18 +270,23 @@ class LayerStep:
             self.logp_train, self.logp_rollout, self.metric_out, self.metric_ws), "n%d" % self.M))
         return out
 
-    def host_io(self):
+    def host_io(self, outputs=False):
         """Pinned host copies of the step's inputs (X, the BF16 master weights,
         dY and both log-probability vectors) and a buffer for its result, the
         mismatch metric; Y, dX and dW stay on the device, where the next
-        layer, the previous layer and the optimizer read them."""
+        layer, the previous layer and the optimizer read them, unless
+        `outputs` (then they are copied back too)."""
         import torch
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-        self.h_in = [(pin(v["x"]), v["x"]) for v in self.inputs.values()]
-        self.h_in += [(pin(L["w"]), L["w"]) for L in self.lin]
-        self.h_in += [(pin(L["dy"]), L["dy"]) for L in self.lin]
-        self.h_in += [(pin(self.logp_train), self.logp_train), (pin(self.logp_rollout), self.logp_rollout)]
+        if not hasattr(self, "h_in"):
+            self.h_in = [(pin(v["x"]), v["x"]) for v in self.inputs.values()]
+            self.h_in += [(pin(L["w"]), L["w"]) for L in self.lin]
+            self.h_in += [(pin(L["dy"]), L["dy"]) for L in self.lin]
+            self.h_in += [(pin(self.logp_train), self.logp_train),
+                          (pin(self.logp_rollout), self.logp_rollout)]
         outs = [self.metric_out]
+        if outputs:
+            outs += [L[k] for L in self.lin for k in ("y", "dx", "dw")]
         self.h_out = [(torch.empty(t.shape, dtype=t.dtype, pin_memory=True), t) for t in outs]
         nbytes = lambda pairs: sum(h.numel() * h.element_size() for h, _ in pairs)
         return nbytes(self.h_in), nbytes(self.h_out)
@@ -709,18 +714,19 @@ class MetricStep:
                     self.scount), "S2048")]
 
 
-def make_step(args, device, rank):
-    if args.workload in ("train8b", "train32b"):
-        return LayerStep(args.workload, device, seed=args.seed + rank)
-    if args.workload == "rollout":
+def make_step(args, device, rank, workload=None):
+    workload = workload or args.workload
+    if workload in ("train8b", "train32b"):
+        return LayerStep(workload, device, seed=args.seed + rank)
+    if workload == "rollout":
         return RolloutStep(args.tokens, device, seed=args.seed + rank)
-    if args.workload == "sync":
+    if workload == "sync":
         return SyncStep(device, seed=args.seed + rank)
-    if args.workload == "moe":
+    if workload == "moe":
         return MoeStep(device, seed=args.seed + rank)
-    if args.workload == "moe_train":
+    if workload == "moe_train":
         return MoeTrainStep(device, seed=args.seed + rank)
-    if args.workload == "kvcache":
+    if workload == "kvcache":
         return KvCacheStep(device, seed=args.seed + rank)
     return MetricStep(device, seed=args.seed + rank)
 
@@ -820,14 +826,16 @@ def host_link_gbs(torch, device, nbytes=1 << 30):
     return out
 
 
-def run_e2e(args, step_a, step_b, world, device, unit, amount, scale, torch, barrier):
-    """End-to-end rate through the C-ABI calls with pinned host buffers."""
+def run_e2e(args, step_a, step_b, world, device, unit, amount, scale, torch, barrier,
+            outputs=False):
+    """End-to-end rate through the C-ABI calls with pinned host buffers
+    (`outputs`: a layer step also copies Y, dX and dW back)."""
     insts = [step_a, step_b]
     host_cpus = bind_to_gpu_numa_node(torch, device)
     link = host_link_gbs(torch, device)
     h2d = d2h = 0
     for st in insts:
-        h2d, d2h = st.host_io()
+        h2d, d2h = st.host_io(outputs=True) if outputs else st.host_io()
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     calls = [st.calls() for st in insts]
 
@@ -876,30 +884,27 @@ def run_e2e(args, step_a, step_b, world, device, unit, amount, scale, torch, bar
             "steps": n, "pipelining": "2 buffer sets; copy-in, compute and copy-out streams"}
 
 
-def run_gpu(args):
-    import torch
-    import torch.distributed as dist
+def peak_for_region(region_ms: float, pk: dict, pk_kind: str):
+    """Dense FP8 peak (TFLOP/s) for a kernel family timed over `region_ms`:
+    the burst cuBLAS BF16 figure x 2 when the family's timed region is
+    shorter than a second (a kernel timed alone), the sustained figure
+    (seconds under the power cap) otherwise.  Returns (peak, note)."""
+    if region_ms < 1000.0:
+        bf16, which = float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"])), "burst"
+    else:
+        bf16 = float(pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
+        which = "sustained"
+    note = (f"dense FP8 = {FP8_OVER_BF16:g} x {pk_kind} {which} cuBLAS BF16 "
+            f"({which}: the family's timed region is {region_ms:.0f} ms)")
+    return FP8_OVER_BF16 * bf16, note
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
 
-    import fp8_block_quantized_gb300 as jet
-    jet.load()
-
-    step = make_step(args, device, rank)
+def measure(args, workload, device, rank, world, torch, jet, barrier):
+    """Time one workload: the whole step (CUDA-graph replays), each kernel
+    family, the end-to-end leg; returns the JSON fields of its line."""
+    step = make_step(args, device, rank, workload)
     calls = step.calls()
     stream = torch.cuda.current_stream()
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
 
     for _ in range(args.warmup):
         for _, f, _ in calls:
@@ -931,7 +936,7 @@ def run_gpu(args):
         launch_mode = "stream"
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    with ClockSampler(local) as clk:
+    with ClockSampler(int(device.index or 0)) as clk:
         clk.wait_first()
         if graphs is not None:
             g_step.replay()          # one untimed replay: graph upload
@@ -1001,28 +1006,27 @@ def run_gpu(args):
     unit, amount = step.primary
     scale = 1e12 if unit == "TFLOP/s" else 1e9
     value = job_rate(world, amount, ms_per_step, scale)
+    del graphs
+    clocks = clk.summary()
 
     # ---- end to end: pinned host inputs in, results out, through the same
     # calls.  Every step copies all of its inputs in from pinned host memory
-    # and all of its results back; the copies are pipelined the way a caller
-    # would run them: two sets of device buffers, inputs of step k+1 copied in
-    # (one stream) while step k computes (a second) and step k-1's results
-    # are copied out (a third), with events ordering each buffer's reuse.
-    e2e = None
+    # and its result back; the copies are pipelined the way a caller would
+    # run them: two sets of device buffers, inputs of step k+1 copied in (one
+    # stream) while step k computes (a second) and step k-1's results are
+    # copied out (a third), with events ordering each buffer's reuse.  Layer
+    # steps also report a second variant that copies Y, dX and dW back too.
+    e2e = e2e_out = None
     if not args.no_e2e and hasattr(step, "host_io"):
-        e2e = run_e2e(args, step, make_step(args, device, rank), world, device, unit, amount, scale,
-                      torch, barrier)
-
-    if rank != 0:
-        if world > 1:
-            dist.barrier()
-            dist.destroy_process_group()
-        return
+        step_b = make_step(args, device, rank, workload)
+        e2e = run_e2e(args, step, step_b, world, device, unit, amount, scale, torch, barrier)
+        if isinstance(step, LayerStep):
+            e2e_out = run_e2e(args, step, step_b, world, device, unit, amount, scale, torch,
+                              barrier, outputs=True)
+        del step_b
 
     pk, pk_kind = peaks()
     hbm = float(pk.get("hbm_gbs", FALLBACK["hbm_gbs"]))
-    fp8_burst = FP8_OVER_BF16 * float(pk.get("bf16_tflops", FALLBACK["bf16_tflops"]))
-    fp8_sust = FP8_OVER_BF16 * float(pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"]))
     kernels = {}
     launches = {}
     for fam, _, _ in calls:
@@ -1030,16 +1034,15 @@ def run_gpu(args):
     for fam, ms in fam_ms.items():
         avg_ms = ms / args.steps
         w = step.work[fam]
-        if fam.startswith("gemm") and fam + "_bytes" in step.work:
-            rate = w / (avg_ms * 1e-3) / 1e12
-            grate = step.work[fam + "_bytes"] / (avg_ms * 1e-3) / 1e9
-            kernels[fam] = {"ms_per_step": round(avg_ms, 4), "launches_per_step": launches[fam],
-                            "TFLOP/s": round(rate, 1), "frac_fp8_peak": round(rate / fp8_sust, 4),
-                            "GB/s": round(grate, 1), "frac_hbm": round(grate / hbm, 4)}
-        elif fam.startswith("gemm"):
+        if fam.startswith("gemm"):
+            fp8, _ = peak_for_region(ms, pk, pk_kind)
             rate = w / (avg_ms * 1e-3) / 1e12
             kernels[fam] = {"ms_per_step": round(avg_ms, 4), "launches_per_step": launches[fam],
-                            "TFLOP/s": round(rate, 1), "frac_fp8_peak": round(rate / fp8_sust, 4)}
+                            "TFLOP/s": round(rate, 1), "frac_fp8_peak": round(rate / fp8, 4),
+                            "fp8_peak": round(fp8, 1)}
+            if fam + "_bytes" in step.work:
+                grate = step.work[fam + "_bytes"] / (avg_ms * 1e-3) / 1e9
+                kernels[fam].update({"GB/s": round(grate, 1), "frac_hbm": round(grate / hbm, 4)})
         else:
             rate = w / (avg_ms * 1e-3) / 1e9
             kernels[fam] = {"ms_per_step": round(avg_ms, 4), "launches_per_step": launches[fam],
@@ -1047,10 +1050,11 @@ def run_gpu(args):
     dom = max(fam_ms, key=fam_ms.get)
     dom_ms_launch = fam_ms[dom] / (args.steps * launches[dom])
     dom_work_launch = step.work[dom] / launches[dom]
+    fp8_dom, fp8_note = peak_for_region(fam_ms[dom], pk, pk_kind)
     # a GEMM whose arithmetic intensity is below the ridge point (dense FP8 /
     # HBM) is bounded by streaming its operands: report it against HBM
     hbm_bound_gemm = (dom.startswith("gemm") and dom + "_bytes" in step.work
-                      and step.work[dom] / step.work[dom + "_bytes"] < fp8_sust * 1e3 / hbm)
+                      and step.work[dom] / step.work[dom + "_bytes"] < fp8_dom * 1e3 / hbm)
     if hbm_bound_gemm:
         ach = step.work[dom + "_bytes"] / launches[dom] / (dom_ms_launch * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
@@ -1058,46 +1062,86 @@ def run_gpu(args):
                 "peak_note": f"{pk_kind} copy bandwidth; algorithmic bytes = codes + scales + BF16 out"}
     elif dom.startswith("gemm"):
         ach = dom_work_launch / (dom_ms_launch * 1e-3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_sust, 1),
-                "unit": "TFLOP/s", "frac": round(ach / fp8_sust, 4),
-                "peak_note": f"dense FP8 = {FP8_OVER_BF16:g} x {pk_kind} sustained cuBLAS BF16 "
-                             f"(burst {fp8_burst:.0f})"}
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_dom, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp8_dom, 4), "peak_note": fp8_note}
     else:
         ach = dom_work_launch / (dom_ms_launch * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(ach / hbm, 4), "peak_note": f"{pk_kind} copy bandwidth"}
-    roof["traffic"] = measured_traffic(dom, workload_name(args))
+    roof["traffic"] = measured_traffic(dom, step.config["workload"])
     quant_fams = [f for f in fam_ms if not f.startswith("gemm") and f != "token_mult_prob_error"]
     q_bytes = sum(step.work[f] for f in quant_fams)
     q_ms = sum(fam_ms[f] for f in quant_fams) / args.steps
-    gemm_ms = sum(fam_ms[f] for f in fam_ms if f.startswith("gemm")) / args.steps
+    gemm_fams = [f for f in fam_ms if f.startswith("gemm")]
+    gemm_ms = sum(fam_ms[f] for f in gemm_fams) / args.steps
 
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-        "data": "synthetic",
+        "value": round(value, 2), "unit": unit, "ms_per_step": round(ms_per_step, 4),
         "config": dict(step.config, parallelism="replicas" if world > 1 else "single",
                        launch=launch_mode),
         "kernels": kernels,
         "roofline": roof,
         "gpu_launches": step.launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     if gemm_ms > 0:
         g = step.flops / (gemm_ms * 1e-3) / 1e12
-        line["gemm_only"] = {"TFLOP/s": round(g, 1), "frac_fp8_peak": round(g / fp8_sust, 4)}
+        fp8_g, _ = peak_for_region(gemm_ms * args.steps, pk, pk_kind)
+        line["gemm_only"] = {"TFLOP/s": round(g, 1), "frac_fp8_peak": round(g / fp8_g, 4)}
     if q_ms > 0:
         qr = q_bytes / (q_ms * 1e-3) / 1e9
         line["quantize"] = {"GB/s": round(qr, 1), "frac_hbm": round(qr / hbm, 4)}
     if e2e is not None:
         line["e2e"] = e2e
+    if e2e_out is not None:
+        line["e2e_with_outputs"] = e2e_out
     if args.detail:
         line["detail_ms_per_step"] = {f"{fam}/{label}": round(ms / args.steps, 4)
                                       for (fam, label), ms in detail_ms.items()}
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, seconds=args.cpu_seconds)
-    print(json.dumps(line), flush=True)
+    del step, calls
+    return line
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    import fp8_block_quantized_gb300 as jet
+    jet.load()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    body = measure(args, args.workload, device, rank, world, torch, jet, barrier)
+    # The default workload (the 8B-shaped layer) is followed by the 32B-shaped
+    # layer in the same run, so that one line carries both training shapes.
+    also = None
+    if args.workload == "train8b" and not args.no_train32b:
+        torch.cuda.empty_cache()
+        also = measure(args, "train32b", device, rank, world, torch, jet, barrier)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": body.pop("value"), "unit": body.pop("unit"),
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": body.pop("ms_per_step"), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic"}
+        line.update(body)
+        if also is not None:
+            line["train32b"] = also
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.workload, seconds=args.cpu_seconds)
+        print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -1388,6 +1432,9 @@ def main():
                     help="launch every call from the host inside the timed region "
                          "instead of replaying a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-train32b", action="store_true",
+                    help="with the default train8b workload, skip the 32B-shaped layer that "
+                         "is otherwise measured after it and reported under `train32b`")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--detail", action="store_true",
                     help="also report per-launch-site kernel times")

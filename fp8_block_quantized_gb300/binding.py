@@ -24,7 +24,7 @@ OP = {"quant_act_1x128": 0, "quant_w_128x128": 1, "requant_128x1": 2,
       "gemm_fp8_fwd": 3, "gemm_fp8_dgrad": 4, "gemm_fp8_wgrad": 5,
       "token_mult_prob_error": 6, "quant_dual_1x128_128x1": 7, "token_mismatch_masked": 8,
       "swiglu_quant_1x128": 9, "kv_calibrate": 10, "kv_cache_write": 11,
-      "token_mismatch_per_sequence": 12}
+      "token_mismatch_per_sequence": 12, "rmsnorm_quant_1x128": 13}
 
 # name -> argtypes (restype is int status unless listed in _RESTYPE)
 P, I, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
@@ -36,6 +36,7 @@ SIGNATURES = {
     "jet_requant_128x1": [P, P, I, I, P, P, P],
     "jet_quant_dual_1x128_128x1": [P, I, I, P, P, P, P, P],
     "jet_swiglu_quant_1x128": [P, P, I, I, I, P, P, P],
+    "jet_rmsnorm_quant_1x128": [P, P, I, I, ctypes.c_float, P, P, P],
     "jet_kv_calibrate": [P, I, I, I, P, P],
     "jet_token_mismatch_per_sequence": [P, P, P, P, I, I, ctypes.c_float, P, P, P, P],
     "jet_kv_cache_write": [P, P, P, I, I, I, P, I, P],
@@ -51,6 +52,7 @@ SIGNATURES = {
     "jet_workspace_bytes": [ctypes.c_int, I, I, I],
     "jet_device_status": [P, ctypes.POINTER(ctypes.c_uint32)],
     "jet_selftest_bounded_wait": [ctypes.c_uint32, P],
+    "jet_selftest_gemm_timeout": [P, P, P, P, I, I, I, P, ctypes.c_uint64, P],
     "jet_selftest_quotient": [P, P, I, P, P],
 }
 _RESTYPE = {"jet_status_str": ctypes.c_char_p, "jet_version": ctypes.c_int,
@@ -121,6 +123,23 @@ def workspace_bytes(op: str, M=0, N=0, K=0) -> int:
 def selftest_bounded_wait(limit_us: int, stream=None):
     """Run the library's bounded-wait self-test kernel (records a timeout)."""
     _check("jet_selftest_bounded_wait", load().jet_selftest_bounded_wait(limit_us, _stream(stream)))
+
+
+def selftest_gemm_timeout(qx, sx, qw, sw, limit_cycles: int, stream=None):
+    """The forward product on the single-CTA GEMM kernel with its pipeline
+    waits limited to `limit_cycles` SM cycles (the GEMM's time-out path);
+    returns Y (unspecified when a wait ran out; see device_status())."""
+    import torch
+    M, K = qx.shape
+    N = qw.shape[0]
+    _need(qx, torch.uint8, (M, K), "qx")
+    _need(sx, torch.float32, (K // 128, M), "sx")
+    _need(qw, torch.uint8, (N, K), "qw")
+    _need(sw, torch.float32, (N // 128, K // 128), "sw")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device)
+    _check("jet_selftest_gemm_timeout", load().jet_selftest_gemm_timeout(
+        _ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), M, N, K, _ptr(y), limit_cycles, _stream(stream)))
+    return y
 
 
 def selftest_quotient(x, s, stream=None):
@@ -206,6 +225,17 @@ def jet_swiglu_quant_1x128(gate, up, q, s, stream=None):
     _need(s, torch.float32, (F // 128, M), "s")
     _check("jet_swiglu_quant_1x128", load().jet_swiglu_quant_1x128(
         _ptr(gate), _ptr(up), ld, M, F, _ptr(q), _ptr(s), _stream(stream)))
+
+
+def jet_rmsnorm_quant_1x128(x, g, eps, q, s, stream=None):
+    import torch
+    M, K = x.shape
+    _need(x, torch.bfloat16, (M, K), "x")
+    _need(g, torch.bfloat16, (K,), "g")
+    _need(q, torch.uint8, (M, K), "q")
+    _need(s, torch.float32, (K // 128, M), "s")
+    _check("jet_rmsnorm_quant_1x128", load().jet_rmsnorm_quant_1x128(
+        _ptr(x), _ptr(g), M, K, float(eps), _ptr(q), _ptr(s), _stream(stream)))
 
 
 def jet_kv_calibrate(x, scale, stream=None):
@@ -448,6 +478,17 @@ def quant_dual_1x128_128x1(x, stream=None):
     sT = torch.empty((M // 128, K), dtype=torch.float32, device=x.device)
     jet_quant_dual_1x128_128x1(x, q, s, qT, sT, stream)
     return q, s, qT, sT
+
+
+def rmsnorm_quant_1x128(x, g, eps=1e-5, stream=None):
+    """RMSNorm of x [M,K] with gain g [K] fused with the 1x128 quantization:
+    (codes uint8 [M,K], scales float32 [K/128, M])."""
+    import torch
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    s = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    jet_rmsnorm_quant_1x128(x, g, eps, q, s, stream)
+    return q, s
 
 
 def swiglu_quant_1x128(gate, up, stream=None):

@@ -42,9 +42,14 @@
 // unit per (tile, range).  Each unit writes its FP32
 // partial tile to a caller-provided workspace [splits][R][C]; a second kernel
 // adds the partials in split order (deterministic) and rounds once to BF16.
-// Every mbarrier wait is bounded (see jet_common.cuh); a role that gives up
-// records JET_ERR_TIMEOUT, the others stop at their next wait, in-flight
-// copies and MMAs are drained and TMEM is freed before the kernel returns.
+// Every mbarrier wait is bounded by kWaitLimitCycles SM cycles (~2 s at the
+// maximum clock; jet_common.cuh), except the pipeline waits of the time-out
+// self-test (kFwdTimeoutTest), which poll against a limit given at launch.  A
+// role that gives up records JET_ERR_TIMEOUT and sets the CTA's abort flag;
+// the CTA's other roles stop at their next wait, in-flight copies and MMAs are
+// drained and TMEM is freed before the kernel returns.  The abort flag is per
+// CTA: in a CTA pair the peer learns of it only through its own waits running
+// out.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -62,9 +67,20 @@ using namespace jet::ptx;
 // (tokens concatenated in expert order, weights stacked [E][N][K]):
 // kFwdGrouped and kDgradGrouped split the rows by expert, kWgradGrouped the
 // contraction (each expert's dW over its own tokens, outputs stacked).
-enum Mode { kFwd = 0, kDgrad = 1, kWgrad = 2, kFwdGrouped = 3, kDgradGrouped = 4, kWgradGrouped = 5 };
+// kFwdTimeoutTest is the forward product of the time-out self-test: its
+// pipeline waits poll (mbar_wait_polled) against a limit given at launch.
+enum Mode {
+    kFwd = 0, kDgrad = 1, kWgrad = 2, kFwdGrouped = 3, kDgradGrouped = 4, kWgradGrouped = 5,
+    kFwdTimeoutTest = 6
+};
 constexpr int base_mode(int mode) {
-    return mode == kFwdGrouped ? kFwd : mode == kDgradGrouped ? kDgrad : mode == kWgradGrouped ? kWgrad : mode;
+    return mode == kFwdGrouped || mode == kFwdTimeoutTest ? kFwd
+           : mode == kDgradGrouped                        ? kDgrad
+           : mode == kWgradGrouped                        ? kWgrad
+                                                          : mode;
+}
+constexpr bool is_grouped(int mode) {
+    return mode == kFwdGrouped || mode == kDgradGrouped || mode == kWgradGrouped;
 }
 constexpr int kMaxGroups = 384;  // one expert per thread of the unit-count scan
 
@@ -198,8 +214,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const float *__restrict__ sb,
                 uint16_t *__restrict__ out, int R, int C, int D, Raster raster, int splits,
                 float *__restrict__ partial, const int64_t *__restrict__ goff, int gE,
-                unsigned *status) {
-    using CF = Cfg<BN, CL, CL == 2 || MODE >= kFwdGrouped>;
+                unsigned *status, uint64_t wait_limit) {
+    using CF = Cfg<BN, CL, CL == 2 || is_grouped(MODE)>;
     constexpr int S = CF::kStages;
     constexpr int SS = CF::kScaleSlots;
     constexpr bool kPair = CL == 2;
@@ -210,7 +226,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     // grouped forward: per expert, its first row and the prefix of its units
-    constexpr bool kGrp = MODE >= kFwdGrouped;
+    constexpr bool kGrp = is_grouped(MODE);
     constexpr int BASE = base_mode(MODE);
     constexpr bool kFwdLike = BASE == kFwd;
     constexpr int kGT = kGrp ? kMaxGroups + 1 : 1;
@@ -230,6 +246,14 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const bool leader = rank == 0;
     const int unit0 = blockIdx.x / CL, unit_step = gridDim.x / CL;
     volatile int *abort = &abort_sh;
+    // Pipeline waits (abortable): bounded by kWaitLimitCycles, or by the
+    // launch's `wait_limit` with polling in the time-out self-test.
+    auto pwait = [&](uint64_t *bar, uint32_t parity, unsigned site) -> bool {
+        if constexpr (MODE == kFwdTimeoutTest)
+            return mbar_wait_polled(bar, parity, abort, status, site, wait_limit);
+        else
+            return mbar_wait(bar, parity, abort, status, site);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -366,10 +390,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const uint32_t use = it / S;
                     const int ss = it % SS;
                     const uint32_t suse = it / SS;
-                    if (!mbar_wait(&empty_bar[s], (use & 1u) ^ 1u, abort, status,
-                                   SITE_GEMM_PRODUCER_EMPTY) ||
-                        !mbar_wait(&sempty_bar[ss], (suse & 1u) ^ 1u, abort, status,
-                                   SITE_GEMM_PRODUCER_EMPTY)) {
+                    if (!pwait(&empty_bar[s], (use & 1u) ^ 1u, SITE_GEMM_PRODUCER_EMPTY) ||
+                        !pwait(&sempty_bar[ss], (suse & 1u) ^ 1u, SITE_GEMM_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
@@ -450,9 +472,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const uint32_t use = it / S;
                     const int buf = it & 1;
                     const uint32_t tuse = it >> 1;
-                    if (!mbar_wait(&tempty_bar[buf], (tuse & 1u) ^ 1u, abort, status,
-                                   SITE_GEMM_MMA_TMEM_EMPTY) ||
-                        !mbar_wait(&full_bar[s], use & 1u, abort, status, SITE_GEMM_MMA_FULL)) {
+                    if (!pwait(&tempty_bar[buf], (tuse & 1u) ^ 1u, SITE_GEMM_MMA_TMEM_EMPTY) ||
+                        !pwait(&full_bar[s], use & 1u, SITE_GEMM_MMA_FULL)) {
                         ok = false;
                         break;
                     }
@@ -539,8 +560,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const uint32_t tuse = it >> 1;
                 const int ss = it % SS;
                 const uint32_t suse = it / SS;
-                if (!mbar_wait(&sfull_bar[ss], suse & 1u, abort, status,
-                               SITE_GEMM_EPI_TMEM_FULL)) {
+                if (!pwait(&sfull_bar[ss], suse & 1u, SITE_GEMM_EPI_TMEM_FULL)) {
                     ok = false;
                     break;
                 }
@@ -554,8 +574,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sempty_bar[ss]);
                 }
-                if (!mbar_wait(&tfull_bar[buf], tuse & 1u, abort, status,
-                               SITE_GEMM_EPI_TMEM_FULL)) {
+                if (!pwait(&tfull_bar[buf], tuse & 1u, SITE_GEMM_EPI_TMEM_FULL)) {
                     ok = false;
                     break;
                 }
@@ -781,8 +800,8 @@ template <int BN, int MODE, int CL>
 jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, const uint8_t *b,
                   const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D, int splits,
                   float *partial, cudaStream_t stream, const int64_t *goff = nullptr,
-                  int gE = 0) {
-    using CF = Cfg<BN, CL, CL == 2 || MODE >= kFwdGrouped>;
+                  int gE = 0, uint64_t wait_limit = kWaitLimitCycles) {
+    using CF = Cfg<BN, CL, CL == 2 || is_grouped(MODE)>;
     auto kernel = gemm_fp8_kernel<BN, MODE, CL>;
     static std::mutex mu;
     static int max_units[64] = {};  // co-resident CTAs (CL = 1) or clusters (CL = 2)
@@ -824,7 +843,7 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     CUtensorMap ta, tb, ty;
     if (!make_map_u8(&ta, a, (uint64_t)D, (uint64_t)R, BK, BM)) return JET_ERR_CUDA;
     constexpr int BASE = base_mode(MODE);
-    constexpr bool kStagedOut = CL == 2 || MODE >= kFwdGrouped;
+    constexpr bool kStagedOut = CL == 2 || is_grouped(MODE);
     // grouped WGrad writes the experts' dW stacked, [gE * R][C]
     const uint64_t out_rows = MODE == kWgradGrouped ? (uint64_t)gE * (uint64_t)R : (uint64_t)R;
     if (kStagedOut && !make_map_out(&ty, out, (uint64_t)C, out_rows)) return JET_ERR_CUDA;
@@ -847,7 +866,7 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kernel, tmA_arg(ta), tmA_arg(tb), tmA_arg(ty), sa, sb, out,
                            (int)R, (int)C, (int)D, raster, splits, partial, goff, gE,
-                           dev.status_word) != cudaSuccess) {
+                           dev.status_word, wait_limit) != cudaSuccess) {
         cudaGetLastError();
         return JET_ERR_CUDA;
     }
@@ -1094,6 +1113,28 @@ jet_status jet_gemm_fp8_wgrad(const uint8_t *qdyT, const float *sdyT, const uint
                     aligned16(dw),
                 JET_ERR_ALIGN);
     return run_gemm<kWgrad>(qdyT, sdyT, qxT, sxT, dw, N, K, M, ws, stream);
+}
+
+jet_status jet_selftest_gemm_timeout(const uint8_t *qx, const float *sx, const uint8_t *qw,
+                                     const float *sw, int64_t M, int64_t N, int64_t K,
+                                     uint16_t *y, uint64_t limit_cycles, jet_stream_t stream) {
+    JET_REQUIRE(qx && sx && qw && sw && y, JET_ERR_NULL);
+    JET_REQUIRE(M >= 1 && M <= BM && N >= 128 && K >= 128 && N % 128 == 0 && K % 128 == 0 &&
+                    N < kMaxDim && K < kMaxDim,
+                JET_ERR_SHAPE);
+    JET_REQUIRE(limit_cycles >= 1 && limit_cycles <= kWaitLimitCycles, JET_ERR_SHAPE);
+    JET_REQUIRE(aligned16(qx) && aligned16(sx) && aligned16(qw) && aligned16(sw) &&
+                    aligned16(y),
+                JET_ERR_ALIGN);
+    DeviceInfo dev;
+    jet_status st = current_device(&dev);
+    if (st != JET_OK) return st;
+    // the single-CTA forward kernel, contraction not split
+    if (N % 256 == 0)
+        return launch<256, kFwdTimeoutTest, 1>(dev, qx, sx, qw, sw, y, M, N, K, 1, nullptr,
+                                               as_stream(stream), nullptr, 0, limit_cycles);
+    return launch<128, kFwdTimeoutTest, 1>(dev, qx, sx, qw, sw, y, M, N, K, 1, nullptr,
+                                           as_stream(stream), nullptr, 0, limit_cycles);
 }
 
 jet_status jet_selftest_bounded_wait(uint32_t limit_us, jet_stream_t stream) {

@@ -1,5 +1,7 @@
 // Library-wide entry points: status strings, device checks, the device-side
 // status word and workspace sizing.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "jet_common.cuh"
@@ -15,10 +17,35 @@ struct Cached {
     int state;  // 0 unknown, 1 ok, 2 wrong arch
     int num_sms;
     unsigned *status_word;
+    void *context;  // the context the status word's address belongs to
 };
 Cached g_cache[kMaxDevices];
 std::mutex g_mu;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
 }  // namespace
+
+void *current_context() {
+    CtxGetCurrentFn fn = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return static_cast<void *>(ctx);
+}
 
 jet_status current_device(DeviceInfo *info) {
     int dev = -1;
@@ -26,8 +53,14 @@ jet_status current_device(DeviceInfo *info) {
         cudaGetLastError();
         return JET_ERR_DEVICE;
     }
+    // After cudaDeviceReset (or any other teardown of the device's primary
+    // context) the module is loaded again and a __device__ variable can sit at
+    // a new address, so the cached address is only trusted for the context it
+    // was looked up in.
+    void *ctx = current_context();
     std::lock_guard<std::mutex> lock(g_mu);
     Cached &c = g_cache[dev];
+    if (c.state == 1 && c.context != ctx) c.state = 0;
     if (c.state == 0) {
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -44,8 +77,11 @@ jet_status current_device(DeviceInfo *info) {
                 cudaGetLastError();
                 return JET_ERR_CUDA;
             }
+            // the lookup may have created the primary context: ask again
+            if (ctx == nullptr) ctx = current_context();
             c.num_sms = sms;
             c.status_word = static_cast<unsigned *>(p);
+            c.context = ctx;
             c.state = 1;
         }
     }
@@ -53,6 +89,7 @@ jet_status current_device(DeviceInfo *info) {
     info->ordinal = dev;
     info->num_sms = c.num_sms;
     info->status_word = c.status_word;
+    info->context = ctx;
     return JET_OK;
 }
 

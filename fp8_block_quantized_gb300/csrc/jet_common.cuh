@@ -17,10 +17,17 @@ struct DeviceInfo {
     int ordinal;
     int num_sms;
     unsigned *status_word;  // device address of the library's status word
+    void *context;          // the current CUDA context (a CUcontext), or null
 };
 
-// Checks that a current device exists and is sm_103; fills `info`.
+// Checks that a current device exists and is sm_103; fills `info`.  Device
+// addresses cached by the library are looked up again when the current
+// context differs from the one they were looked up in (after a device reset
+// the module, and its __device__ variables, may be loaded elsewhere).
 jet_status current_device(DeviceInfo *info);
+
+// The calling thread's current CUDA context (a CUcontext), or null.
+void *current_context();
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -119,28 +119,37 @@ constexpr int kNoAllocPartials = 1024;
 // tokens, so 1024 partials cover 2,097,152 tokens.
 constexpr int64_t kNoAllocMaxTokens = (int64_t)kNoAllocPartials * kElemsPerBlockTarget;
 
-// 8 KB on every device that loads the library, kept until the process exits.
+// 8 KB on every device that loads the library, kept until the process exits
+// (or until the device is reset, after which it is loaded again).
 // In host code this name is only a host-side stand-in for the device array;
 // its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) double g_tmpe_scratch[kNoAllocPartials];
 
 std::mutex g_scratch_mu;
-double *g_scratch_ptr[64] = {};
+struct ScratchAddr {
+    double *ptr;
+    void *context;  // the context the address was looked up in
+};
+ScratchAddr g_scratch[64] = {};
 
-// Device address of g_tmpe_scratch on the current device `dev`, looked up once
-// per device (with that device current) and cached.
-jet_status scratch_address(int dev, double **out) {
+// Device address of g_tmpe_scratch on the current device `dev` (with that
+// device current), looked up on the first call in each context and cached:
+// after a device reset the module is loaded again and the array may move, so
+// a cached address is only reused while the context is the same.
+jet_status scratch_address(const jet::DeviceInfo &dev, double **out) {
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (dev < 0 || dev >= 64) return JET_ERR_DEVICE;
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (dev.ordinal < 0 || dev.ordinal >= 64) return JET_ERR_DEVICE;
+    ScratchAddr &c = g_scratch[dev.ordinal];
+    if (c.ptr == nullptr || c.context != dev.context) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_tmpe_scratch) != cudaSuccess || p == nullptr) {
             cudaGetLastError();
             return JET_ERR_CUDA;
         }
-        g_scratch_ptr[dev] = static_cast<double *>(p);
+        c.ptr = static_cast<double *>(p);
+        c.context = dev.context;
     }
-    *out = g_scratch_ptr[dev];
+    *out = c.ptr;
     return JET_OK;
 }
 
@@ -159,7 +168,7 @@ extern "C" jet_status jet_token_mult_prob_error_noalloc(const float *logp_train,
     if (st != JET_OK) return st;
     if (jet_metric_blocks(n) > kNoAllocPartials) return JET_ERR_SHAPE;
     double *partial = nullptr;
-    st = scratch_address(dev.ordinal, &partial);
+    st = scratch_address(dev, &partial);
     if (st != JET_OK) return st;
     // Every slot the second pass reads is written by the first pass of this
     // call, so the array needs no clearing between calls.

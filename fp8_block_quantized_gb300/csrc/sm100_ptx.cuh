@@ -73,6 +73,41 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait for the time-out self-test: polls with the non-blocking test and
+// reads the clock on every poll, so that a limit of a few hundred cycles is
+// honoured (a try_wait may suspend the thread until the phase completes).
+// Called by whole warps; every decision is made warp-uniform (all lanes see
+// the phase complete, any lane sees the abort flag, lane 0's clock), so the
+// lanes of a warp always leave together.
+__device__ __forceinline__ bool mbar_wait_polled(uint64_t *bar, uint32_t parity,
+                                                 volatile int *abort, unsigned *status,
+                                                 unsigned site, uint64_t limit_cycles) {
+    const uint64_t t0 = clock64();
+    for (;;) {
+        if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+        if (__any_sync(0xffffffffu, abort != nullptr && *abort != 0)) return false;
+        const int late = (uint64_t)(clock64() - t0) > limit_cycles ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, late, 0)) {
+            if ((threadIdx.x & 31) == 0) report_timeout(status, site);
+            if (abort) *abort = 1;
+            return false;
+        }
+    }
+}
+
 // Register reallocation between warpgroups (all 128 threads of the
 // warpgroup execute it).  The new counts must stay within what the block was
 // launched with: sum over warpgroups of 128 * count <= threads * launch regs.

@@ -80,7 +80,8 @@ typedef enum {
     JET_OP_SWIGLU_QUANT_1X128 = 9,
     JET_OP_KV_CALIBRATE = 10,
     JET_OP_KV_CACHE_WRITE = 11,
-    JET_OP_TOKEN_MISMATCH_PER_SEQUENCE = 12
+    JET_OP_TOKEN_MISMATCH_PER_SEQUENCE = 12,
+    JET_OP_RMSNORM_QUANT_1X128 = 13
 } jet_op;
 
 /* A cudaStream_t handle passed as an opaque pointer. */
@@ -153,6 +154,31 @@ JET_API jet_status jet_requant_128x1(const uint8_t *q, const float *s, int64_t M
 JET_API jet_status jet_swiglu_quant_1x128(const uint16_t *gate, const uint16_t *up, int64_t ld,
                                           int64_t M, int64_t F, uint8_t *q, float *s,
                                           jet_stream_t stream);
+
+/*
+ * RMSNorm with the 1x128 quantization of its output fused: the input of the
+ * q/k/v and gate/up projections written as E4M3 codes and FP32 scales
+ * straight from the residual stream, with no BF16 normalised activation.
+ * Source: gist.science summary, "Implementierung" (fused activation/RMSNorm
+ * operators in custom kernels), and 163.com article, section 五 (a linear
+ * layer's input quantized in the operator that produces it).  The pages give
+ * no arithmetic; y = x * g / sqrt(mean(x^2) + eps) is evaluated in binary32
+ * in one fixed order: lane partial sums of squares (lane l adds the elements
+ * 8 (32 j + l) + t in order of j, then t = 0 .. 7), a five-level butterfly,
+ * ms = ss / K, v = ms + eps, r = 1 / sqrt(v) (IEEE operations; r = 0 when
+ * v == 0), y = (x * r) * g; its 128-wide groups then follow the 1x128 group
+ * rule.  Within a few ulps of binary64 RMSNorm (at most (K/64 + 8.5) 2^-24
+ * relative).
+ *   x   [M][K] BF16 bits (in; the residual stream), g [K] BF16 bits (in; the
+ *       norm's gain).  M, K >= 0, K a multiple of 128 and below 2^24.
+ *   eps >= 0 (finite); the model's value, e.g. 1e-5.
+ *   q   [M][K] E4M3 codes, s [K/128][M] FP32 scales (out).
+ * Rows whose sum of squares overflows binary32 are a precondition violation
+ * with unspecified codes.
+ */
+JET_API jet_status jet_rmsnorm_quant_1x128(const uint16_t *x, const uint16_t *g, int64_t M,
+                                           int64_t K, float eps, uint8_t *q, float *s,
+                                           jet_stream_t stream);
 
 /*
  * FP8 KV cache, scales recalibrated after each model update.  Source: FP8-RL
@@ -353,7 +379,9 @@ JET_API jet_status jet_token_mult_prob_error(const float *logp_train,
  * library (1024 FP64 slots; every device that loads the library keeps it until
  * the process exits).  The library allocates and frees nothing here.  The first
  * call on a device looks up that array's device address (with the device
- * current) and caches it; make that first call before any stream capture.
+ * current) and caches it for the device's current context (after a device
+ * reset the next call looks it up again); make that first call before any
+ * stream capture.
  * All calls share the one array: calls whose kernels overlap on the GPU (e.g.
  * on two streams at once) race on it and may return wrong values - order them
  * on one stream or use jet_token_mult_prob_error with separate workspaces.
@@ -439,6 +467,27 @@ JET_API jet_status jet_device_status(jet_stream_t stream, uint32_t *detail);
  * usable.  The pages have no counterpart; it exists to test the bounded waits.
  */
 JET_API jet_status jet_selftest_bounded_wait(uint32_t limit_us, jet_stream_t stream);
+
+/*
+ * Self-test of the GEMM's own failure path: runs the forward product
+ * Y = X W^T (same operands and layouts as jet_gemm_fp8_fwd, M <= 128 tokens,
+ * on the single-CTA tensor-core kernel, contraction not split) with every
+ * pipeline wait limited to `limit_cycles` SM cycles (1 .. 4e9; the library's
+ * GEMMs use 4e9, about 2 s).  With a limit shorter than the first operand
+ * load, a role of the kernel gives up: it records JET_ERR_TIMEOUT and its wait
+ * site (1 producer, 2 MMA issuer waiting for operands, 3 MMA issuer waiting
+ * for an accumulator, 4 promotion warps) in the device status word and sets
+ * the CTA's abort flag; the other roles stop at their next wait, the producer
+ * waits for its loads in flight, the MMA issuer for its MMAs, TMEM is freed
+ * and the kernel returns, so jet_device_status() reports JET_ERR_TIMEOUT and
+ * the context stays usable.  Y is then unspecified.  Same argument checks as
+ * jet_gemm_fp8_fwd, plus M <= 128 and the limit's range (JET_ERR_SHAPE).
+ * The pages have no counterpart; it exists to test the bounded waits.
+ */
+JET_API jet_status jet_selftest_gemm_timeout(const uint8_t *qx, const float *sx,
+                                             const uint8_t *qw, const float *sw, int64_t M,
+                                             int64_t N, int64_t K, uint16_t *y,
+                                             uint64_t limit_cycles, jet_stream_t stream);
 
 /*
  * Self-test of the division the quantizers use: q[i] = x[i] / s[i] computed

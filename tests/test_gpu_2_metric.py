@@ -9,6 +9,7 @@ import torch
 
 import oracle
 from fp8_block_quantized_gb300 import workloads as wl
+from tests.gpu_util import assert_gemm_close
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +66,42 @@ def test_bounded_wait_times_out_and_context_survives(jet):
     assert code == 0 and word == 0
     a, b = wl.logprobs(4096)
     check(jet, a, b)                              # the context is still usable
+
+
+def test_gemm_timeout_path_and_context_survives(jet):
+    """The GEMM's own failure path: with its pipeline waits limited to a few
+    hundred SM cycles (shorter than the first operand load from memory), a
+    role of the single-CTA kernel gives up, records a GEMM wait site, the
+    others stop, loads and MMAs drain and TMEM is freed; afterwards the same
+    product at the normal limit matches the oracle, and so does a larger
+    product that fills every SM (TMEM was released everywhere)."""
+    x = wl.activations(128, 1024, seed=31, config=1)
+    w = wl.weights(512, 1024, seed=31, config=1)
+    qx, sx = oracle.quant_act_1x128(wl.bf16_bits(x))
+    qw, sw = oracle.quant_w_128x128(wl.bf16_bits(w))
+    dq = [torch.from_numpy(a).cuda() for a in (qx, sx, qw, sw)]
+    code, word = jet.device_status()
+    assert code == 0 and word == 0
+    for limit in (64, 300):
+        # fresh operands in DRAM each time (not in L2): evict with a write
+        torch.empty(256 << 20, dtype=torch.uint8, device="cuda").fill_(1)
+        jet.selftest_gemm_timeout(*dq, limit)
+        code, word = jet.device_status()
+        assert code == 7, (limit, code, word)                 # JET_ERR_TIMEOUT
+        assert (word >> 8) in (1, 2, 3, 4), hex(word)         # a GEMM wait site
+        assert jet.device_status() == (0, 0)                  # reading clears it
+    y = jet.selftest_gemm_timeout(*dq, 4_000_000_000)          # the library's own limit
+    assert jet.device_status() == (0, 0)
+    assert_gemm_close(y, oracle.gemm_fwd(qx, sx, qw, sw), "fwd after time-outs")
+    xb = wl.activations(4096, 1024, seed=32, config=1)
+    wb = wl.weights(2048, 1024, seed=32, config=1)
+    qxb, sxb = oracle.quant_act_1x128(wl.bf16_bits(xb))
+    qwb, swb = oracle.quant_w_128x128(wl.bf16_bits(wb))
+    yb = jet.gemm_fp8_fwd(*(torch.from_numpy(a).cuda() for a in (qxb, sxb, qwb, swb)))
+    assert jet.device_status() == (0, 0)
+    rows = np.arange(0, 4096, 97)
+    assert_gemm_close(yb[torch.as_tensor(rows).cuda()], oracle.gemm_fwd(qxb, sxb, qwb, swb, rows=rows),
+                      "fwd on every SM after time-outs")
 
 
 

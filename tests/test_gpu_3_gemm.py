@@ -199,6 +199,20 @@ def test_fwd_rollout_shapes(jet, name, N, K, M):
             nrows=24)
 
 
+@pytest.mark.parametrize("idx", range(len(wl.LLAMA8B_LINEARS)),
+                         ids=[n for n, _, _ in wl.LLAMA8B_LINEARS])
+@pytest.mark.parametrize("M", [16, 2048])
+def test_fwd_rollout_every_linear(jet, idx, M):
+    """Each of the 7 rollout linears of the 8B layer (its own weight tensor)
+    at a decode-batch and a prefill token count: split contraction at 16
+    tokens, CTA pairs at 2048."""
+    name, N, K = wl.LLAMA8B_LINEARS[idx]
+    key = wl.SHARED_INPUT[name]
+    xid = list(dict.fromkeys(wl.SHARED_INPUT[n] for n, _, _ in wl.LLAMA8B_LINEARS)).index(key)
+    run_fwd(jet, wl.activations(M, K, seed=0, config=2, tensor_id=xid),
+            wl.weights(N, K, seed=0, config=2, tensor_id=100 + idx), nrows=24)
+
+
 def test_train8b_q_proj_fwd_dgrad_wgrad(jet):
     layer = wl.training_layer("train8b")
     q = layer[0]

@@ -1,9 +1,12 @@
 """jet_token_mult_prob_error_noalloc: the metric for callers that cannot
 allocate device memory (the library keeps the partial sums in its own static
-device array).  Called through the C ABI with raw device pointers and checked
-against jet_token_mult_prob_error (caller-supplied workspace) within the
-metric's test tolerance, on two calls in a row with different inputs so that
-the second call runs over the first call's leftover scratch contents.
+device array).  Called through the C ABI with raw device pointers and
+compared with jet_token_mult_prob_error (caller-supplied workspace), which
+launches the same kernels on the same grid and sums in the same fixed order,
+so the two must agree bit for bit; also compared with the oracle's binary64
+metric within the metric's tolerance, and called once through the Python
+binding.  Two calls in a row with different inputs, so that the second call
+(fewer blocks) runs over the first call's leftover scratch contents.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it also passes alone in a fresh process."""
@@ -12,6 +15,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from fp8_block_quantized_gb300 import binding
 from fp8_block_quantized_gb300 import workloads as wl
 
@@ -40,15 +44,24 @@ def test_noalloc_matches_workspace_version_twice(torch_cuda):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     cases = [wl.logprobs(MAX_TOKENS, seed=11), wl.logprobs(300_001, seed=12)]
     outs = []
-    for a, b in cases:                       # two calls in a row
-        a, b = a.cuda(), b.cuda()
+    for a_h, b_h in cases:                   # two calls in a row
+        a, b = a_h.cuda(), b_h.cuda()
         out = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
         code = lib.jet_token_mult_prob_error_noalloc(raw(a), raw(b), a.numel(), raw(out), stream)
         assert code == 0, binding.STATUS.get(code, code)
         ref = reference_value(lib, a, b, stream)
         torch.cuda.synchronize()
-        got, want = float(out.cpu()[0]), float(ref.cpu()[0])
+        # same kernels, grid and summation order: identical bits
+        assert out.view(torch.int32).item() == ref.view(torch.int32).item(), \
+            (out.item(), ref.item())
+        want = oracle.token_mult_prob_error(a_h.numpy(), b_h.numpy())
+        got = float(out.item())
         assert abs(got - want) <= RTOL * want, (got, want)
+        # the Python binding's wrapper reaches the same entry point
+        out2 = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+        binding.jet_token_mult_prob_error_noalloc(a, b, out2)
+        torch.cuda.synchronize()
+        assert out2.view(torch.int32).item() == out.view(torch.int32).item()
         outs.append(got)
     assert outs[0] != outs[1]
     code, word = binding.device_status()
