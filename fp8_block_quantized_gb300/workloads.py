@@ -121,6 +121,14 @@ def grad_output(M: int, N: int, *, seed=0, config=3, tensor_id=200, device="cpu"
     return dy.to(torch.bfloat16)
 
 
+def norm_gain(K: int, *, seed=0, config=3, tensor_id=600, device="cpu",
+              std=0.1) -> torch.Tensor:
+    """RMSNorm gain g [K] = 1 + N(0, std) in BF16 (a learned norm weight near 1;
+    the pages give no value)."""
+    g = _gen(seed, config, tensor_id, device)
+    return (1.0 + std * _randn((K,), g, device)).to(torch.bfloat16)
+
+
 def heavy_activations(M: int, K: int, *, seed=0, config=5, tensor_id=300,
                       device="cpu") -> torch.Tensor:
     g = _gen(seed, config, tensor_id, device)

@@ -160,6 +160,22 @@ def test_swiglu_quant_checks(lib):
     assert lib.jet_workspace_bytes(binding.OP["swiglu_quant_1x128"], 4, 0, 256) == 0
 
 
+def test_rmsnorm_quant_checks(lib):
+    f = lib.jet_rmsnorm_quant_1x128
+    assert f(None, fake(B), 4, 256, 1e-5, fake(C), fake(D), None) == NULL
+    assert f(fake(A), None, 4, 256, 1e-5, fake(C), fake(D), None) == NULL
+    assert f(fake(A), fake(B), 4, 256, 1e-5, fake(C), None, None) == NULL
+    assert f(fake(A), fake(B), -1, 256, 1e-5, fake(C), fake(D), None) == SHAPE
+    assert f(fake(A), fake(B), 4, 200, 1e-5, fake(C), fake(D), None) == SHAPE     # K % 128
+    assert f(fake(A), fake(B), 4, 256, -1.0, fake(C), fake(D), None) == SHAPE     # eps < 0
+    assert f(fake(A), fake(B), 4, 256, float("nan"), fake(C), fake(D), None) == SHAPE
+    assert f(fake(A), fake(B), 4, 256, float("inf"), fake(C), fake(D), None) == SHAPE
+    assert f(fake(MIS), fake(B), 4, 256, 1e-5, fake(C), fake(D), None) == ALIGN
+    assert f(fake(A), fake(MIS), 4, 256, 1e-5, fake(C), fake(D), None) == ALIGN
+    assert f(None, None, 0, 256, 1e-5, None, None, None) in (OK, DEVICE)        # empty
+    assert lib.jet_workspace_bytes(binding.OP["rmsnorm_quant_1x128"], 4, 0, 256) == 0
+
+
 def test_grouped_gemm_checks(lib):
     f = lib.jet_gemm_fp8_fwd_grouped
     args = [fake(A), fake(B), fake(C), fake(D)]
@@ -258,6 +274,15 @@ def test_masked_metric_checks(lib):
 def test_selftest_limit_checks(lib):
     assert lib.jet_selftest_bounded_wait(0, None) == SHAPE
     assert lib.jet_selftest_bounded_wait(2_000_000, None) == SHAPE
+    f = lib.jet_selftest_gemm_timeout
+    args = (fake(A), fake(B), fake(C), fake(D))
+    assert f(None, fake(B), fake(C), fake(D), 128, 256, 256, fake(A), 100, None) == NULL
+    assert f(*args, 129, 256, 256, fake(A), 100, None) == SHAPE       # at most 128 rows
+    assert f(*args, 0, 256, 256, fake(A), 100, None) == SHAPE
+    assert f(*args, 128, 200, 256, fake(A), 100, None) == SHAPE
+    assert f(*args, 128, 256, 256, fake(A), 0, None) == SHAPE         # limit out of range
+    assert f(*args, 128, 256, 256, fake(A), 4_000_000_001, None) == SHAPE
+    assert f(fake(MIS), fake(B), fake(C), fake(D), 128, 256, 256, fake(A), 100, None) == ALIGN
 
 
 def test_no_device_is_reported():
@@ -276,6 +301,8 @@ def test_no_device_is_reported():
                                         128, 128, fake(A), None) == DEVICE
     assert lib.jet_swiglu_quant_1x128(fake(A), fake(B), 512, 4, 256, fake(C), fake(D),
                                       None) == DEVICE
+    assert lib.jet_rmsnorm_quant_1x128(fake(A), fake(B), 4, 256, 1e-5, fake(C), fake(D),
+                                       None) == DEVICE
     assert lib.jet_token_mismatch_per_sequence(fake(A), fake(B), None, fake(D), 4, 16, 0.0, None,
                                                fake(C), None, None) == DEVICE
     assert lib.jet_kv_calibrate(fake(A), 4, 8, 128, fake(B), None) == DEVICE

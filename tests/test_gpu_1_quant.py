@@ -347,3 +347,65 @@ def test_swiglu_empty(jet):
     e = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
     q, s = jet.swiglu_quant_1x128(e, e)
     assert q.shape == (0, 256) and s.shape == (2, 0)
+
+
+# ----------------------------------------------- RMSNorm + 1x128, fused --
+
+def check_rmsnorm(jet, x_cpu, g_cpu, eps, rows=None):
+    """The fused RMSNorm quantizer against the oracle's binary32 RMSNorm (its
+    fixed order of operations) and 1x128 group rule: codes and scales bit for
+    bit."""
+    q, s = jet.rmsnorm_quant_1x128(x_cpu.cuda(), g_cpu.cuda(), eps)
+    torch.cuda.synchronize()
+    xb, gb = bits(x_cpu), bits(g_cpu)
+    if rows is None:
+        q_ref, s_ref = oracle.rmsnorm_quant_1x128(xb, gb, eps)
+        assert_codes_equal(q, q_ref, "rmsnorm codes")
+        assert_scales_equal(s, s_ref, "rmsnorm scales")
+    else:
+        q_ref, s_ref = oracle.rmsnorm_quant_1x128(xb[rows], gb, eps)
+        r = torch.as_tensor(rows).cuda()
+        assert_codes_equal(q[r], q_ref, "rmsnorm codes")
+        assert_scales_equal(s[:, r], s_ref, "rmsnorm scales")
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (37, 384), (300, 1024), (129, 4096), (64, 5120),
+                                 (16, 8192), (9, 14336), (3, 25600)])
+@pytest.mark.parametrize("eps", [1e-5, 1e-6])
+def test_rmsnorm_shapes(jet, M, K, eps):
+    x = wl.activations(M, K, seed=M + K, config=3, tensor_id=40)
+    check_rmsnorm(jet, x, wl.norm_gain(K, seed=K), eps)
+
+
+def test_rmsnorm_edge_values(jet):
+    M, K = 40, 512
+    gen = torch.Generator().manual_seed(12)
+    x = torch.randn((M, K), generator=gen)
+    x[0] = 0.0                                     # zero row: r = 1/sqrt(eps)
+    x[1] = -0.0
+    x[2] = 1e-30                                   # tiny rows: eps dominates
+    x[3, :] = 3.0                                  # exact normalisation
+    x[4] = 1e17                                    # large (the sum stays finite)
+    x[5, :128] = 0.0                               # an all-zero group in a live row
+    x[6] = torch.linspace(-7, 7, K)
+    x[7, ::2] = 448.0
+    g = (1.0 + 0.1 * torch.randn(K, generator=gen))
+    g[::17] = -g[::17]                             # negative gains
+    g[5] = 0.0
+    for eps in (1e-5, 0.0):
+        check_rmsnorm(jet, x.to(torch.bfloat16), g.to(torch.bfloat16), eps)
+
+
+def test_rmsnorm_train32b_sampled(jet):
+    """The 32B layer's attention input at full size (16384 x 5120)."""
+    x = wl.activations(16384, 5120, seed=0, config=4, tensor_id=0)
+    rows = np.sort(np.random.default_rng(4).choice(16384, 1024, replace=False))
+    rows[0], rows[-1] = 0, 16383
+    check_rmsnorm(jet, x, wl.norm_gain(5120, seed=0, config=4), 1e-6, rows)
+
+
+def test_rmsnorm_empty(jet):
+    e = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones((256,), dtype=torch.bfloat16, device="cuda")
+    q, s = jet.rmsnorm_quant_1x128(e, g)
+    assert q.shape == (0, 256) and s.shape == (2, 0)
