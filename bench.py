@@ -6,7 +6,9 @@ One step = one pass of the whole hot path over one training layer of the
 32B-shaped layer at M = 16384 with --workload train32b):
 
   weight sync   128x128 quantization of the 7 BF16 master weights
-  forward       1x128 quantization of the 4 distinct inputs, 7 forward GEMMs
+  forward       1x128 quantization of the 4 distinct inputs (the attention
+                and MLP inputs through the fused RMSNorm quantizer), 7
+                forward GEMMs
   backward      both forms (1x128 and 128x1) of the 7 output gradients from
                 one read each, 7 DGrad GEMMs, 128x1 re-quantization of the 4
                 inputs, 7 WGrad GEMMs
@@ -64,7 +66,11 @@ BYTES_PER_ELEM = {
     "token_mult_prob_error": 8,                  # two FP32 per token
     "token_mismatch_masked": 4 + 4 + 1 + 4,      # two FP32 and the mask in, the weight out
     "swiglu_quant_1x128": 2 + 2 + 1 + 4 / 128,   # gate and up BF16 in, code + scale out
+    "rmsnorm_quant_1x128": 2 + 1 + 4 / 128,      # BF16 in, code + scale out (gain: K values per call)
 }
+# RMSNorm epsilon of the two model families (Llama-3.1-8B: 1e-5; the 32B-class
+# dense model: 1e-6)
+RMS_EPS = {"train8b": 1e-5, "train32b": 1e-6}
 
 
 def peaks():
@@ -192,12 +198,17 @@ class LayerStep:
         dev = device
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
-        # distinct inputs
+        # distinct inputs; the attention and MLP inputs come out of an RMSNorm
+        # (its gain drawn per norm), the other two are plain activations
         self.inputs = {}
+        self.eps = RMS_EPS[kind]
         for c in self.cases:
             key = wl.SHARED_INPUT[c.name]
             if key not in self.inputs:
-                self.inputs[key] = {"x": c.x, "K": c.K,
+                norm = key in ("attn_in", "mlp_in")
+                g = (wl.norm_gain(c.K, seed=seed, config=wl.CONFIG_ID[kind],
+                                  tensor_id=600 + len(self.inputs), device=dev) if norm else None)
+                self.inputs[key] = {"x": c.x, "K": c.K, "g": g,
                                     "q": e((M, c.K), u8), "s": e((c.K // 128, M), f32),
                                     "qT": e((c.K, M), u8), "sT": e((M // 128, c.K), f32)}
             c.key = key
@@ -223,8 +234,11 @@ class LayerStep:
                      "gemm_fp8_dgrad": sum(2 * M * c.N * c.K for c in self.cases),
                      "gemm_fp8_wgrad": sum(2 * M * c.N * c.K for c in self.cases),
                      "quant_w_128x128": sum(c.N * c.K for c in self.cases) * BYTES_PER_ELEM["quant_w_128x128"],
-                     "quant_act_1x128": sum(M * v["K"] for v in self.inputs.values())
+                     "quant_act_1x128": sum(M * v["K"] for v in self.inputs.values() if v["g"] is None)
                                         * BYTES_PER_ELEM["quant_act_1x128"],
+                     "rmsnorm_quant_1x128": sum(M * v["K"] * BYTES_PER_ELEM["rmsnorm_quant_1x128"]
+                                                + 2 * v["K"] for v in self.inputs.values()
+                                                if v["g"] is not None),
                      "requant_128x1": sum(M * v["K"] for v in self.inputs.values())
                                       * BYTES_PER_ELEM["requant_128x1"],
                      "quant_dual_1x128_128x1": sum(M * c.N for c in self.cases)
@@ -247,9 +261,13 @@ class LayerStep:
         for L in self.lin:
             out.append(("quant_w_128x128", lambda L=L: j.jet_quant_w_128x128(L["w"], L["qw"], L["sw"]),
                         L["case"].name))
-        for v in self.inputs.values():
-            out.append(("quant_act_1x128", lambda v=v: j.jet_quant_act_1x128(v["x"], v["q"], v["s"]),
-                        "x%d" % v["K"]))
+        for key, v in self.inputs.items():
+            if v["g"] is not None:
+                out.append(("rmsnorm_quant_1x128", lambda v=v: j.jet_rmsnorm_quant_1x128(
+                    v["x"], v["g"], self.eps, v["q"], v["s"]), key))
+            else:
+                out.append(("quant_act_1x128", lambda v=v: j.jet_quant_act_1x128(v["x"], v["q"], v["s"]),
+                            key))
         for L in self.lin:
             v = self.inputs[L["case"].key]
             out.append(("gemm_fp8_fwd", lambda L=L, v=v: j.jet_gemm_fp8_fwd(v["q"], v["s"], L["qw"], L["sw"], L["y"]),
@@ -293,9 +311,10 @@ class LayerStep:
 
 
 class RolloutStep:
-    """Forward only (rollout): 1x128 quantization of the 4 distinct inputs and
-    the 7 forward GEMMs of the 8B layer at M tokens; the weights are quantized
-    once beforehand (per weight sync) and not timed."""
+    """Forward only (rollout): the 4 distinct inputs quantized 1x128 (the
+    attention and MLP inputs through the fused RMSNorm quantizer) and the 7
+    forward GEMMs of the 8B layer at M tokens; the weights are quantized once
+    beforehand (per weight sync) and not timed."""
 
     def __init__(self, M: int, device, seed: int = 0):
         import torch
@@ -306,10 +325,14 @@ class RolloutStep:
         self.cases = wl.training_layer("train8b", seed=seed, device=device, M=M, with_grad=False)
         e = lambda shape, dt: torch.empty(shape, dtype=dt, device=device)
         self.inputs, self.lin = {}, []
+        self.eps = RMS_EPS["train8b"]
         for c in self.cases:
             key = wl.SHARED_INPUT[c.name]
             if key not in self.inputs:
-                self.inputs[key] = {"x": c.x, "K": c.K, "q": e((M, c.K), torch.uint8),
+                norm = key in ("attn_in", "mlp_in")
+                g = (wl.norm_gain(c.K, seed=seed, config=wl.CONFIG_ID["rollout"],
+                                  tensor_id=600 + len(self.inputs), device=device) if norm else None)
+                self.inputs[key] = {"x": c.x, "K": c.K, "g": g, "q": e((M, c.K), torch.uint8),
                                     "s": e((c.K // 128, M), torch.float32)}
             c.key = key
             qw, sw = jet.quant_w_128x128(c.w)
@@ -323,8 +346,11 @@ class RolloutStep:
         gemm_bytes = sum(M * c.K + c.N * c.K + 4 * (M * c.K // 128 + c.N * c.K // 16384)
                          + 2 * M * c.N for c in self.cases)
         self.work = {"gemm_fp8_fwd": self.flops, "gemm_fp8_fwd_bytes": gemm_bytes,
-                     "quant_act_1x128": sum(M * v["K"] for v in self.inputs.values())
-                     * BYTES_PER_ELEM["quant_act_1x128"]}
+                     "quant_act_1x128": sum(M * v["K"] for v in self.inputs.values() if v["g"] is None)
+                     * BYTES_PER_ELEM["quant_act_1x128"],
+                     "rmsnorm_quant_1x128": sum(M * v["K"] * BYTES_PER_ELEM["rmsnorm_quant_1x128"]
+                                                + 2 * v["K"] for v in self.inputs.values()
+                                                if v["g"] is not None)}
         # a split GEMM is two launches: the partial tiles and their reduction
         self.launches_per_step = (len(self.lin) + len(self.inputs)
                                   + sum(L["ws"] is not None for L in self.lin))
@@ -336,9 +362,13 @@ class RolloutStep:
 
     def calls(self):
         j, out = self.jet, []
-        for v in self.inputs.values():
-            out.append(("quant_act_1x128", lambda v=v: j.jet_quant_act_1x128(v["x"], v["q"], v["s"]),
-                        "x%d" % v["K"]))
+        for key, v in self.inputs.items():
+            if v["g"] is not None:
+                out.append(("rmsnorm_quant_1x128", lambda v=v: j.jet_rmsnorm_quant_1x128(
+                    v["x"], v["g"], self.eps, v["q"], v["s"]), key))
+            else:
+                out.append(("quant_act_1x128", lambda v=v: j.jet_quant_act_1x128(v["x"], v["q"], v["s"]),
+                            key))
         for L in self.lin:
             v = self.inputs[L["case"].key]
             out.append(("gemm_fp8_fwd", lambda L=L, v=v: j.jet_gemm_fp8_fwd(
@@ -1207,21 +1237,24 @@ class CpuSample:
             name, N, K = wl.layer_linears(kind)[0]
             cfg, T = wl.CONFIG_ID[workload], 128
             self.x = b(wl.activations(T, K, seed=seed, config=cfg, tensor_id=0))
+            self.g = b(wl.norm_gain(K, seed=seed, config=cfg, tensor_id=600))
+            self.eps = RMS_EPS[kind]
             self.w = b(wl.weights(N, K, seed=seed, config=cfg, tensor_id=100))
             if workload == "rollout":
                 import oracle
                 self.qw, self.sw = oracle.quant_w_128x128(self.w)
                 self.run = self._rollout
                 self.amount = 2 * T * N * K
-                self.desc = (f"{name} projection at {T} tokens: 1x128 quantization of X and the "
-                             f"binary64 forward product (weights quantized beforehand)")
+                self.desc = (f"{name} projection at {T} tokens: RMSNorm fused with the 1x128 "
+                             f"quantization of X and the binary64 forward product (weights "
+                             f"quantized beforehand)")
             else:
                 self.dy = b(wl.grad_output(T, N, seed=seed, config=cfg, tensor_id=200))
                 self.run = self._train
                 self.amount = 3 * 2 * T * N * K
                 self.desc = (f"{name} projection chain (N={N}, K={K}) at {T} tokens: 128x128 "
-                             f"weight quantization, 1x128 of X and dY, 128x1 requant of both, "
-                             f"binary64 forward/dgrad/wgrad")
+                             f"weight quantization, RMSNorm + 1x128 of X, 1x128 of dY, 128x1 "
+                             f"requant of both, binary64 forward/dgrad/wgrad")
         elif workload == "sync":
             self.unit = "GB/s"
             self.w = b(wl.weights(4096, 4096, seed=seed, config=5, tensor_id=1000))
@@ -1290,7 +1323,7 @@ class CpuSample:
     def _train(self, nt):
         import oracle
         qw, sw = oracle.quant_w_128x128(self.w, nthreads=nt)
-        qx, sx = oracle.quant_act_1x128(self.x, nthreads=nt)
+        qx, sx = oracle.rmsnorm_quant_1x128(self.x, self.g, self.eps, nthreads=nt)
         oracle.gemm_fwd(qx, sx, qw, sw, nthreads=nt)
         qdy, sdy = oracle.quant_act_1x128(self.dy, nthreads=nt)
         oracle.gemm_dgrad(qdy, sdy, qw, sw, nthreads=nt)
@@ -1300,7 +1333,7 @@ class CpuSample:
 
     def _rollout(self, nt):
         import oracle
-        qx, sx = oracle.quant_act_1x128(self.x, nthreads=nt)
+        qx, sx = oracle.rmsnorm_quant_1x128(self.x, self.g, self.eps, nthreads=nt)
         oracle.gemm_fwd(qx, sx, self.qw, self.sw, nthreads=nt)
 
     def _sync(self, nt):
