@@ -19,11 +19,12 @@
 //              memory stages with 128-byte swizzle, and the slice's FP32
 //              scales (128 row scales, the column scales) into an 8-slot
 //              ring by cp.async, so promotion never waits on global memory.
-//   warp 1     allocates TMEM and issues tcgen05.mma (K = 32 per instruction,
-//              four per slice) into one of two TMEM accumulators of BN
-//              columns, then commits to the stage's "empty" and the
-//              accumulator's "full" barriers.
-//   warps 2-3  idle.  Warpgroup 0 (warps 0-3) gives registers back
+//   warp 1     allocates TMEM; warps 1 and 2 issue tcgen05.mma (K = 32 per
+//              instruction, four per slice) into one of two TMEM accumulators
+//              of BN columns (warp 1 the even slices, warp 2 the odd ones),
+//              then commit to the stage's "empty" and the accumulator's
+//              "full" barriers.
+//   warp 3     idle.  Warpgroup 0 (warps 0-3) gives registers back
 //              (setmaxnreg 72) so that the epilogue warpgroups can hold their
 //              accumulators (setmaxnreg 200): 128*72 + 256*200 <= 384 * 168,
 //              the allocation the block is launched with.
@@ -217,6 +218,9 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 unsigned *status, uint64_t wait_limit) {
     using CF = Cfg<BN, CL, CL == 2 || is_grouped(MODE)>;
     constexpr int S = CF::kStages;
+    // MMA-issuing warps (see the MMA role): two when every stage and every
+    // TMEM accumulator is used by one issuer only, i.e. an even stage count.
+    constexpr uint32_t kIssuers = S % 2 == 0 ? 2u : 1u;
     constexpr int SS = CF::kScaleSlots;
     constexpr bool kPair = CL == 2;
     constexpr uint16_t kPairMask = 0x3;
@@ -268,7 +272,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(&tfull_bar[b], 1);
             mbar_init(&tempty_bar[b], 8 * CL);  // epilogue warps of every CTA of the pair
         }
-        mbar_init(&drain_bar, 1);
+        mbar_init(&drain_bar, kIssuers);  // one drain commit per MMA-issuing warp
         abort_sh = 0;
         fence_mbar_init();
     }
@@ -456,9 +460,20 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     mbar_wait(&full_bar[j % S], (j / S) & 1u, nullptr, status, SITE_GEMM_DRAIN);
             for (uint32_t j = it > (uint32_t)SS ? it - SS : 0u; j < it; ++j)
                 mbar_wait(&sfull_bar[j % SS], (j / SS) & 1u, nullptr, status, SITE_GEMM_DRAIN);
-        } else if (warp == 1 && leader) {
-            // --------------------------------------------------- MMA issuer
+        } else if ((warp == 1 || (warp == 2 && kIssuers == 2)) && leader) {
+            // -------------------------------------------------- MMA issuers
             // (in a pair only the leader issues; the MMA spans both CTAs)
+            // Warp 1 issues the even slices (TMEM accumulator 0), warp 2 the
+            // odd ones (accumulator 1).  A thread that issues tcgen05.mma while
+            // the tensor core's queue is full stalls there, about 128 cycles
+            // per MMA, and holds back the other warps of its SM sub-partition
+            // (here promotion warps, the critical path); two issuers halve that
+            // per sub-partition.  Each warp's slices use one accumulator and
+            // (S even) every second stage, so each warp waits on each
+            // barrier's phases in order; with an odd stage count, or a third
+            // issuer, a warp would skip a phase, whose parity then aliases the
+            // one before, so those configurations keep a single issuer.
+            const uint32_t mw = (uint32_t)(warp - 1);
             constexpr bool kMN = BASE == kDgrad;
             constexpr uint32_t kIdesc =
                 kPair ? idesc_e4m3_f32(2 * BM, BN, kMN) : idesc_e4m3_f32(BM, kMN ? 128 : BN, kMN);
@@ -468,6 +483,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 int m0, n0, kb0, kb1, grp, mo, rlim;
                 coords(t, m0, n0, kb0, kb1, grp, mo, rlim);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    if (it % kIssuers != mw) continue;  // the other issuer's slice
                     const int s = it % S;
                     const uint32_t use = it / S;
                     const int buf = it & 1;
