@@ -52,3 +52,19 @@ def assert_gemm_close(y_gpu, ref, what="gemm"):
 
 def bits(t):
     return wl.bf16_bits(t)
+
+
+def pair_tile_rows(M, seed=0):
+    """Output rows that reach every 256-row pair tile in both of its 128-row
+    halves (alternately the half's first row, its last row or a random one),
+    plus the matrix's first and last rows.  Whole rows are compared, so each
+    tile of the output is checked whatever order the tiles ran in."""
+    rng = np.random.default_rng(1000 + seed)
+    e = [0, M - 1]
+    for t0 in range(0, M, 256):
+        for h0 in (t0, t0 + 128):
+            pick = (t0 // 256) % 3
+            r = h0 if pick == 0 else h0 + 127 if pick == 1 else h0 + int(rng.integers(128))
+            if r < M:
+                e.append(r)
+    return e

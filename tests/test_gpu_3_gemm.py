@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from fp8_block_quantized_gb300 import workloads as wl
-from tests.gpu_util import assert_gemm_close, bits, host, to_dev
+from tests.gpu_util import assert_gemm_close, bits, host, pair_tile_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -39,22 +39,28 @@ def sample_rows(n, k, seed=0):
     return np.unique(r)
 
 
-def run_fwd(jet, x, w, nrows=None):
+def run_fwd(jet, x, w, nrows=None, rows=None):
     qx, sx, qw, sw = quant_pair(x, w)
     y = jet.gemm_fp8_fwd(to_dev(qx), to_dev(sx), to_dev(qw), to_dev(sw))
     torch.cuda.synchronize()
-    rows = sample_rows(qx.shape[0], nrows) if nrows else None
+    if rows is None:
+        rows = sample_rows(qx.shape[0], nrows) if nrows else None
+    else:
+        rows = np.unique(np.asarray(rows, np.int64))
     ref = oracle.gemm_fwd(qx, sx, qw, sw, rows=rows)
     assert_gemm_close(y if rows is None else y[torch.as_tensor(rows).cuda()], ref, "fwd")
     return y
 
 
-def run_dgrad(jet, dy, w, nrows=None):
+def run_dgrad(jet, dy, w, nrows=None, rows=None):
     qdy, sdy = oracle.quant_act_1x128(bits(dy))
     qw, sw = oracle.quant_w_128x128(bits(w))
     dx = jet.gemm_fp8_dgrad(to_dev(qdy), to_dev(sdy), to_dev(qw), to_dev(sw))
     torch.cuda.synchronize()
-    rows = sample_rows(qdy.shape[0], nrows) if nrows else None
+    if rows is None:
+        rows = sample_rows(qdy.shape[0], nrows) if nrows else None
+    else:
+        rows = np.unique(np.asarray(rows, np.int64))
     ref = oracle.gemm_dgrad(qdy, sdy, qw, sw, rows=rows)
     assert_gemm_close(dx if rows is None else dx[torch.as_tensor(rows).cuda()], ref, "dgrad")
     return dx
@@ -229,13 +235,32 @@ def test_train32b_kv_proj_wgrad(jet):
 
 
 def test_train8b_down_proj_fwd_dgrad_wgrad(jet):
-    """The widest contraction of the 8B layer (K = 14336) in all three products."""
+    """The widest contraction of the 8B layer (K = 14336) in all three
+    products.  Neither forward operand fits the tile order's L2 budget, so
+    its 16 column tiles run in two groups of 8: every pair tile is checked."""
     layer = wl.training_layer("train8b")
     d = layer[6]
     assert (d.name, d.M, d.N, d.K) == ("down", 8192, 4096, 14336)
-    run_fwd(jet, d.x, d.w, nrows=16)
+    run_fwd(jet, d.x, d.w, rows=pair_tile_rows(d.M))
     run_dgrad(jet, d.dy, d.w, nrows=16)
     run_wgrad(jet, d.dy, d.x, nrows=8)
+
+
+def test_train8b_gate_proj_dgrad_column_groups(jet):
+    """dX = dY_gate W_gate (8192 x 4096 over N = 14336): 16 column tiles in
+    two groups of 8, every pair tile checked."""
+    M, N, K = 8192, 14336, 4096
+    run_dgrad(jet, wl.grad_output(M, N, seed=0, config=2, tensor_id=204),
+              wl.weights(N, K, seed=0, config=2, tensor_id=104), rows=pair_tile_rows(M))
+
+
+def test_fwd_short_last_row_group(jet):
+    """Y = X W^T for 3712 x 3584 over K = 14336: neither operand fits the L2
+    budget and the 15 row tiles (the last one's second CTA past the last
+    row) run in groups of 8 and 7; every pair tile checked."""
+    M, N, K = 3712, 3584, 14336
+    run_fwd(jet, wl.activations(M, K, seed=1, config=2, tensor_id=3),
+            wl.weights(N, K, seed=1, config=2, tensor_id=106), rows=pair_tile_rows(M, 5))
 
 
 def test_train32b_gate_proj_fwd(jet):

@@ -5,15 +5,17 @@ same dequantized operands (|Y - ref| <= 2^-7 |ref| + 1e-3 rms(ref row)):
 * the down projection's forward (Y [16384, 5120], contraction 25600 = 200
   slices) and the gate projection's DGrad (contraction 25600): both operands
   are larger than the L2 budget of the tile order, so the tiles run in groups
-  of 16 row tiles (the third tile order), here with whole groups only;
-* the same products at 4224 rows, where the last group holds one row tile
-  (the short final group of that order);
-* the o projection's DGrad and the down projection's WGrad.
+  of column tiles (20 column tiles in groups of 7, 7 and 6);
+* the same products at 4224 rows (17 row tiles, the last one's second CTA
+  entirely past the last row);
+* the o projection's DGrad and the down projection's WGrad (dW rows: 20 row
+  tiles in two groups of 10).
 
 The operands are the oracle's own quantization of the seeded layer tensors
 (the tensor ids of the 32B training layer), copied to the device; the
-outputs are checked on sampled rows that always include the first and last
-rows of each raster group and of both CTAs of a CTA pair's 256-row tile.
+outputs are checked on whole rows: one row in each 128-row half of every
+256-row pair tile (so every tile of the output, whatever the tile order, is
+checked in both CTAs of its pair), the first and last rows, and random ones.
 ("Jet-RL ..." gist.science summary, "Quantisierungsschema": forward, DGrad
 and WGrad in FP8.)"""
 import numpy as np
@@ -22,7 +24,7 @@ import torch
 
 import oracle
 from fp8_block_quantized_gb300 import workloads as wl
-from tests.gpu_util import assert_gemm_close, bits, to_dev
+from tests.gpu_util import assert_gemm_close, bits, pair_tile_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -68,19 +70,9 @@ def dy_quant(name, M=M32):
 
 
 def checked_rows(M, extra, k=16, seed=0):
-    """k random rows plus the given rows (first/last rows of raster groups
-    and of the two 128-row halves of a pair tile)."""
+    """k random rows plus the given rows."""
     r = np.random.default_rng(seed).choice(M, k, replace=False)
     return np.unique(np.concatenate([r, np.asarray([x for x in extra if x < M])]))
-
-
-def group_edges(M, gm_rows=16 * 256):
-    """First and last rows of each raster group of 16 pair tiles, and the
-    last rows of the matrix."""
-    e = []
-    for g0 in range(0, M, gm_rows):
-        e += [g0, g0 + 127, g0 + 128, g0 + 255, min(M, g0 + gm_rows) - 1]
-    return e + [M - 129, M - 128, M - 1]
 
 
 def check(out, ref, rows, what):
@@ -93,7 +85,7 @@ def test_train32b_down_fwd_raster_groups(jet):
     qw, sw = w_quant("down")
     y = jet.gemm_fp8_fwd(to_dev(qx), to_dev(sx), to_dev(qw), to_dev(sw))
     torch.cuda.synchronize()
-    rows = checked_rows(M32, group_edges(M32))
+    rows = checked_rows(M32, pair_tile_rows(M32))
     check(y, oracle.gemm_fwd(qx, sx, qw, sw, rows=rows), rows, "down fwd 32B")
 
 
@@ -103,15 +95,15 @@ def test_train32b_gate_dgrad_raster_groups(jet):
     qw, sw = w_quant("gate")
     dx = jet.gemm_fp8_dgrad(to_dev(qdy), to_dev(sdy), to_dev(qw), to_dev(sw))
     torch.cuda.synchronize()
-    rows = checked_rows(M32, group_edges(M32), seed=1)
+    rows = checked_rows(M32, pair_tile_rows(M32, 1), seed=1)
     check(dx, oracle.gemm_dgrad(qdy, sdy, qw, sw, rows=rows), rows, "gate dgrad 32B")
 
 
 @pytest.mark.parametrize("M", [4224])
 def test_short_last_raster_group(jet, M):
-    """17 pair tiles of rows: one whole group of 16 and a last group of one
-    (whose second CTA lies entirely past the last row), for the forward and
-    the DGrad of the widest contraction."""
+    """17 pair tiles of rows, the last one's second CTA entirely past the
+    last row, for the forward and the DGrad of the widest contraction
+    (column groups of 7, 7 and 6)."""
     qx, sx = x_quant(3, 25600, M=M)
     qw, sw = w_quant("down")
     y = jet.gemm_fp8_fwd(to_dev(qx), to_dev(sx), to_dev(qw), to_dev(sw))
@@ -119,7 +111,7 @@ def test_short_last_raster_group(jet, M):
     qg, sg = w_quant("gate")
     dx = jet.gemm_fp8_dgrad(to_dev(qdy), to_dev(sdy), to_dev(qg), to_dev(sg))
     torch.cuda.synchronize()
-    rows = checked_rows(M, group_edges(M) + list(range(4096, 4224, 9)), k=8, seed=2)
+    rows = checked_rows(M, pair_tile_rows(M, 2) + list(range(4096, 4224, 9)), k=8, seed=2)
     check(y, oracle.gemm_fwd(qx, sx, qw, sw, rows=rows), rows, "fwd, short group")
     check(dx, oracle.gemm_dgrad(qdy, sdy, qg, sg, rows=rows), rows, "dgrad, short group")
 
@@ -143,5 +135,5 @@ def test_train32b_down_wgrad(jet):
     qdyT, sdyT = oracle.requant_128x1(qdy, sdy)
     dw = jet.gemm_fp8_wgrad(to_dev(qdyT), to_dev(sdyT), to_dev(qxT), to_dev(sxT))
     torch.cuda.synchronize()
-    rows = checked_rows(5120, [0, 127, 128, 255, 5119], seed=4)
+    rows = checked_rows(5120, pair_tile_rows(5120, 4), seed=4)
     check(dw, oracle.gemm_wgrad(qdyT, sdyT, qxT, sxT, rows=rows), rows, "down wgrad 32B")

@@ -102,3 +102,22 @@ def test_rows_and_groups_are_independent():
     assert np.array_equal(qp, q[perm]) and np.array_equal(sp, s[:, perm])
     q2, s2 = oracle.swiglu_quant_1x128(gb[:, 256:384], ub[:, 256:384])
     assert np.array_equal(q2, q[:, 256:384]) and np.array_equal(s2[0], s[2])
+
+
+def test_reciprocal_seed_constant_is_the_balanced_linear_seed():
+    """The seed 0x7EF311C7 - bits(d) of the silu's reciprocal is the
+    bit-pattern seed whose relative error over a binade equioscillates:
+    about +-5.05%, equal at both ends to 1e-5, so that three Newton steps
+    (error squared each time) leave 1/d to below 1e-10 in exact arithmetic.
+    Any other constant nearby unbalances the two extremes."""
+    d = np.linspace(1.0, 4.0, 3_000_001, dtype=np.float32)  # two binades
+    def seed_err(c):
+        y = (np.uint32(c) - d.view(np.uint32)).view(np.float32).astype(np.float64)
+        return y * d.astype(np.float64) - 1.0
+    e = seed_err(0x7EF311C7)
+    assert 0.0504 < e.max() < 0.0506 and -0.0506 < e.min() < -0.0504
+    assert abs(e.max() + e.min()) < 1e-5
+    for c in (0x7EF00000, 0x7EF80000):
+        f = seed_err(c)
+        assert abs(f.max() + f.min()) > 1e-3
+    assert np.abs(e).max() ** 8 < 1e-10
