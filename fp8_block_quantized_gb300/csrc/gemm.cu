@@ -24,7 +24,10 @@
 //              of BN columns (warp 1 the even slices, warp 2 the odd ones),
 //              then commit to the stage's "empty" and the accumulator's
 //              "full" barriers.
-//   warp 3     idle.  Warpgroup 0 (warps 0-3) gives registers back
+//   warp 3     pair kernel: issues each finished tile's TMA stores once the
+//              promotion warps have staged it (a store's issue can hold its
+//              thread for 800-1500 cycles); otherwise idle.
+//              Warpgroup 0 (warps 0-3) gives registers back
 //              (setmaxnreg 72) so that the epilogue warpgroups can hold their
 //              accumulators (setmaxnreg 200): 128*72 + 256*200 <= 384 * 168,
 //              the allocation the block is launched with.
@@ -162,6 +165,12 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, Ras
 // because splits <= nkb.
 __device__ __forceinline__ void unit_coords(int t, int splits, int nkb, int tiles_m, int tiles_n,
                                             Raster r, int &mt, int &nt, int &kb0, int &kb1) {
+    if (splits == 1) {  // the common case, without its two divisions
+        tile_coords(t, tiles_m, tiles_n, r, mt, nt);
+        kb0 = 0;
+        kb1 = nkb;
+        return;
+    }
     const int tile = t / splits, sp = t - tile * splits;
     tile_coords(tile, tiles_m, tiles_n, r, mt, nt);
     kb0 = sp * nkb / splits;
@@ -235,6 +244,11 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     constexpr uint16_t kPairMask = 0x3;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ uint64_t full_bar[S], empty_bar[S], tfull_bar[2], tempty_bar[2], drain_bar;
+    // Output stores of the pair kernel: the promotion warps stage a tile and
+    // arrive on "staged"; warp 3 issues the TMA stores, waits until they have
+    // read the staging buffers and arrives on "staging free".
+    constexpr bool kStoreWarp = CL == 2 && !is_grouped(MODE);
+    __shared__ uint64_t staged_bar, sfree_bar;
     __shared__ uint64_t sfull_bar[SS], sempty_bar[SS];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -282,6 +296,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(&tempty_bar[b], 8 * CL);  // epilogue warps of every CTA of the pair
         }
         mbar_init(&drain_bar, kIssuers);  // one drain commit per MMA-issuing warp
+        mbar_init(&staged_bar, 8);         // one arrival per epilogue warp
+        mbar_init(&sfree_bar, 1);          // the store warp
         abort_sh = 0;
         fence_mbar_init();
     }
@@ -554,6 +570,33 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             __syncwarp();
             mbar_wait(&drain_bar, 0, nullptr, status, SITE_GEMM_DRAIN);
+        } else if (warp == 3 && kStoreWarp) {
+            // -------------------------------------------------- output stores
+            // Issuing a TMA store can hold the issuing thread for 800-1500
+            // cycles (measured) while the TMA unit works through the operand
+            // loads; here that wait is off the promotion warps' path.
+            uint32_t j = 0;
+            for (int t = unit0; t < total; t += unit_step, ++j) {
+                int m0, n0, kb0, kb1, grp, mo, rlim;
+                coords(t, m0, n0, kb0, kb1, grp, mo, rlim);
+                if (!pwait(&staged_bar, j & 1u, SITE_GEMM_EPI_TMEM_FULL)) break;
+                if (lane == 0) {
+                    const uint64_t pol_out = policy_evict_first();  // not re-read here
+#pragma unroll 1
+                    for (int ew = 0; ew < 8; ++ew) {
+                        const uint32_t wbuf = out_base + ew * CF::kOutWarpBytes;
+                        const int col0 = n0 + (ew >> 2) * CF::kHalf, row0 = mo + (ew & 3) * 32;
+#pragma unroll
+                        for (int h = 0; h < CF::kHalf / 64; ++h)
+                            tma_store_2d_hint(&tmY, wbuf + 4096 * h, col0 + 64 * h, row0, pol_out);
+                    }
+                    bulk_commit_group();
+                    bulk_wait_group_read0();  // the staging buffers have been read
+                    mbar_arrive(&sfree_bar);
+                }
+                __syncwarp();
+            }
+            if (lane == 0) bulk_wait_group0();  // every store complete before exit
         }
     } else {
         reg_alloc<kRegsEpilogue>();
@@ -571,7 +614,8 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         uint32_t it = 0;
         bool ok = true;
-        for (int t = unit0; ok && t < total; t += unit_step) {
+        uint32_t tile_j = 0;  // this CTA's tiles so far (store-warp hand-off phases)
+        for (int t = unit0; ok && t < total; t += unit_step, ++tile_j) {
             int m0, n0, kb0, kb1, grp, mo, rlim;
             coords(t, m0, n0, kb0, kb1, grp, mo, rlim);
             const int row = mo + quad * 32 + lane;  // output row
@@ -656,8 +700,16 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // grouped tile's warp whose rows cross its expert's end takes
                 // the plain stores below instead.)
                 const uint32_t wbuf = out_base + ew * CF::kOutWarpBytes;
-                if (lane == 0) bulk_wait_group_read0();  // previous tile's stores have read it
-                __syncwarp();
+                if constexpr (kStoreWarp) {
+                    // the store warp has read out the previous tile's staging
+                    if (!pwait(&sfree_bar, (tile_j & 1u) ^ 1u, SITE_GEMM_EPI_TMEM_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                } else {
+                    if (lane == 0) bulk_wait_group_read0();  // previous tile's stores have read it
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int i = 0; i < H / 8; ++i) {
                     uint4 v;
@@ -673,7 +725,9 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) {
+                if constexpr (kStoreWarp) {
+                    if (lane == 0) mbar_arrive(&staged_bar);
+                } else if (lane == 0) {
 #pragma unroll
                     for (int h = 0; h < H / 64; ++h)
                         tma_store_2d_hint(&tmY, wbuf + 4096 * h, col0 + 64 * h, mo + quad * 32,
