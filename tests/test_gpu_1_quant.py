@@ -119,6 +119,17 @@ def test_w_gate_sampled_block_rows(jet):
     check_w(jet, wl.weights(14336, 4096, seed=0, config=5, tensor_id=104), [0, 5, 57, 111])
 
 
+@pytest.mark.parametrize("layer", [0, 13, 31])
+def test_w_sync_layer_every_weight_sampled(jet, layer):
+    """Weight sync (the 32-layer 8B model's weights, seeded as the sync
+    workload draws them): every one of the layer's 7 weights, 3 block rows
+    each (the first, the last and one in between), bit-exact."""
+    for i, (name, N, K) in enumerate(wl.LLAMA8B_LINEARS):
+        w = wl.weights(N, K, seed=0, config=5, tensor_id=1000 + 10 * layer + i)
+        nb = N // 128
+        check_w(jet, w, sorted({0, (layer * 7 + i * 13) % nb, nb - 1}))
+
+
 def test_w_identity_and_zero(jet):
     w = torch.zeros((256, 256))
     w[:128, :128] = torch.eye(128) * 448.0

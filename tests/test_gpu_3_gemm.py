@@ -228,6 +228,40 @@ def test_train8b_q_proj_fwd_dgrad_wgrad(jet):
     run_wgrad(jet, q.dy, q.x, nrows=16)
 
 
+def run_wgrad_rows(jet, dy, x, rows):
+    qx, sx = oracle.quant_act_1x128(bits(x))
+    qdy, sdy = oracle.quant_act_1x128(bits(dy))
+    qxT, sxT = oracle.requant_128x1(qx, sx)
+    qdyT, sdyT = oracle.requant_128x1(qdy, sdy)
+    dw = jet.gemm_fp8_wgrad(to_dev(qdyT), to_dev(sdyT), to_dev(qxT), to_dev(sxT))
+    torch.cuda.synchronize()
+    rows = np.unique(np.asarray(rows, np.int64))
+    ref = oracle.gemm_wgrad(qdyT, sdyT, qxT, sxT, rows=rows)
+    assert_gemm_close(dw[torch.as_tensor(rows).cuda()], ref, "wgrad")
+
+
+def test_train8b_gate_proj_wgrad_every_pair_tile(jet):
+    """dW_gate = dY^T X (14336 x 4096 over 8192 tokens): one row in each
+    128-row half of every one of the 56 pair tiles of dW rows."""
+    layer = wl.training_layer("train8b")
+    g = layer[4]
+    assert (g.name, g.M, g.N, g.K) == ("gate", 8192, 14336, 4096)
+    run_wgrad_rows(jet, g.dy, g.x, pair_tile_rows(g.N, 6))
+
+
+@pytest.mark.parametrize("name,N,K", [("o", 5120, 8192), ("q", 8192, 5120)])
+def test_train32b_wgrad_groups_every_pair_tile(jet, name, N, K):
+    """32B-layer WGrad over 16384 tokens whose operands both exceed the tile
+    order's L2 budget: dW rows in groups (o: 20 row tiles in groups of 10)
+    or columns in groups (q: 20 column tiles in groups of 10); one row in
+    each half of every pair tile."""
+    M = 16384
+    idx = [n for n, _, _ in wl.DENSE32B_LINEARS].index(name)
+    run_wgrad_rows(jet, wl.grad_output(M, N, seed=0, config=4, tensor_id=200 + idx),
+                   wl.activations(M, K, seed=0, config=4, tensor_id=7 + idx),
+                   pair_tile_rows(N, 7))
+
+
 def test_train32b_kv_proj_wgrad(jet):
     M, N, K = 16384, 1024, 5120
     run_wgrad(jet, wl.grad_output(M, N, seed=0, config=4, tensor_id=201),
