@@ -147,6 +147,52 @@ rmsnorm_quant_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict_
     }
 }
 
+// Few rows (decode: fewer rows than SMs): one CTA per row.  Its 8 warps load
+// the row into shared memory in one round trip, warp 0 forms the sum of
+// squares from there in the order above, and the 8 warps then quantize the
+// row's chunks j = w, w + 8, ... (the same group arithmetic) - so a row no
+// longer costs one warp's whole dependent chain.  Rows of at most
+// kRnRowCtaMaxK elements (the row's BF16 in dynamic shared memory).
+constexpr int64_t kRnRowCtaMaxK = 32768;
+
+__global__ void __launch_bounds__(kRnThreads)
+rmsnorm_quant_row_cta_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ g,
+                             int64_t M, int64_t K, float eps, uint8_t *__restrict__ q,
+                             float *__restrict__ s) {
+    extern __shared__ uint4 rowbuf[];  // the row's K / 8 chunks of 8 BF16
+    __shared__ float nr_sh;
+    jet::griddep_launch_dependents();
+    jet::griddep_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t nchunks = K / 8;
+    const int64_t nj = (nchunks + 31) / 32;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const uint4 *gain = reinterpret_cast<const uint4 *>(g);
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(x + m * K);
+        for (int64_t ci = threadIdx.x; ci < nchunks; ci += kRnThreads) rowbuf[ci] = row[ci];
+        __syncthreads();
+        if (warp == 0) {
+            float acc = 0.0f;
+            for (int64_t j = 0; j < nj; ++j) {
+                const int64_t ci = 32 * j + lane;
+                acc = add_squares(acc, ci < nchunks ? rowbuf[ci] : zero);
+            }
+            const float nr = -rms_factor(acc, K, eps);
+            if (lane == 0) nr_sh = nr;
+        }
+        __syncthreads();
+        const float nr = nr_sh;
+        for (int64_t j = warp; j < nj; j += kRnThreads / 32) {  // warp-uniform
+            const int64_t ci = 32 * j + lane;
+            const bool ok = ci < nchunks;
+            quant_chunk(ok ? rowbuf[ci] : zero, ok ? gain[ci] : zero, nr, ok,
+                        2 * j + (lane >> 4), m, M, K, lane, q, s);
+        }
+        __syncthreads();  // the next row overwrites rowbuf and nr_sh
+    }
+}
+
 }  // namespace
 
 jet_status jet_rmsnorm_quant_1x128(const uint16_t *x, const uint16_t *g, int64_t M, int64_t K,
@@ -163,6 +209,20 @@ jet_status jet_rmsnorm_quant_1x128(const uint16_t *x, const uint16_t *g, int64_t
     jet_status st = jet::current_device(&dev);
     if (st != JET_OK) return st;
     if (empty) return JET_OK;
+    if (M <= 2 * (int64_t)dev.num_sms && K <= kRnRowCtaMaxK) {
+        static bool attr_set[64] = {};
+        if (!attr_set[dev.ordinal]) {
+            if (cudaFuncSetAttribute(rmsnorm_quant_row_cta_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kRnRowCtaMaxK * 2)) != cudaSuccess) {
+                cudaGetLastError();
+                return JET_ERR_CUDA;
+            }
+            attr_set[dev.ordinal] = true;
+        }
+        return jet::launch_pdl(rmsnorm_quant_row_cta_kernel, dim3((unsigned)M), dim3(kRnThreads),
+                               (size_t)K * 2, jet::as_stream(stream), x, g, M, K, eps, q, s);
+    }
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rmsnorm_quant_kernel, kRnThreads,
                                                       0) != cudaSuccess ||
