@@ -97,7 +97,7 @@ static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168,
 constexpr int BM = 128;  // output rows per tile (TMEM lanes)
 constexpr int BK = 128;  // contraction slice = one scale block
 
-template <int BN, int CL, bool STAGED>
+template <int BN, int CL, bool STAGED, int ST = 0>
 struct Cfg {
     // Per CTA and stage: A's 128 rows and B's BN (CL = 1) or BN/2 (pair) rows.
     static constexpr int kBRows = BN / CL;
@@ -115,9 +115,14 @@ struct Cfg {
     // while the stores drain.
     static constexpr int kOutWarpBytes = 32 * 128 * 2;
     static constexpr int kOutBytes = STAGED ? 8 * kOutWarpBytes : 0;
-    // four operand stages where they fit beside the staging, else three
+    // four operand stages where they fit beside the staging, else three;
+    // ST > 0 asks for ST stages (the deep split-contraction kernel: six
+    // 32 KB stages keep 96 KB of weights in flight per SM)
     static constexpr int kStages =
-        4 * kStageBytes + kOutBytes + kScaleSlots * kScaleSlotBytes + 1024 <= 227 * 1024 ? 4 : 3;
+        ST > 0 ? ST
+               : (4 * kStageBytes + kOutBytes + kScaleSlots * kScaleSlotBytes + 1024 <= 227 * 1024
+                      ? 4
+                      : 3);
     static constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes +
                                       kScaleSlots * kScaleSlotBytes + 1024;  // + alignment slack
     static constexpr int kTmemCols = 2 * BN;                           // two accumulators
@@ -226,7 +231,7 @@ __device__ __forceinline__ void load_cs(float4 (&cs)[4], const float *src) {
 // leader's commits arrive on both CTAs' "empty" and "TMEM full" barriers; both
 // CTAs' promotion warps release the leader's "TMEM empty" barrier; each CTA
 // promotes and stores its own 128 rows from its own TMEM.
-template <int BN, int MODE, int CL>
+template <int BN, int MODE, int CL, int ST = 0>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const float *__restrict__ sa,
@@ -234,7 +239,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 uint16_t *__restrict__ out, int R, int C, int D, Raster raster, int splits,
                 float *__restrict__ partial, const int64_t *__restrict__ goff, int gE,
                 unsigned *status, uint64_t wait_limit) {
-    using CF = Cfg<BN, CL, CL == 2 || is_grouped(MODE)>;
+    using CF = Cfg<BN, CL, CL == 2 || is_grouped(MODE), ST>;
     constexpr int S = CF::kStages;
     // MMA-issuing warps (see the MMA role): two when every stage and every
     // TMEM accumulator is used by one issuer only, i.e. an even stage count.
@@ -916,13 +921,13 @@ Raster choose_raster(int64_t R, int64_t C, int64_t D, int64_t rows, int64_t cols
 // Kernel arguments are passed by value; a CUtensorMap goes as is.
 inline const CUtensorMap &tmA_arg(const CUtensorMap &m) { return m; }
 
-template <int BN, int MODE, int CL>
+template <int BN, int MODE, int CL, int ST = 0>
 jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, const uint8_t *b,
                   const float *sb, uint16_t *out, int64_t R, int64_t C, int64_t D, int splits,
                   float *partial, cudaStream_t stream, const int64_t *goff = nullptr,
                   int gE = 0, uint64_t wait_limit = kWaitLimitCycles) {
-    using CF = Cfg<BN, CL, CL == 2 || is_grouped(MODE)>;
-    auto kernel = gemm_fp8_kernel<BN, MODE, CL>;
+    using CF = Cfg<BN, CL, CL == 2 || is_grouped(MODE), ST>;
+    auto kernel = gemm_fp8_kernel<BN, MODE, CL, ST>;
     static std::mutex mu;
     static int max_units[64] = {};  // co-resident CTAs (CL = 1) or clusters (CL = 2)
     cudaLaunchConfig_t cfg = {};
@@ -1000,33 +1005,58 @@ jet_status launch(const DeviceInfo &dev, const uint8_t *a, const float *sa, cons
     return launch_status();
 }
 
-// Number of contraction ranges for an R x C x D product (1 = no split).
-// Products of at most 512 rows (decode and short prefill) have too few
-// output tiles for 152 SMs; they run on the single-CTA kernel with the
-// contraction cut into ranges of whole 128-slices: about 128 units in all,
-// at most 8 ranges per tile, at most one per slice, and FP32 partials
-// (4 * splits * R * C bytes, written and read back by the reduction) of at
-// most 32 MB, so that they stay in L2.  Measured on the 8B projections at 16,
-// 64 and 256 tokens against every split count from 1 to 32 (weights streamed
-// from DRAM): this count was the fastest or within 3% of it, except q at 64
-// tokens (8%); more units cost more than they gain (each unit restarts the
-// pipeline and adds a partial to reduce).  One range means no split (and
-// rows above 128 then take the CTA-pair kernel).  It depends only on the
-// sizes, never on the device, so the workspace size and the summation order
-// (hence the result) are the same on every GPU.
+// How an R x C x D product of at most 512 rows (decode and short prefill) is
+// cut.  Such a product has too few output tiles for 152 SMs; it runs on the
+// single-CTA kernel with the contraction cut into ranges of whole
+// 128-slices: about 128 units in all, at most 8 ranges per tile, at most one
+// per slice, and FP32 partials (4 * splits * R * C bytes, written and read
+// back by the reduction) of at most 32 MB, so that they stay in L2.  Tiles
+// are 128 wide when that count is at least 2 (q, k, v, o and down of the 8B
+// and 32B layers), else 256 wide (gate and up up to 128 rows); one range
+// means no split (and rows above 128 then take the CTA-pair kernel).  A
+// 128-wide unit of at least 8 slices on at most 64 rows, or of at least 24
+// slices, runs on the six-stage kernel: there the weights stream from DRAM
+// and the stages in flight set the rate, while on short units the larger
+// shared-memory footprint cost 8-13% (k and v at 128-512 rows).  Measured on
+// the 7 projections of both layers at 16 to 512 rows (weights streamed from
+// DRAM): against 256-wide tiles throughout, 128-wide tiles took 12-38% less
+// time on k and v at every row count and 10-30% on q, o and down at 32-256
+// rows, and lost 10% on the 32B q at 16 rows; with fewer ranges per tile
+// each unit runs a longer pipeline and the reduction reads fewer partials.
+// The plan depends only on the sizes, never on the device, so the workspace
+// size and the summation order (hence the result) are the same on every GPU.
 constexpr int64_t kSplitMaxRows = 512;
 
-int splitk_splits(int64_t R, int64_t C, int64_t D) {
+struct SplitPlan {
+    int splits;  // contraction ranges per output tile (1 = no split)
+    int bn;      // tile width of a split product
+    bool deep;   // six operand stages
+};
+
+int64_t split_count(int64_t R, int64_t C, int64_t D, int64_t bn) {
     constexpr int64_t kTargetUnits = 128, kMaxSplits = 8;
     constexpr int64_t kPartialBudget = 32ll << 20;
-    if (R <= 0 || R > kSplitMaxRows || C <= 0 || D <= 0 || C % 128 != 0 || D % BK != 0) return 1;
-    const int64_t tiles = (R + BM - 1) / BM * (C / (C % 256 == 0 ? 256 : 128));
+    const int64_t tiles = (R + BM - 1) / BM * (C / bn);
     int64_t s = kTargetUnits / tiles;
     if (s > kMaxSplits) s = kMaxSplits;
     if (s > D / BK) s = D / BK;
     while (s > 1 && 4 * s * R * C > kPartialBudget) --s;
-    return s >= 2 ? (int)s : 1;
+    return s;
 }
+
+SplitPlan split_plan(int64_t R, int64_t C, int64_t D) {
+    if (R <= 0 || R > kSplitMaxRows || C <= 0 || D <= 0 || C % 128 != 0 || D % BK != 0)
+        return SplitPlan{1, 0, false};
+    int64_t s = split_count(R, C, D, 128);
+    if (s >= 2) {
+        const int64_t slices = D / BK / s;
+        return SplitPlan{(int)s, 128, (slices >= 8 && R <= 64) || slices >= 24};
+    }
+    if (C % 256 == 0 && (s = split_count(R, C, D, 256)) >= 2) return SplitPlan{(int)s, 256, false};
+    return SplitPlan{1, 0, false};
+}
+
+int splitk_splits(int64_t R, int64_t C, int64_t D) { return split_plan(R, C, D).splits; }
 
 size_t splitk_workspace(int64_t R, int64_t C, int64_t D) {
     const int s = splitk_splits(R, C, D);
@@ -1045,17 +1075,26 @@ jet_status run_gemm(const uint8_t *a, const float *sa, const uint8_t *b, const f
         return cudaMemsetAsync(out, 0, (size_t)R * C * 2, stream) == cudaSuccess ? JET_OK
                                                                                : JET_ERR_CUDA;
     }
-    // A split contraction runs on the single-CTA kernel; otherwise the pair
-    // MMA (256 x 256 per CTA pair) whenever there are at least two row tiles
-    // and the output is a multiple of 256 wide.
-    const int splits = MODE == kWgrad ? 1 : splitk_splits(R, C, D);
-    float *partial = splits > 1 ? static_cast<float *>(ws) : nullptr;
-    if (C % 256 == 0) {
-        if (R > BM && splits == 1)
-            return launch<256, MODE, 2>(dev, a, sa, b, sb, out, R, C, D, 1, nullptr, stream);
-        return launch<256, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, splits, partial, stream);
+    // A split contraction runs on the single-CTA kernel (see split_plan);
+    // otherwise the pair MMA (256 x 256 per CTA pair) whenever there are at
+    // least two row tiles and the output is a multiple of 256 wide.
+    const SplitPlan plan = MODE == kWgrad ? SplitPlan{1, 0, false} : split_plan(R, C, D);
+    if (plan.splits > 1) {
+        float *partial = static_cast<float *>(ws);
+        if (plan.bn == 256)
+            return launch<256, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, plan.splits, partial,
+                                        stream);
+        if (plan.deep)
+            return launch<128, MODE, 1, 6>(dev, a, sa, b, sb, out, R, C, D, plan.splits,
+                                           partial, stream);
+        return launch<128, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, plan.splits, partial,
+                                    stream);
     }
-    return launch<128, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, splits, partial, stream);
+    if (C % 256 == 0) {
+        if (R > BM) return launch<256, MODE, 2>(dev, a, sa, b, sb, out, R, C, D, 1, nullptr, stream);
+        return launch<256, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, 1, nullptr, stream);
+    }
+    return launch<128, MODE, 1>(dev, a, sa, b, sb, out, R, C, D, 1, nullptr, stream);
 }
 
 constexpr int64_t kMaxDim = (int64_t)1 << 30;

@@ -52,28 +52,29 @@ def test_workspace_bytes(lib):
                  "gemm_fp8_fwd", "gemm_fp8_dgrad", "gemm_fp8_wgrad"):
         assert lib.jet_workspace_bytes(op[name], 8192, 4096, 4096) == 0
     # split contraction for at most 512 output rows: FP32 partials [splits][R][C];
-    # about 128 units, at most 8 ranges per tile, partials at most 32 MB
+    # about 128 units of 128-wide tiles (of 256-wide ones when that gives one),
+    # at most 8 ranges per tile, partials at most 32 MB
     fwd, dgrad, wgrad = op["gemm_fp8_fwd"], op["gemm_fp8_dgrad"], op["gemm_fp8_wgrad"]
     assert lib.jet_workspace_bytes(fwd, 1, 4096, 4096) == 0                     # decode kernel
     assert lib.jet_workspace_bytes(fwd, 1, 14336, 4096) == 0                    # one token: always
     assert lib.jet_workspace_bytes(fwd, 2, 4096, 4096) == 0                     # M N K = 2^25
     assert lib.jet_workspace_bytes(fwd, 4, 1024, 4096) == 0
-    assert lib.jet_workspace_bytes(fwd, 4, 4096, 4096) == 8 * 4 * 4096 * 4      # 16 tiles
-    assert lib.jet_workspace_bytes(fwd, 2, 14336, 4096) == 2 * 2 * 14336 * 4    # 56 tiles
-    assert lib.jet_workspace_bytes(fwd, 5, 4096, 4096) == 8 * 5 * 4096 * 4
-    assert lib.jet_workspace_bytes(fwd, 64, 4096, 4096) == 8 * 64 * 4096 * 4
+    assert lib.jet_workspace_bytes(fwd, 4, 4096, 4096) == 4 * 4 * 4096 * 4      # 32 tiles
+    assert lib.jet_workspace_bytes(fwd, 2, 14336, 4096) == 2 * 2 * 14336 * 4    # 112: 56 of 256
+    assert lib.jet_workspace_bytes(fwd, 5, 4096, 4096) == 4 * 5 * 4096 * 4
+    assert lib.jet_workspace_bytes(fwd, 64, 4096, 4096) == 4 * 64 * 4096 * 4
     assert lib.jet_workspace_bytes(fwd, 64, 14336, 4096) == 2 * 64 * 14336 * 4
-    assert lib.jet_workspace_bytes(fwd, 16, 1024, 4096) == 8 * 16 * 1024 * 4    # 4 tiles: at most 8
+    assert lib.jet_workspace_bytes(fwd, 16, 1024, 4096) == 8 * 16 * 1024 * 4    # 8 tiles: at most 8
     assert lib.jet_workspace_bytes(fwd, 128, 128, 128) == 0                     # one slice
-    assert lib.jet_workspace_bytes(fwd, 129, 4096, 4096) == 4 * 129 * 4096 * 4  # two row tiles
-    assert lib.jet_workspace_bytes(fwd, 256, 4096, 14336) == 4 * 256 * 4096 * 4
+    assert lib.jet_workspace_bytes(fwd, 129, 4096, 4096) == 2 * 129 * 4096 * 4  # two row tiles
+    assert lib.jet_workspace_bytes(fwd, 256, 4096, 14336) == 2 * 256 * 4096 * 4
     assert lib.jet_workspace_bytes(fwd, 513, 4096, 14336) == 0                  # pair kernel
-    assert lib.jet_workspace_bytes(fwd, 256, 14336, 4096) == 0                  # 112 tiles
-    assert lib.jet_workspace_bytes(fwd, 128, 4096, 1024) == 8 * 128 * 4096 * 4  # one slice each
-    assert lib.jet_workspace_bytes(fwd, 512, 4096, 14336) == 2 * 512 * 4096 * 4  # 64 tiles
-    assert lib.jet_workspace_bytes(fwd, 512, 8192, 4096) == 0                   # 128 tiles
+    assert lib.jet_workspace_bytes(fwd, 256, 14336, 4096) == 0                  # 112 of 256
+    assert lib.jet_workspace_bytes(fwd, 128, 4096, 1024) == 4 * 128 * 4096 * 4  # two slices each
+    assert lib.jet_workspace_bytes(fwd, 512, 4096, 14336) == 2 * 512 * 4096 * 4  # 64 of 256
+    assert lib.jet_workspace_bytes(fwd, 512, 8192, 4096) == 0                   # 128 of 256
     assert lib.jet_workspace_bytes(dgrad, 16, 4096, 1024) == 8 * 16 * 1024 * 4  # C = K = 1024
-    assert lib.jet_workspace_bytes(dgrad, 16, 1024, 4096) == 8 * 16 * 4096 * 4
+    assert lib.jet_workspace_bytes(dgrad, 16, 1024, 4096) == 4 * 16 * 4096 * 4
     assert lib.jet_workspace_bytes(wgrad, 128, 128, 4096) == 0
     m = op["token_mult_prob_error"]
     assert lib.jet_workspace_bytes(m, 1, 0, 0) == 8

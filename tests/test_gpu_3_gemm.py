@@ -137,11 +137,15 @@ def test_wgrad_shapes(jet, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 512, 1024), (1, 4096, 1024), (100, 2048, 384),
-                                   (128, 4096, 1024), (256, 4096, 1024), (300, 8192, 512)])
+                                   (128, 4096, 1024), (256, 4096, 1024), (300, 8192, 512),
+                                   (16, 4096, 4096), (16, 4096, 14336)])
 def test_dgrad_small_rows_split_contraction(jet, M, N, K):
-    # at most 512 rows: the contraction (N) is split into ranges of 128-slices
+    # at most 512 rows: the contraction (N) is split into ranges of 128-slices;
+    # 16 x 4096 x 4096 runs 8-slice ranges on the six-stage 128-wide kernel,
+    # 16 x 4096 x 14336 (112 tiles of 128) two ranges of 256-wide tiles
     assert jet.workspace_bytes("gemm_fp8_dgrad", M, N, K) > 0
-    run_dgrad(jet, wl.grad_output(M, N, seed=M + N, config=3), wl.weights(N, K, seed=K, config=3))
+    run_dgrad(jet, wl.grad_output(M, N, seed=M + N, config=3), wl.weights(N, K, seed=K, config=3),
+              nrows=None if M * K <= 16 * 4096 else 8)
 
 
 def test_split_contraction_deterministic_and_workspace_agnostic(jet):
