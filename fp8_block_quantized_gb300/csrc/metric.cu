@@ -1,7 +1,10 @@
 // token-mult-prob-error = (1/n) * sum_i exp(|logp_train_i - logp_rollout_i|)
 // ("NVIDIA强化学习加速实操：10分钟提升2倍训练效率", section
 // "FP8面临的关键挑战：数值分歧").  Two passes: a grid of G blocks streams the two
-// FP32 vectors with 16-byte loads, sums exp|a-b| in FP32 per thread and in
+// FP32 vectors with 16-byte loads (each thread issues the loads of kUnroll
+// grid strides before using them, so its share of the vectors is in flight
+// at once rather than one round trip per stride; the order of its sums is
+// the stride order either way), sums exp|a-b| in FP32 per thread and in
 // FP64 across the block, and stores one FP64 partial per block in the
 // workspace; one block then adds the G partials in a fixed order (so the
 // result is deterministic) and writes the mean as FP32.
@@ -14,6 +17,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxBlocks = 1024;
 constexpr int64_t kElemsPerBlockTarget = 2048;
+constexpr int kUnroll = 4;  // grid strides whose loads a thread issues together
 
 __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
     float4 v;
@@ -23,6 +27,7 @@ __device__ __forceinline__ float4 ld_stream_f4(const float *p) {
     return v;
 }
 
+// FP64 sum over the block (the second passes, one block each).
 __device__ __forceinline__ double block_sum(double v) {
     __shared__ double warp_sum[kThreads / 32];
 #pragma unroll
@@ -35,6 +40,38 @@ __device__ __forceinline__ double block_sum(double v) {
     return t;  // valid in thread 0
 }
 
+// Sum over the block of one FP32 value per thread (the first passes, run by
+// every block): a butterfly over each warp in FP32 (every lane ends with the
+// same bits, additions being commutative), then the warps' sums in FP64 by
+// thread 0 in warp order.  FP64 arithmetic is scarce on this GPU: the same
+// tree in FP64 on every thread took about 40% of the per-sequence pass.  The
+// FP32 tree adds at most 5 roundings (under 3.1e-7 relative) to a sum of
+// positive terms.
+__device__ __forceinline__ double block_sum_f(float v) {
+    __shared__ double warp_sum[kThreads / 32];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = (double)v;
+    __syncthreads();
+    double t = 0.0;
+    if (threadIdx.x == 0)
+        for (int i = 0; i < kThreads / 32; ++i) t += warp_sum[i];
+    return t;  // valid in thread 0
+}
+
+// Exact integer sum over the block (token counts).
+__device__ __forceinline__ long long block_count(int c) {
+    __shared__ long long warp_cnt[kThreads / 32];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+    if ((threadIdx.x & 31) == 0) warp_cnt[threadIdx.x >> 5] = c;
+    __syncthreads();
+    long long t = 0;
+    if (threadIdx.x == 0)
+        for (int i = 0; i < kThreads / 32; ++i) t += warp_cnt[i];
+    return t;  // valid in thread 0
+}
+
 __global__ void __launch_bounds__(kThreads)
 tmpe_partial_kernel(const float *__restrict__ a, const float *__restrict__ b, int64_t n,
                     double *__restrict__ partial) {
@@ -44,16 +81,29 @@ tmpe_partial_kernel(const float *__restrict__ a, const float *__restrict__ b, in
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     const int64_t n4 = n >> 2;
-    for (int64_t i = tid; i < n4; i += stride) {
-        const float4 x = ld_stream_f4(a + 4 * i);
-        const float4 y = ld_stream_f4(b + 4 * i);
-        acc += expf(fabsf(x.x - y.x));
-        acc += expf(fabsf(x.y - y.y));
-        acc += expf(fabsf(x.z - y.z));
-        acc += expf(fabsf(x.w - y.w));
+    for (int64_t i0 = tid; i0 < n4; i0 += stride * kUnroll) {
+        float4 x[kUnroll], y[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            x[u] = y[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (i < n4) {
+                x[u] = ld_stream_f4(a + 4 * i);
+                y[u] = ld_stream_f4(b + 4 * i);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            if (i0 + u * stride < n4) {
+                acc += expf(fabsf(x[u].x - y[u].x));
+                acc += expf(fabsf(x[u].y - y[u].y));
+                acc += expf(fabsf(x[u].z - y[u].z));
+                acc += expf(fabsf(x[u].w - y[u].w));
+            }
+        }
     }
     for (int64_t i = 4 * n4 + tid; i < n; i += stride) acc += expf(fabsf(a[i] - b[i]));
-    const double t = block_sum((double)acc);
+    const double t = block_sum_f(acc);
     if (threadIdx.x == 0) partial[blockIdx.x] = t;
 }
 
@@ -184,8 +234,9 @@ extern "C" jet_status jet_token_mult_prob_error_noalloc(const float *logp_train,
 // a = logp_train, b = logp_rollout, capped at `cap` when cap > 0 (the pages
 // give no constant), 0 outside the mask.  The metric is token-mult-prob-error
 // over the masked tokens.  Pass 1: four tokens per thread and step (16-byte
-// loads of a and b, one 4-byte load of the mask, a 16-byte store of w), FP32
-// sums per thread, FP64 per block; pass 2 adds the block partials in order.
+// loads of a and b, one 4-byte load of the mask, a 16-byte store of w; the
+// loads of kUnroll steps issued together), FP32 sums per thread, FP64 per
+// block; pass 2 adds the block partials in order.
 // ---------------------------------------------------------------------------
 
 namespace {
@@ -206,20 +257,36 @@ tmm_partial_kernel(const float *__restrict__ a, const float *__restrict__ b,
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     const int64_t n4 = n >> 2;
-    for (int64_t i = tid; i < n4; i += stride) {
-        const float4 x = ld_stream_f4(a + 4 * i);
-        const float4 y = ld_stream_f4(b + 4 * i);
-        const uint32_t m4 = mask ? *reinterpret_cast<const uint32_t *>(mask + 4 * i) : 0x01010101u;
-        const float d[4] = {x.x - y.x, x.y - y.y, x.z - y.z, x.w - y.w};
-        float wv[4];
+    for (int64_t i0 = tid; i0 < n4; i0 += stride * kUnroll) {
+        float4 x[kUnroll], y[kUnroll];
+        uint32_t m4[kUnroll];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const bool on = ((m4 >> (8 * j)) & 0xFFu) != 0u;
-            wv[j] = on ? is_weight(d[j], cap) : 0.0f;
-            acc += on ? expf(fabsf(d[j])) : 0.0f;
-            cnt += on ? 1 : 0;
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            x[u] = y[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            m4[u] = 0u;
+            if (i < n4) {
+                x[u] = ld_stream_f4(a + 4 * i);
+                y[u] = ld_stream_f4(b + 4 * i);
+                m4[u] = mask ? *reinterpret_cast<const uint32_t *>(mask + 4 * i) : 0x01010101u;
+            }
         }
-        if (w) *reinterpret_cast<float4 *>(w + 4 * i) = make_float4(wv[0], wv[1], wv[2], wv[3]);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t i = i0 + u * stride;
+            if (i >= n4) continue;
+            const float d[4] = {x[u].x - y[u].x, x[u].y - y[u].y, x[u].z - y[u].z,
+                                x[u].w - y[u].w};
+            float wv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool on = ((m4[u] >> (8 * j)) & 0xFFu) != 0u;
+                wv[j] = on ? is_weight(d[j], cap) : 0.0f;
+                acc += on ? expf(fabsf(d[j])) : 0.0f;
+                cnt += on ? 1 : 0;
+            }
+            if (w) *reinterpret_cast<float4 *>(w + 4 * i) = make_float4(wv[0], wv[1], wv[2], wv[3]);
+        }
     }
     for (int64_t i = 4 * n4 + tid; i < n; i += stride) {
         const bool on = mask == nullptr || mask[i] != 0;
@@ -228,12 +295,11 @@ tmm_partial_kernel(const float *__restrict__ a, const float *__restrict__ b,
         acc += on ? expf(fabsf(d)) : 0.0f;
         cnt += on ? 1 : 0;
     }
-    const double t = block_sum((double)acc);
-    __syncthreads();  // block_sum's shared scratch is reused below
-    const double c = block_sum((double)cnt);
+    const double t = block_sum_f(acc);
+    const long long c = block_count(cnt);
     if (threadIdx.x == 0) {
         partial[2 * blockIdx.x] = t;
-        partial[2 * blockIdx.x + 1] = c;
+        partial[2 * blockIdx.x + 1] = (double)c;
     }
 }
 
@@ -264,7 +330,9 @@ namespace {
 // threads striding over the sequence's tokens four at a time (all loads of a
 // step issued before use); exp|a-b| of a step's four tokens summed in FP32,
 // the steps in FP64; the block's sums combined in a fixed order
-// (deterministic).
+// (deterministic).  Measured slower: 512 or 1024 threads per block, or 8 or
+// 16 tokens per step (fewer blocks fit, and the sequences, most of them
+// short, take more rounds).
 constexpr int kSeqUnroll = 4;
 
 __global__ void __launch_bounds__(kThreads)
@@ -302,11 +370,10 @@ tms_kernel(const float *__restrict__ a, const float *__restrict__ b,
             }
             sum += (double)part;
         }
-        const double t = block_sum(sum);
-        __syncthreads();  // block_sum's shared scratch is reused below
-        const double c = block_sum((double)cnt);
+        const double t = block_sum_f((float)sum);
+        const long long c = block_count(cnt);
         if (threadIdx.x == 0) {
-            out[s] = c > 0.0 ? (float)(t / c) : __int_as_float(0x7fc00000);
+            out[s] = c > 0 ? (float)(t / (double)c) : __int_as_float(0x7fc00000);
             if (count) count[s] = (int64_t)c;
         }
         __syncthreads();  // before the next sequence reuses the scratch
