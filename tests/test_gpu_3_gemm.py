@@ -202,9 +202,14 @@ def test_fwd_persistent_many_tiles(jet):
             nrows=48)
 
 
-@pytest.mark.parametrize("name,N,K", [("kv", 1024, 4096), ("down", 4096, 14336)])
+@pytest.mark.parametrize("name,N,K", [("kv", 1024, 4096), ("down", 4096, 14336),
+                                      ("q", 4096, 4096), ("gate", 14336, 4096)])
 @pytest.mark.parametrize("M", [1, 64, 256, 385, 2048])
 def test_fwd_rollout_shapes(jet, name, N, K, M):
+    # every split plan appears: 128-wide ranges on six stages (q and down
+    # at 64 rows, down at 256) and on four (kv; q at 256), 256-wide ranges
+    # (gate at 64 rows; q and down at 385), no split on the CTA-pair kernel
+    # (gate at 256 and 385 rows; everything at 2048)
     run_fwd(jet, wl.activations(M, K, seed=M, config=2), wl.weights(N, K, seed=N, config=2),
             nrows=24)
 
