@@ -29,8 +29,9 @@
 //              thread for 800-1500 cycles); otherwise idle.
 //              Warpgroup 0 (warps 0-3) gives registers back
 //              (setmaxnreg 72) so that the epilogue warpgroups can hold their
-//              accumulators (setmaxnreg 200): 128*72 + 256*200 <= 384 * 168,
-//              the allocation the block is launched with.
+//              accumulators and three TMEM load buffers (setmaxnreg 216):
+//              128*72 + 256*216 = 384 * 168, the allocation the block is
+//              launched with.
 //   warps 4-11 promotion/epilogue: two warpgroups split the tile's columns;
 //              each thread owns one output row (its TMEM lane) and BN/2 FP32
 //              accumulators, loads each slice from TMEM, applies the scales,
@@ -91,7 +92,7 @@ constexpr int kMaxGroups = 384;  // one expert per thread of the unit-count scan
 constexpr int kThreads = 384;
 static_assert(kMaxGroups <= kThreads, "the unit-count scan takes one expert per thread");
 constexpr uint32_t kRegsControl = 72;    // warpgroup 0 after setmaxnreg
-constexpr uint32_t kRegsEpilogue = 200;  // warpgroups 1-2 after setmaxnreg
+constexpr uint32_t kRegsEpilogue = 216;  // warpgroups 1-2 after setmaxnreg
 static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr int BM = 128;  // output rows per tile (TMEM lanes)
@@ -655,18 +656,26 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * BN + ch * H;
-                uint32_t p0[16], p1[16];
-                tmem_ld16(taddr, p0);
+                // Three 16-column buffers: a wait (which covers every TMEM
+                // load of the thread) comes every second chunk, after two
+                // chunks of arithmetic, instead of after each one.
+                uint32_t pb[3][16];
+                tmem_ld16(taddr, pb[0]);
+                if (NCH > 1) tmem_ld16(taddr + 16, pb[1]);
+                tmem_ld_wait(pb[0]);
+                if (NCH > 1) tmem_ld_pin(pb[1]);
                 if (BASE != kWgrad) {
                     const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
                     for (int c = 0; c < NCH; c += 2) {
-                        tmem_ld_wait(p0);
-                        tmem_ld16(taddr + (c + 1) * 16, p1);
-                        promote16(acc, c * 8, p0, sc2);
-                        tmem_ld_wait(p1);
-                        if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
-                        promote16(acc, (c + 1) * 8, p1, sc2);
+                        if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, pb[(c + 2) % 3]);
+                        promote16(acc, c * 8, pb[c % 3], sc2);
+                        if (c + 3 < NCH) tmem_ld16(taddr + (c + 3) * 16, pb[c % 3]);
+                        promote16(acc, (c + 1) * 8, pb[(c + 1) % 3], sc2);
+                        if (c + 2 < NCH) {
+                            tmem_ld_wait(pb[(c + 2) % 3]);
+                            if (c + 3 < NCH) tmem_ld_pin(pb[c % 3]);
+                        }
                     }
                 } else {
                     // Column scales are loaded one chunk ahead of their use so
@@ -677,14 +686,16 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     load_cs(csa, cs);
 #pragma unroll
                     for (int c = 0; c < NCH; c += 2) {
+                        if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, pb[(c + 2) % 3]);
                         load_cs(csb, cs + (c + 1) * 16);
-                        tmem_ld_wait(p0);
-                        tmem_ld16(taddr + (c + 1) * 16, p1);
-                        promote16_cols(acc, c * 8, p0, rs2, csa);
+                        promote16_cols(acc, c * 8, pb[c % 3], rs2, csa);
+                        if (c + 3 < NCH) tmem_ld16(taddr + (c + 3) * 16, pb[c % 3]);
                         if (c + 2 < NCH) load_cs(csa, cs + (c + 2) * 16);
-                        tmem_ld_wait(p1);
-                        if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
-                        promote16_cols(acc, (c + 1) * 8, p1, rs2, csb);
+                        promote16_cols(acc, (c + 1) * 8, pb[(c + 1) % 3], rs2, csb);
+                        if (c + 2 < NCH) {
+                            tmem_ld_wait(pb[(c + 2) % 3]);
+                            if (c + 3 < NCH) tmem_ld_pin(pb[c % 3]);
+                        }
                     }
                 }
                 tc_fence_before();

@@ -383,6 +383,17 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
                  : "memory");
 }
 
+// After a tmem_ld_wait (which waits for all of the thread's TMEM loads):
+// orders every use of a second load's registers after it.
+__device__ __forceinline__ void tmem_ld_pin(uint32_t (&r)[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), the fixed 0b001 at bits 46..48, base
 // offset 0, and the swizzle mode in bits 61..63 (2 = 128-byte swizzle).
