@@ -148,6 +148,24 @@ def test_dgrad_small_rows_split_contraction(jet, M, N, K):
               nrows=None if M * K <= 16 * 4096 else 8)
 
 
+@pytest.mark.parametrize("kind,M,N,K", [
+    ("fwd", 50, 384, 8192),     # 128-wide ranges on six stages, ragged rows, 3 column tiles
+    ("fwd", 200, 4096, 8192),   # six stages over two row tiles, the second ragged
+    ("fwd", 129, 640, 8192),    # four stages, one row past the first tile
+    ("dgrad", 50, 8192, 384),   # DGrad (C = K = 384) on six stages
+])
+def test_split_contraction_plans(jet, kind, M, N, K):
+    """Decode-sized products on every kind of split kernel, ragged in rows
+    and in column tiles, against the oracle on sampled rows."""
+    assert jet.workspace_bytes("gemm_fp8_" + kind, M, N, K) > 0
+    if kind == "fwd":
+        run_fwd(jet, wl.activations(M, K, seed=M + K, config=2),
+                wl.weights(N, K, seed=N + K, config=2), nrows=24)
+    else:
+        run_dgrad(jet, wl.grad_output(M, N, seed=M + N, config=3),
+                  wl.weights(N, K, seed=K + 1, config=3), nrows=24)
+
+
 def test_split_contraction_deterministic_and_workspace_agnostic(jet):
     """Same bits on repeated calls, whatever the workspace held before."""
     M, N, K = 16, 1024, 4096
