@@ -314,7 +314,11 @@ class RolloutStep:
     """Forward only (rollout): the 4 distinct inputs quantized 1x128 (the
     attention and MLP inputs through the fused RMSNorm quantizer) and the 7
     forward GEMMs of the 8B layer at M tokens; the weights are quantized once
-    beforehand (per weight sync) and not timed."""
+    beforehand (per weight sync) and not timed.  The products of one input
+    (q, k, v; gate, up) are independent and run on their own streams, forked
+    from and joined back into the step's stream, as an inference engine
+    issues them: at decode sizes each product's launch, pipeline fill and
+    split reduction then overlap the others' weight streams."""
 
     def __init__(self, M: int, device, seed: int = 0):
         import torch
@@ -342,6 +346,7 @@ class RolloutStep:
                              "y": e((M, c.N), torch.bfloat16),
                              "ws": e((nws,), torch.uint8) if nws else None})
         torch.cuda.synchronize()
+        self.streams = [torch.cuda.Stream(device=device) for _ in range(3)]
         self.flops = sum(2 * M * c.N * c.K for c in self.cases)
         gemm_bytes = sum(M * c.K + c.N * c.K + 4 * (M * c.K // 128 + c.N * c.K // 16384)
                          + 2 * M * c.N for c in self.cases)
@@ -358,6 +363,7 @@ class RolloutStep:
         self.config = {"workload": f"rollout8b_M{M}", "tokens": M,
                        "linears": [(c.name, c.N, c.K) for c in self.cases],
                        "gemm_tflop_per_step": round(self.flops / 1e12, 6),
+                       "concurrency": "q, k, v on three streams and gate, up on two",
                        "l2": "weights (218 M codes) > 129 MB L2; activations may stay in L2"}
 
     def calls(self):
@@ -369,11 +375,30 @@ class RolloutStep:
             else:
                 out.append(("quant_act_1x128", lambda v=v: j.jet_quant_act_1x128(v["x"], v["q"], v["s"]),
                             key))
+        # one call per input: its products forked onto the side streams
+        groups = {}
         for L in self.lin:
-            v = self.inputs[L["case"].key]
-            out.append(("gemm_fp8_fwd", lambda L=L, v=v: j.jet_gemm_fp8_fwd(
-                v["q"], v["s"], L["qw"], L["sw"], L["y"], ws=L["ws"]), L["case"].name))
+            groups.setdefault(L["case"].key, []).append(L)
+        for key, lins in groups.items():
+            v = self.inputs[key]
+            fns = [lambda L=L, v=v: j.jet_gemm_fp8_fwd(v["q"], v["s"], L["qw"], L["sw"], L["y"],
+                                                      ws=L["ws"]) for L in lins]
+            name = "+".join(L["case"].name for L in lins)
+            out.append(("gemm_fp8_fwd", fns[0] if len(fns) == 1 else self._fork(fns), name))
         return out
+
+    def _fork(self, fns):
+        import torch
+
+        def run():
+            cur = torch.cuda.current_stream()
+            for st, f in zip(self.streams, fns):
+                st.wait_stream(cur)
+                with torch.cuda.stream(st):
+                    f()
+            for st in self.streams[:len(fns)]:
+                cur.wait_stream(st)
+        return run
 
     def host_io(self):
         import torch
