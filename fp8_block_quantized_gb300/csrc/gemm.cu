@@ -29,7 +29,8 @@
 //              thread for 800-1500 cycles); otherwise idle.
 //              Warpgroup 0 (warps 0-3) gives registers back
 //              (setmaxnreg 72) so that the epilogue warpgroups can hold their
-//              accumulators and three TMEM load buffers (setmaxnreg 216):
+//              accumulators and three TMEM load buffers (setmaxnreg 216;
+//              200 and two buffers for the grouped products):
 //              128*72 + 256*216 = 384 * 168, the allocation the block is
 //              launched with.
 //   warps 4-11 promotion/epilogue: two warpgroups split the tile's columns;
@@ -93,7 +94,11 @@ constexpr int kThreads = 384;
 static_assert(kMaxGroups <= kThreads, "the unit-count scan takes one expert per thread");
 constexpr uint32_t kRegsControl = 72;    // warpgroup 0 after setmaxnreg
 constexpr uint32_t kRegsEpilogue = 216;  // warpgroups 1-2 after setmaxnreg
-static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168,
+// the grouped products, whose expert tables already take registers, keep
+// 200 and two TMEM load buffers: at 216 their kernels spilled
+constexpr uint32_t kRegsEpilogueGrouped = 200;
+static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= kThreads * 168 &&
+                  128 * kRegsControl + 256 * kRegsEpilogueGrouped <= kThreads * 168,
               "register split exceeds the launch allocation");
 constexpr int BM = 128;  // output rows per tile (TMEM lanes)
 constexpr int BK = 128;  // contraction slice = one scale block
@@ -605,7 +610,7 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (lane == 0) bulk_wait_group0();  // every store complete before exit
         }
     } else {
-        reg_alloc<kRegsEpilogue>();
+        reg_alloc<kGrp ? kRegsEpilogueGrouped : kRegsEpilogue>();
         // ----------------------------------------- promotion and epilogue
         constexpr int H = CF::kHalf;
         constexpr int NCH = H / 16;
@@ -656,45 +661,80 @@ gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * BN + ch * H;
-                // Three 16-column buffers: a wait (which covers every TMEM
-                // load of the thread) comes every second chunk, after two
-                // chunks of arithmetic, instead of after each one.
-                uint32_t pb[3][16];
-                tmem_ld16(taddr, pb[0]);
-                if (NCH > 1) tmem_ld16(taddr + 16, pb[1]);
-                tmem_ld_wait(pb[0]);
-                if (NCH > 1) tmem_ld_pin(pb[1]);
-                if (BASE != kWgrad) {
-                    const float2 sc2 = make_float2(sc, sc);
-#pragma unroll
-                    for (int c = 0; c < NCH; c += 2) {
-                        if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, pb[(c + 2) % 3]);
-                        promote16(acc, c * 8, pb[c % 3], sc2);
-                        if (c + 3 < NCH) tmem_ld16(taddr + (c + 3) * 16, pb[c % 3]);
-                        promote16(acc, (c + 1) * 8, pb[(c + 1) % 3], sc2);
-                        if (c + 2 < NCH) {
-                            tmem_ld_wait(pb[(c + 2) % 3]);
-                            if (c + 3 < NCH) tmem_ld_pin(pb[c % 3]);
+                if constexpr (!kGrp) {
+                    // Three 16-column buffers: a wait (which covers every TMEM
+                    // load of the thread) comes every second chunk, after two
+                    // chunks of arithmetic, instead of after each one.
+                    uint32_t pb[3][16];
+                    tmem_ld16(taddr, pb[0]);
+                    if (NCH > 1) tmem_ld16(taddr + 16, pb[1]);
+                    tmem_ld_wait(pb[0]);
+                    if (NCH > 1) tmem_ld_pin(pb[1]);
+                    if (BASE != kWgrad) {
+                        const float2 sc2 = make_float2(sc, sc);
+    #pragma unroll
+                        for (int c = 0; c < NCH; c += 2) {
+                            if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, pb[(c + 2) % 3]);
+                            promote16(acc, c * 8, pb[c % 3], sc2);
+                            if (c + 3 < NCH) tmem_ld16(taddr + (c + 3) * 16, pb[c % 3]);
+                            promote16(acc, (c + 1) * 8, pb[(c + 1) % 3], sc2);
+                            if (c + 2 < NCH) {
+                                tmem_ld_wait(pb[(c + 2) % 3]);
+                                if (c + 3 < NCH) tmem_ld_pin(pb[c % 3]);
+                            }
+                        }
+                    } else {
+                        // Column scales are loaded one chunk ahead of their use so
+                        // that shared-memory latency overlaps the previous chunk.
+                        const float *cs = scol + ch * H;
+                        const float2 rs2 = make_float2(rs, rs);
+                        float4 csa[4], csb[4];
+                        load_cs(csa, cs);
+    #pragma unroll
+                        for (int c = 0; c < NCH; c += 2) {
+                            if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, pb[(c + 2) % 3]);
+                            load_cs(csb, cs + (c + 1) * 16);
+                            promote16_cols(acc, c * 8, pb[c % 3], rs2, csa);
+                            if (c + 3 < NCH) tmem_ld16(taddr + (c + 3) * 16, pb[c % 3]);
+                            if (c + 2 < NCH) load_cs(csa, cs + (c + 2) * 16);
+                            promote16_cols(acc, (c + 1) * 8, pb[(c + 1) % 3], rs2, csb);
+                            if (c + 2 < NCH) {
+                                tmem_ld_wait(pb[(c + 2) % 3]);
+                                if (c + 3 < NCH) tmem_ld_pin(pb[c % 3]);
+                            }
                         }
                     }
                 } else {
-                    // Column scales are loaded one chunk ahead of their use so
-                    // that shared-memory latency overlaps the previous chunk.
-                    const float *cs = scol + ch * H;
-                    const float2 rs2 = make_float2(rs, rs);
-                    float4 csa[4], csb[4];
-                    load_cs(csa, cs);
+                    // The grouped products keep two buffers and a wait per
+                    // chunk (their register budget has no room for a third).
+                    uint32_t p0[16], p1[16];
+                    tmem_ld16(taddr, p0);
+                    if (BASE != kWgrad) {
+                        const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-                    for (int c = 0; c < NCH; c += 2) {
-                        if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, pb[(c + 2) % 3]);
-                        load_cs(csb, cs + (c + 1) * 16);
-                        promote16_cols(acc, c * 8, pb[c % 3], rs2, csa);
-                        if (c + 3 < NCH) tmem_ld16(taddr + (c + 3) * 16, pb[c % 3]);
-                        if (c + 2 < NCH) load_cs(csa, cs + (c + 2) * 16);
-                        promote16_cols(acc, (c + 1) * 8, pb[(c + 1) % 3], rs2, csb);
-                        if (c + 2 < NCH) {
-                            tmem_ld_wait(pb[(c + 2) % 3]);
-                            if (c + 3 < NCH) tmem_ld_pin(pb[c % 3]);
+                        for (int c = 0; c < NCH; c += 2) {
+                            tmem_ld_wait(p0);
+                            tmem_ld16(taddr + (c + 1) * 16, p1);
+                            promote16(acc, c * 8, p0, sc2);
+                            tmem_ld_wait(p1);
+                            if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
+                            promote16(acc, (c + 1) * 8, p1, sc2);
+                        }
+                    } else {
+                        const float *cs = scol + ch * H;
+                        const float2 rs2 = make_float2(rs, rs);
+                        float4 csa[4], csb[4];
+                        load_cs(csa, cs);
+#pragma unroll
+                        for (int c = 0; c < NCH; c += 2) {
+                            load_cs(csb, cs + (c + 1) * 16);
+                            tmem_ld_wait(p0);
+                            tmem_ld16(taddr + (c + 1) * 16, p1);
+                            promote16_cols(acc, c * 8, p0, rs2, csa);
+                            if (c + 2 < NCH) load_cs(csa, cs + (c + 2) * 16);
+                            tmem_ld_wait(p1);
+                            if (c + 2 < NCH) tmem_ld16(taddr + (c + 2) * 16, p0);
+                            promote16_cols(acc, (c + 1) * 8, p1, rs2, csb);
                         }
                     }
                 }
