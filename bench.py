@@ -310,6 +310,22 @@ class LayerStep:
         return nbytes(self.h_in), nbytes(self.h_out)
 
 
+def fork_calls(streams, fns):
+    """One call that runs independent thunks on their own streams, forked from
+    and joined back into the current stream (captured as such in a graph)."""
+    import torch
+
+    def run():
+        cur = torch.cuda.current_stream()
+        for st, f in zip(streams, fns):
+            st.wait_stream(cur)
+            with torch.cuda.stream(st):
+                f()
+        for st in streams[:len(fns)]:
+            cur.wait_stream(st)
+    return run
+
+
 class RolloutStep:
     """Forward only (rollout): the 4 distinct inputs quantized 1x128 (the
     attention and MLP inputs through the fused RMSNorm quantizer) and the 7
@@ -384,21 +400,9 @@ class RolloutStep:
             fns = [lambda L=L, v=v: j.jet_gemm_fp8_fwd(v["q"], v["s"], L["qw"], L["sw"], L["y"],
                                                       ws=L["ws"]) for L in lins]
             name = "+".join(L["case"].name for L in lins)
-            out.append(("gemm_fp8_fwd", fns[0] if len(fns) == 1 else self._fork(fns), name))
+            out.append(("gemm_fp8_fwd", fns[0] if len(fns) == 1 else fork_calls(self.streams, fns),
+                        name))
         return out
-
-    def _fork(self, fns):
-        import torch
-
-        def run():
-            cur = torch.cuda.current_stream()
-            for st, f in zip(self.streams, fns):
-                st.wait_stream(cur)
-                with torch.cuda.stream(st):
-                    f()
-            for st in self.streams[:len(fns)]:
-                cur.wait_stream(st)
-        return run
 
     def host_io(self):
         import torch
@@ -441,15 +445,22 @@ class SyncStep:
         self.bytes = sum(self.work.values())
         self.flops = 0
         self.launches_per_step = len(self.w) + 1
+        self.streams = [torch.cuda.Stream(device=device) for _ in range(3)]
         self.primary = ("GB/s", self.bytes)
         self.config = {"workload": "sync8b_32layers", "parameters": params,
+                       "concurrency": "weights three at a time on their own streams",
                        "activation": [16384, 14336],
                        "l2": "no flush: 21 GB of weights and codes per step"}
 
     def calls(self):
+        # the weights are independent: three at a time on their own streams
         j = self.jet
-        out = [("quant_w_128x128", lambda t=t: j.jet_quant_w_128x128(t["w"], t["q"], t["s"]),
-                t["name"].split(".")[1]) for t in self.w]
+        out = []
+        for i in range(0, len(self.w), len(self.streams)):
+            ts = self.w[i:i + len(self.streams)]
+            fns = [lambda t=t: j.jet_quant_w_128x128(t["w"], t["q"], t["s"]) for t in ts]
+            out.append(("quant_w_128x128", fork_calls(self.streams, fns),
+                        "+".join(t["name"] for t in ts)))
         out.append(("quant_act_1x128", lambda: j.jet_quant_act_1x128(self.x, self.xq, self.xs),
                     "x16384x14336"))
         return out
@@ -687,15 +698,18 @@ class KvCacheStep:
         self.flops = 0
         self.launches_per_step = 6   # a calibration is two kernels
         self.primary = ("GB/s", self.bytes)
+        self.streams = [torch.cuda.Stream(device=device) for _ in range(2)]
         self.config = {"workload": f"kvcache8b_T{T}", "tokens": T, "kv_heads": H, "head_dim": D,
-                       "cache_slots": S, "l2": "no flush: 268 MB of K/V read per step > 129 MB L2"}
+                       "cache_slots": S, "concurrency": "K and V on two streams",
+                       "l2": "no flush: 268 MB of K/V read per step > 129 MB L2"}
 
     def calls(self):
         j = self.jet
-        return [("kv_calibrate", lambda: j.jet_kv_calibrate(self.k, self.sk), "k"),
-                ("kv_calibrate", lambda: j.jet_kv_calibrate(self.v, self.sv), "v"),
-                ("kv_cache_write", lambda: j.jet_kv_cache_write(self.k, self.sk, self.slots, self.ck), "k"),
-                ("kv_cache_write", lambda: j.jet_kv_cache_write(self.v, self.sv, self.slots, self.cv), "v")]
+        cal = [lambda: j.jet_kv_calibrate(self.k, self.sk), lambda: j.jet_kv_calibrate(self.v, self.sv)]
+        wr = [lambda: j.jet_kv_cache_write(self.k, self.sk, self.slots, self.ck),
+              lambda: j.jet_kv_cache_write(self.v, self.sv, self.slots, self.cv)]
+        return [("kv_calibrate", fork_calls(self.streams, cal), "k+v"),
+                ("kv_cache_write", fork_calls(self.streams, wr), "k+v")]
 
     def host_io(self):
         import torch
